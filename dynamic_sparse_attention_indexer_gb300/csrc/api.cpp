@@ -1,0 +1,434 @@
+// The C ABI: argument checks, workspace layout, launch order.
+//
+// Nothing here touches the GPU before every argument has been checked, so the
+// error paths run (and are tested) on machines without a GPU.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/dsa.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_msg;
+
+dsa_status fail(dsa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_msg = buf;
+  return s;
+}
+
+dsa_status cuda_fail(const char* where, cudaError_t e) {
+  return fail(DSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Kernel attributes are set once per device, before the first launch there.
+dsa_status ensure_setup() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  if (dev < 0 || dev >= 64) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return DSA_OK;
+  if ((e = dsa::setup_index_kernels()) != cudaSuccess) return cuda_fail("setup (index kernels)", e);
+  if ((e = dsa::setup_topk_kernels()) != cudaSuccess) return cuda_fail("setup (top-k kernels)", e);
+  if ((e = dsa::setup_attn_kernels()) != cudaSuccess) return cuda_fail("setup (attention kernels)", e);
+  done[dev] = true;
+  return DSA_OK;
+}
+
+dsa_status check_kv(const dsa_paged_kv* kv, dsa::KV* out) {
+  if (!kv) return fail(DSA_ERR_INVALID_ARG, "kv descriptor is NULL");
+  if (kv->block_size != 64) return fail(DSA_ERR_UNSUPPORTED, "block_size %d: only 64 is supported", kv->block_size);
+  if (kv->head_dim != 128) return fail(DSA_ERR_UNSUPPORTED, "head_dim %d: only 128 is supported", kv->head_dim);
+  if (kv->idx_dim != 64) return fail(DSA_ERR_UNSUPPORTED, "idx_dim %d: only 64 is supported", kv->idx_dim);
+  if (kv->num_blocks < 1 || kv->num_kv_heads < 1 || kv->batch < 1 || kv->max_blocks_per_seq < 1)
+    return fail(DSA_ERR_INVALID_ARG, "num_blocks, num_kv_heads, batch and max_blocks_per_seq must be >= 1");
+  if ((int64_t)kv->num_blocks * kv->num_kv_heads * 64 >= (int64_t(1) << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 64 must stay below 2^31 rows");
+  if ((int64_t)kv->max_blocks_per_seq * 64 >= (int64_t(1) << 30))
+    return fail(DSA_ERR_UNSUPPORTED, "max_blocks_per_seq * 64 must stay below 2^30 positions");
+  if (kv->max_context_len < 1 || (int64_t)kv->max_context_len > (int64_t)kv->max_blocks_per_seq * 64)
+    return fail(DSA_ERR_INVALID_ARG, "max_context_len %d outside [1, max_blocks_per_seq * 64]", kv->max_context_len);
+  if (!kv->k_cache || !kv->v_cache || !kv->idx_cache || !kv->block_table || !kv->context_lens)
+    return fail(DSA_ERR_INVALID_ARG, "a cache, block_table or context_lens pointer is NULL");
+  if (!aligned16(kv->k_cache) || !aligned16(kv->v_cache) || !aligned16(kv->idx_cache))
+    return fail(DSA_ERR_INVALID_ARG, "k_cache, v_cache and idx_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(kv->block_table) & 3u) || (reinterpret_cast<uintptr_t>(kv->context_lens) & 3u))
+    return fail(DSA_ERR_INVALID_ARG, "block_table and context_lens must be 4-byte aligned");
+  out->k_cache = kv->k_cache;
+  out->v_cache = kv->v_cache;
+  out->idx_cache = kv->idx_cache;
+  out->block_table = kv->block_table;
+  out->context_lens = kv->context_lens;
+  out->num_blocks = kv->num_blocks;
+  out->hkv = kv->num_kv_heads;
+  out->max_blocks = kv->max_blocks_per_seq;
+  out->batch = kv->batch;
+  out->max_ctx = kv->max_context_len;
+  return DSA_OK;
+}
+
+dsa_status check_qs(const dsa_query_set* qs, const dsa::KV& kv, dsa::QS* out) {
+  if (!qs) return fail(DSA_ERR_INVALID_ARG, "query set is NULL");
+  if (qs->mode == DSA_MODE_DECODE) {
+    if (qs->n_q != kv.batch) return fail(DSA_ERR_INVALID_ARG, "decode: n_q (%d) must equal batch (%d)", qs->n_q, kv.batch);
+  } else if (qs->mode == DSA_MODE_PREFILL) {
+    if (qs->n_q < 1) return fail(DSA_ERR_INVALID_ARG, "prefill: n_q must be >= 1");
+    if (qs->seq < 0 || qs->seq >= kv.batch) return fail(DSA_ERR_INVALID_ARG, "prefill: seq %d outside [0, batch)", qs->seq);
+    if (qs->pos0 < 0 || (int64_t)qs->pos0 + qs->n_q > (int64_t)kv.max_blocks * 64)
+      return fail(DSA_ERR_INVALID_ARG, "prefill: positions [pos0, pos0 + n_q) must lie in [0, max_blocks_per_seq * 64)");
+  } else {
+    return fail(DSA_ERR_INVALID_ARG, "unknown query-set mode %d", qs->mode);
+  }
+  out->mode = qs->mode;
+  out->n_q = qs->n_q;
+  out->seq = qs->seq;
+  out->pos0 = qs->pos0;
+  return DSA_OK;
+}
+
+// Largest position + 1 any query of the set can see.
+int64_t positions_needed(const dsa::KV& kv, const dsa::QS& qs) {
+  return qs.mode == DSA_MODE_DECODE ? (int64_t)kv.max_ctx : (int64_t)qs.pos0 + qs.n_q;
+}
+
+dsa_status check_scores(const int32_t* scores, int32_t ld, const dsa::KV& kv, const dsa::QS& qs) {
+  if (!scores || !aligned16(scores)) return fail(DSA_ERR_INVALID_ARG, "scores must be non-NULL and 16-byte aligned");
+  if (ld % 4 != 0) return fail(DSA_ERR_INVALID_ARG, "ld (%d) must be a multiple of 4", ld);
+  if ((int64_t)ld < positions_needed(kv, qs))
+    return fail(DSA_ERR_INVALID_ARG, "ld (%d) below the largest position + 1 (%lld)", ld,
+                (long long)positions_needed(kv, qs));
+  return DSA_OK;
+}
+
+struct Layout {
+  size_t hist = 0, ticket_h = 0, ticket_c = 0, sel = 0, chunk_cnt = 0, run_pos = 0, run_info = 0;
+  size_t part_o = 0, part_ml = 0;
+  size_t sel_end = 0, total = 0;
+  int n_chunks = 0, rps = 0, max_splits = 1;
+};
+
+Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = up256(off + bytes);
+    return o;
+  };
+  if (qs.mode == DSA_MODE_DECODE) {
+    const size_t B = (size_t)kv.batch;
+    L.n_chunks = (kv.max_ctx + dsa::kCompactChunk - 1) / dsa::kCompactChunk;
+    L.hist = take(B * 8192 * 4);
+    L.ticket_h = take(B * 4);
+    L.ticket_c = take(B * 4);
+    L.sel = take(B * 16);
+    L.chunk_cnt = take(B * L.n_chunks * 8);
+    L.run_pos = take(B * L.n_chunks * dsa::kCompactChunk * 4);
+    L.run_info = take(B * L.n_chunks * dsa::kCompactChunk * 4);
+  }
+  L.sel_end = off;
+  const int64_t rows_max = (int64_t)prefix + k;
+  dsa::attn_split_plan(qs.n_q * kv.hkv, (int)rows_max, qs.mode, &L.rps, &L.max_splits);
+  if (L.max_splits > 1) {
+    const size_t heads = (size_t)qs.n_q * hq;
+    L.part_o = take(heads * L.max_splits * 128 * 4);
+    L.part_ml = take(heads * L.max_splits * 8);
+  }
+  L.total = off;
+  return L;
+}
+
+dsa::SelState sel_state(const Layout& L, void* ws) {
+  char* w = static_cast<char*>(ws);
+  dsa::SelState s;
+  s.hist = reinterpret_cast<int*>(w + L.hist);
+  s.ticket_h = reinterpret_cast<int*>(w + L.ticket_h);
+  s.ticket_c = reinterpret_cast<int*>(w + L.ticket_c);
+  s.sel = reinterpret_cast<int4*>(w + L.sel);
+  s.chunk_cnt = reinterpret_cast<int2*>(w + L.chunk_cnt);
+  s.run_pos = reinterpret_cast<int*>(w + L.run_pos);
+  s.run_info = reinterpret_cast<int*>(w + L.run_info);
+  s.n_chunks = L.n_chunks;
+  return s;
+}
+
+dsa_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return DSA_OK;
+  if (!ws || !aligned16(ws)) return fail(DSA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned");
+  if (ws_bytes < need) return fail(DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return DSA_OK;
+}
+
+dsa_status check_k_prefix(int32_t k, int32_t prefix) {
+  if (k < 1) return fail(DSA_ERR_INVALID_ARG, "k (%d) must be >= 1", k);
+  if (prefix < 0) return fail(DSA_ERR_INVALID_ARG, "prefix_len (%d) must be >= 0", prefix);
+  if ((int64_t)prefix + k > (int64_t(1) << 24)) return fail(DSA_ERR_UNSUPPORTED, "prefix_len + k above 2^24");
+  return DSA_OK;
+}
+
+dsa_status check_heads(int32_t hq, const dsa::KV& kv) {
+  if (hq < 1 || hq % kv.hkv != 0)
+    return fail(DSA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", hq, kv.hkv);
+  if (hq / kv.hkv > 16) return fail(DSA_ERR_UNSUPPORTED, "GQA group %d > 16 query heads per KV head", hq / kv.hkv);
+  return DSA_OK;
+}
+
+#define DSA_TRY(x)                  \
+  do {                              \
+    const dsa_status s_ = (x);      \
+    if (s_ != DSA_OK) return s_;    \
+  } while (0)
+
+#define DSA_CUDA(where, x)                        \
+  do {                                            \
+    const cudaError_t e_ = (x);                   \
+    if (e_ != cudaSuccess) return cuda_fail(where, e_); \
+  } while (0)
+
+dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const void* q, int32_t hq,
+                     const int32_t* idx, const int32_t* n_sel, int32_t k, int32_t prefix, float scale, void* out,
+                     int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  DSA_TRY(check_qs(qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  DSA_TRY(check_heads(hq, kv));
+  if (!q || !aligned16(q) || !out || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  if (out_dtype != DSA_OUT_BF16 && out_dtype != DSA_OUT_F32)
+    return fail(DSA_ERR_INVALID_ARG, "out_dtype %d is neither DSA_OUT_BF16 nor DSA_OUT_F32", out_dtype);
+  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  const Layout L = layout(kv, qs, k, hq, prefix);
+  DSA_TRY(check_ws(ws, ws_bytes, L.max_splits > 1 ? L.total : 0));
+  DSA_TRY(ensure_setup());
+  dsa::AttnArgs a;
+  a.kv = kv;
+  a.qs = qs;
+  a.q = q;
+  a.hq = hq;
+  a.idx = idx;
+  a.n_sel = n_sel;
+  a.k = k;
+  a.prefix = prefix;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.rows_per_split = L.rps;
+  a.max_splits = L.max_splits;
+  a.ws.part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + L.part_o);
+  a.ws.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + L.part_ml);
+  DSA_CUDA("sparse attention launch", dsa::launch_sparse_attn(a, stream));
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_OOM: return "DSA_ERR_OOM";
+    case DSA_ERR_BAD_BLOCK_TABLE: return "DSA_ERR_BAD_BLOCK_TABLE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+const char* dsa_last_error_message(void) { return g_msg.c_str(); }
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+dsa_status dsa_check_device_status(cudaStream_t stream, int32_t* code) {
+  if (!code) return fail(DSA_ERR_INVALID_ARG, "code is NULL");
+  int c = 0;
+  DSA_CUDA("status (index)", dsa::read_clear_status_index(&c, stream));
+  DSA_CUDA("status (top-k)", dsa::read_clear_status_topk(&c, stream));
+  DSA_CUDA("status (attention)", dsa::read_clear_status_attn(&c, stream));
+  DSA_CUDA("status (cache)", dsa::read_clear_status_misc(&c, stream));
+  *code = c;
+  return DSA_OK;
+}
+
+size_t dsa_workspace_size(int32_t op, const dsa_paged_kv* kv_, const dsa_query_set* qs_, int32_t k, int32_t hq,
+                          int32_t prefix) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  if (check_kv(kv_, &kv) != DSA_OK || check_qs(qs_, kv, &qs) != DSA_OK) return 0;
+  if (op == DSA_OP_INDEX_SCORES) return 0;
+  if (check_k_prefix(k, prefix) != DSA_OK || check_heads(hq, kv) != DSA_OK) return 0;
+  const Layout L = layout(kv, qs, k, hq, prefix);
+  switch (op) {
+    case DSA_OP_TOPK_SELECT: return L.sel_end;
+    case DSA_OP_SPARSE_ATTN:
+    case DSA_OP_DECODE_STEP:
+    case DSA_OP_PREFILL_STEP: return L.max_splits > 1 ? L.total : L.sel_end;
+    default: fail(DSA_ERR_INVALID_ARG, "unknown op %d", op); return 0;
+  }
+}
+
+dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (ws_bytes == 0) return DSA_OK;
+  if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
+  DSA_CUDA("workspace memset", cudaMemsetAsync(ws, 0, ws_bytes, stream));
+  return DSA_OK;
+}
+
+dsa_status dsa_kv_write(const dsa_paged_kv* kv_, const int32_t* slots, int32_t ntok, const void* k, const void* v,
+                        const int8_t* idx_k, cudaStream_t stream) {
+  dsa::KV kv{};
+  DSA_TRY(check_kv(kv_, &kv));
+  if (ntok < 0) return fail(DSA_ERR_INVALID_ARG, "ntok (%d) must be >= 0", ntok);
+  if (ntok == 0) return DSA_OK;
+  if (!slots || !k || !v || !idx_k) return fail(DSA_ERR_INVALID_ARG, "slot_mapping, k, v and idx_k must be non-NULL");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(idx_k))
+    return fail(DSA_ERR_INVALID_ARG, "k, v and idx_k must be 16-byte aligned");
+  DSA_TRY(ensure_setup());
+  DSA_CUDA("kv_write launch", dsa::launch_kv_write(kv, slots, ntok, k, v, idx_k, stream));
+  return DSA_OK;
+}
+
+dsa_status dsa_index_scores(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const int8_t* q_idx, int32_t prefix,
+                            int32_t* scores, int32_t ld, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  dsa::KV kv{};
+  dsa::QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  DSA_TRY(check_qs(qs_, kv, &qs));
+  if (prefix < 0) return fail(DSA_ERR_INVALID_ARG, "prefix_len (%d) must be >= 0", prefix);
+  if (!q_idx || !aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx must be non-NULL and 16-byte aligned");
+  DSA_TRY(check_scores(scores, ld, kv, qs));
+  DSA_TRY(ensure_setup());
+  if (qs.mode == DSA_MODE_DECODE)
+    DSA_CUDA("index_scores launch", dsa::launch_decode_index(kv, q_idx, prefix, scores, ld, nullptr, 0, stream));
+  else
+    DSA_CUDA("index_scores launch", dsa::launch_prefill_index(kv, qs, q_idx, prefix, scores, ld, stream));
+  return DSA_OK;
+}
+
+dsa_status dsa_topk_select(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const int32_t* scores, int32_t ld,
+                           int32_t prefix, int32_t k, int32_t* idx, int32_t* n_sel, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  DSA_TRY(check_qs(qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  DSA_TRY(check_scores(scores, ld, kv, qs));
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  if (qs.mode == DSA_MODE_DECODE) {
+    const Layout L = layout(kv, qs, k, kv.hkv, prefix);
+    DSA_TRY(check_ws(ws, ws_bytes, L.sel_end));
+    DSA_TRY(ensure_setup());
+    const dsa::SelState s = sel_state(L, ws);
+    DSA_CUDA("top-k histogram launch", dsa::launch_decode_hist(kv, scores, ld, prefix, k, s, stream));
+    DSA_CUDA("top-k compaction launch", dsa::launch_decode_compact(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
+  } else {
+    DSA_TRY(ensure_setup());
+    DSA_CUDA("top-k launch", dsa::launch_prefill_topk(qs, scores, ld, prefix, k, idx, n_sel, stream));
+  }
+  return DSA_OK;
+}
+
+dsa_status dsa_kv_gather(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const int32_t* idx, const int32_t* n_sel,
+                         int32_t k, int32_t prefix, void* k_out, void* v_out, cudaStream_t stream) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  DSA_TRY(check_qs(qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  if (!k_out || !v_out || !aligned16(k_out) || !aligned16(v_out))
+    return fail(DSA_ERR_INVALID_ARG, "k_out and v_out must be non-NULL and 16-byte aligned");
+  DSA_TRY(ensure_setup());
+  DSA_CUDA("kv_gather launch", dsa::launch_kv_gather(kv, qs, idx, n_sel, k, prefix, k_out, v_out, stream));
+  return DSA_OK;
+}
+
+dsa_status dsa_sparse_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t hq, const int32_t* idx,
+                                  const int32_t* n_sel, int32_t k, int32_t prefix, float scale, void* out,
+                                  int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!kv) return fail(DSA_ERR_INVALID_ARG, "kv descriptor is NULL");
+  dsa_query_set qs = {DSA_MODE_DECODE, kv->batch, 0, 0};
+  return attn_impl(kv, &qs, q, hq, idx, n_sel, k, prefix, scale, out, out_dtype, lse, ws, ws_bytes, stream);
+}
+
+dsa_status dsa_sparse_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q, int32_t hq,
+                                   const int32_t* idx, const int32_t* n_sel, int32_t k, int32_t prefix, float scale,
+                                   void* out, int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream) {
+  if (qs && qs->mode != DSA_MODE_PREFILL)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_prefill needs a DSA_MODE_PREFILL query set");
+  return attn_impl(kv, qs, q, hq, idx, n_sel, k, prefix, scale, out, out_dtype, lse, ws, ws_bytes, stream);
+}
+
+dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t* q_idx, int32_t hq, int32_t prefix,
+                           int32_t k, float scale, int32_t* scores, int32_t ld, int32_t* idx, int32_t* n_sel,
+                           void* out, int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  dsa::KV kv{};
+  DSA_TRY(check_kv(kv_, &kv));
+  const dsa_query_set qs_ = {DSA_MODE_DECODE, kv.batch, 0, 0};
+  dsa::QS qs{};
+  DSA_TRY(check_qs(&qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  DSA_TRY(check_heads(hq, kv));
+  if (!q_idx || !aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx must be non-NULL and 16-byte aligned");
+  DSA_TRY(check_scores(scores, ld, kv, qs));
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  if (!q || !aligned16(q) || !out || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  if (out_dtype != DSA_OUT_BF16 && out_dtype != DSA_OUT_F32)
+    return fail(DSA_ERR_INVALID_ARG, "out_dtype %d is neither DSA_OUT_BF16 nor DSA_OUT_F32", out_dtype);
+  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  const Layout L = layout(kv, qs, k, hq, prefix);
+  DSA_TRY(check_ws(ws, ws_bytes, L.total));
+  DSA_TRY(ensure_setup());
+  const dsa::SelState s = sel_state(L, ws);
+  DSA_CUDA("decode index launch", dsa::launch_decode_index(kv, q_idx, prefix, scores, ld, &s, k, stream));
+  DSA_CUDA("decode compaction launch", dsa::launch_decode_compact(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
+  dsa::AttnArgs a;
+  a.kv = kv;
+  a.qs = qs;
+  a.q = q;
+  a.hq = hq;
+  a.idx = idx;
+  a.n_sel = n_sel;
+  a.k = k;
+  a.prefix = prefix;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.rows_per_split = L.rps;
+  a.max_splits = L.max_splits;
+  a.ws.part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + L.part_o);
+  a.ws.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + L.part_ml);
+  DSA_CUDA("decode attention launch", dsa::launch_sparse_attn(a, stream));
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Host-side interface between the C ABI (api.cpp) and the kernel files.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dsa {
+
+struct KV {
+  const void* k_cache;
+  const void* v_cache;
+  const int8_t* idx_cache;
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  int num_blocks, hkv, max_blocks, batch, max_ctx;
+};
+
+struct QS {
+  int mode, n_q, seq, pos0;
+};
+
+// Per-query selection state kept in the workspace between the histogram and
+// the compaction kernels (decode: one entry per sequence).
+struct SelState {
+  int* hist;        // [n][kHistBins]   zero between calls
+  int* ticket_h;    // [n]              zero between calls
+  int* ticket_c;    // [n]              zero between calls
+  int4* sel;        // [n]              {mode, tau, n_gt, quota}
+  int2* chunk_cnt;  // [n][n_chunks]    {gt, eq} per compaction chunk
+  int* run_pos;     // [n][n_chunks * kCompactChunk]
+  int* run_info;    // same: (tie rank << 1) | is_tie
+  int n_chunks;     // compaction chunks per sequence
+};
+
+constexpr int kCompactChunk = 2048;   // positions per compaction CTA
+constexpr int kCompactThreads = 256;  // 8 positions per thread
+
+struct AttnWs {
+  float* part_o;    // [n_q][hq][max_splits][128]
+  float2* part_ml;  // [n_q][hq][max_splits]  (max in log2 units, sum)
+};
+
+struct AttnArgs {
+  KV kv;
+  QS qs;
+  const void* q;
+  int hq;
+  const int32_t* idx;
+  const int32_t* n_sel;
+  int k, prefix;
+  float scale;
+  void* out;
+  int out_dtype;
+  float* lse;
+  int rows_per_split, max_splits;  // max_splits == 1: no combine pass
+  AttnWs ws;
+};
+
+// Grid planning shared by the workspace sizing and the launches.
+int decode_index_chunk(int batch, int max_ctx);  // positions per indexer CTA
+void attn_split_plan(int pairs, int rows_max, int mode, int* rows_per_split, int* max_splits);
+
+// Kernel launches (return the launch error, if any).
+cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, int* scores, int ld,
+                                const SelState* sel, int k, cudaStream_t st);
+cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
+                               const SelState& sel, cudaStream_t st);
+cudaError_t launch_decode_compact(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
+                                  const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st);
+cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix,
+                                 int* scores, int ld, cudaStream_t st);
+cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k,
+                                int32_t* idx, int32_t* n_sel, cudaStream_t st);
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
+                            const int8_t* idx_k, cudaStream_t st);
+cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, const int32_t* n_sel, int k,
+                             int prefix, void* k_out, void* v_out, cudaStream_t st);
+
+// One-time per-device kernel attribute setup (dynamic shared memory limits).
+cudaError_t setup_index_kernels();
+cudaError_t setup_topk_kernels();
+cudaError_t setup_attn_kernels();
+
+// Device status words, one per kernel file: each reads its word into *code
+// (if *code is still 0) and clears it.
+cudaError_t read_clear_status_index(int* code, cudaStream_t st);
+cudaError_t read_clear_status_topk(int* code, cudaStream_t st);
+cudaError_t read_clear_status_attn(int* code, cudaStream_t st);
+cudaError_t read_clear_status_misc(int* code, cudaStream_t st);
+
+}  // namespace dsa

@@ -1,0 +1,207 @@
+/*
+ * dsa.h — C ABI of the dynamic sparse attention (DSA) hot path on GB300 (sm_103a).
+ *
+ * The method is the one dissected in the article
+ *   "国产AI芯片完成前沿大模型Day-0适配:稀疏注意力与混合精度推理全解析" (ruibaoantu.com),
+ * section 2; "§2.x" below refers to its sub-sections:
+ *   §2.1  index selection on the GPU: a tensor-core similarity score of the query
+ *         against every key, then a reduction that picks the top-k positions;
+ *   §2.2  the KV cache in fixed blocks (e.g. 64 x 128) of consecutive positions, and
+ *         a batched gather of the selected rows ("gather first, then compute");
+ *   §2.3  separate prefill (fused select + gather + attention, with the next block
+ *         prefetched while the current one is computed) and decode (bandwidth-bound:
+ *         load only the active KV, asynchronously) paths;
+ *   §2.4  a KV block allocator ("KDA"), and the vision-token prefix that is always
+ *         attended in full and never takes part in index selection.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE memory owned by the caller; the library never
+ *     allocates, frees or keeps them.  Host pointers are marked "host".
+ *   - Hot-path calls are asynchronous on the given stream, never synchronise and
+ *     never allocate; they may be captured in a CUDA graph once the library has
+ *     made one call on the device (its first call sets kernel attributes).
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED / DSA_ERR_WORKSPACE
+ *     and dsa_last_error_message() (per host thread) says which.
+ *   - Kernels never trap.  A block-table entry outside [0, num_blocks) read on the
+ *     device, or a bounded wait that ran out, sets a device status word and the
+ *     kernel goes on with block 0 in its place (outputs then undefined);
+ *     dsa_check_device_status() reads and clears it.
+ *   - Launch failures return DSA_ERR_CUDA with the CUDA error text.
+ *
+ * Data layout (row-major, innermost last)
+ *   k_cache, v_cache : bf16 [num_blocks][num_kv_heads][64][128]   one 64 x 128 block per head
+ *   idx_cache        : int8 [num_blocks][64][64]                   indexer key per position
+ *   block_table      : int32 [batch][max_blocks_per_seq]           position t of sequence b is
+ *                      row t % 64 of block block_table[b][t / 64]
+ *   context_lens     : int32 [batch]                               tokens in the cache per sequence
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size or range        */
+  DSA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. head_dim != 128)  */
+  DSA_ERR_OOM = 3,              /* block allocator has too few free blocks           */
+  DSA_ERR_BAD_BLOCK_TABLE = 4,  /* device saw a block id outside [0, num_blocks)     */
+  DSA_ERR_CUDA = 5,             /* a CUDA call failed                                */
+  DSA_ERR_TIMEOUT = 6,          /* a bounded device wait ran out                     */
+  DSA_ERR_WORKSPACE = 7         /* workspace pointer null/misaligned or too small    */
+} dsa_status;
+
+enum { DSA_MODE_DECODE = 0, DSA_MODE_PREFILL = 1 };
+enum { DSA_OUT_BF16 = 0, DSA_OUT_F32 = 1 };
+enum {
+  DSA_OP_INDEX_SCORES = 0, DSA_OP_TOPK_SELECT = 1, DSA_OP_SPARSE_ATTN = 2,
+  DSA_OP_DECODE_STEP = 3, DSA_OP_PREFILL_STEP = 4
+};
+
+/* The paged KV cache, described (not owned).  Fixed sizes: block_size 64,
+ * head_dim 128, idx_dim 64 (others return DSA_ERR_UNSUPPORTED).
+ * max_context_len is a HOST upper bound of context_lens[] (decode) used to size
+ * grids; it must be <= max_blocks_per_seq * 64. */
+typedef struct dsa_paged_kv {
+  void* k_cache;
+  void* v_cache;
+  int8_t* idx_cache;
+  const int32_t* block_table;
+  const int32_t* context_lens;
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t idx_dim;
+  int32_t max_blocks_per_seq;
+  int32_t batch;
+  int32_t max_context_len;
+} dsa_paged_kv;
+
+/* Which query tokens a call serves.
+ *   DSA_MODE_DECODE : n_q == batch; query b is the newest token of sequence b, at
+ *                     position context_lens[b] - 1 (its K, V and indexer key are
+ *                     already in the cache).  seq and pos0 are ignored.
+ *   DSA_MODE_PREFILL: n_q query tokens of sequence `seq` at positions pos0 .. pos0+n_q-1;
+ *                     query i sees keys [0, pos0 + i] (causal, also inside the prefix);
+ *                     pos0 + n_q <= max_blocks_per_seq * 64. */
+typedef struct dsa_query_set {
+  int32_t mode;
+  int32_t n_q;
+  int32_t seq;
+  int32_t pos0;
+} dsa_query_set;
+
+/* ---------------------------------------------------------------- status --- */
+const char* dsa_status_string(dsa_status s);
+/* Message of the last failed call on this host thread ("" if none). */
+const char* dsa_last_error_message(void);
+int32_t dsa_abi_version(void);
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  *code (host) receives DSA_OK, DSA_ERR_BAD_BLOCK_TABLE or
+ * DSA_ERR_TIMEOUT; the return value reports CUDA failures only. */
+dsa_status dsa_check_device_status(cudaStream_t stream, int32_t* code);
+
+/* --------------------------------------------- block allocator (§2.4 KDA) --- */
+/* Host-side free list of block ids [0, num_blocks).  Not thread-safe. */
+typedef struct dsa_kv_alloc dsa_kv_alloc;
+dsa_status dsa_kv_alloc_create(int32_t num_blocks, dsa_kv_alloc** out /* host */);
+/* Takes n free ids into out_ids (host, n entries), lowest ids first.  If fewer
+ * than n are free it takes none and returns DSA_ERR_OOM. */
+dsa_status dsa_kv_alloc_blocks(dsa_kv_alloc* a, int32_t n, int32_t* out_ids);
+/* Returns ids to the free list.  An id out of range or already free makes the
+ * whole call fail with DSA_ERR_INVALID_ARG and change nothing. */
+dsa_status dsa_kv_free_blocks(dsa_kv_alloc* a, const int32_t* ids /* host */, int32_t n);
+int32_t dsa_kv_alloc_num_free(const dsa_kv_alloc* a);
+void dsa_kv_alloc_destroy(dsa_kv_alloc* a);
+
+/* ------------------------------------------------------- cache write (§2.2) --- */
+/* Scatters ntok new tokens into the cache: token j goes to slot slot_mapping[j]
+ * = block_id * 64 + row.  k, v: bf16 [ntok][num_kv_heads][128]; idx_k: int8
+ * [ntok][64].  Slots outside the pool set DSA_ERR_BAD_BLOCK_TABLE on the device
+ * and are skipped. */
+dsa_status dsa_kv_write(const dsa_paged_kv* kv, const int32_t* slot_mapping, int32_t ntok,
+                        const void* k, const void* v, const int8_t* idx_k, cudaStream_t stream);
+
+/* -------------------------------------------------------------- workspace --- */
+/* Bytes of workspace an op needs for these sizes (0 when it needs none, or on
+ * invalid arguments: see the message).  A buffer sized for DSA_OP_DECODE_STEP
+ * serves every decode op, one sized for DSA_OP_PREFILL_STEP every prefill op.
+ * index_scores never needs one; pass NULL / 0 there. */
+size_t dsa_workspace_size(int32_t op, const dsa_paged_kv* kv, const dsa_query_set* qs,
+                          int32_t k, int32_t num_q_heads, int32_t prefix_len);
+/* Zeroes a workspace (async on `stream`).  Required once before first use: the
+ * ops leave the counters they use at zero again when they finish, so a
+ * workspace stays ready; after a failed or interrupted call, call it again. */
+dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ----------------------------------------------------- step 1: scores (§2.1) --- */
+/* scores[i * ld + t] = sum_d q_idx[i][d] * key(t)[d] (exact int32) for every
+ * candidate key t of query i: t in [prefix_len, pos_i].  Other entries of the row
+ * are left untouched.  q_idx: int8 [n_q][64].  ld >= max position + 1, ld % 4 == 0,
+ * scores 16-byte aligned. */
+dsa_status dsa_index_scores(const dsa_paged_kv* kv, const dsa_query_set* qs, const int8_t* q_idx,
+                            int32_t prefix_len, int32_t* scores, int32_t ld,
+                            void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* --------------------------------------------------- step 2: top-k (§2.1, §2.4) --- */
+/* For each query: the k candidates t in [prefix_len, pos_i] with the largest
+ * scores, ties to the lower position (all candidates when there are <= k).
+ * idx: int32 [n_q][k], ascending positions, padded with -1; n_sel: int32 [n_q].
+ * The prefix [0, min(prefix_len, pos_i + 1)) is not part of idx: it is always
+ * attended (the attention calls add it). */
+dsa_status dsa_topk_select(const dsa_paged_kv* kv, const dsa_query_set* qs, const int32_t* scores,
+                           int32_t ld, int32_t prefix_len, int32_t k, int32_t* idx, int32_t* n_sel,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* --------------------------------------------------- step 3: gather (§2.2) --- */
+/* Copies the attended rows of each query into contiguous buffers
+ * k_out, v_out: bf16 [n_q][num_kv_heads][prefix_len + k][128].  Row r of query i:
+ * r < P_i = min(prefix_len, pos_i + 1) is position r; P_i <= r < P_i + n_sel[i] is
+ * position idx[i][r - P_i]; later rows are zero. */
+dsa_status dsa_kv_gather(const dsa_paged_kv* kv, const dsa_query_set* qs, const int32_t* idx,
+                         const int32_t* n_sel, int32_t k, int32_t prefix_len,
+                         void* k_out, void* v_out, cudaStream_t stream);
+
+/* ------------------------------------------------ step 4: attention (§2.3) --- */
+/* out[i][h] = softmax(softmax_scale * q[i][h] . K_S^T) V_S over the attended set
+ * S_i = prefix part + idx[i][0 .. n_sel[i]), read straight from the paged cache
+ * (the gather is fused).  Query head h uses KV head h / (num_q_heads / num_kv_heads).
+ * q: bf16 [n_q][num_q_heads][128]; out: [n_q][num_q_heads][128] bf16 (RNE) or f32;
+ * lse: f32 [n_q][num_q_heads] natural-log softmax denominator (may be NULL).
+ * Decode form (query set = decode of the whole batch): */
+dsa_status dsa_sparse_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t num_q_heads,
+                                  const int32_t* idx, const int32_t* n_sel, int32_t k,
+                                  int32_t prefix_len, float softmax_scale, void* out,
+                                  int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+/* Prefill form: the queries of `qs` (mode DSA_MODE_PREFILL). */
+dsa_status dsa_sparse_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q,
+                                   int32_t num_q_heads, const int32_t* idx, const int32_t* n_sel,
+                                   int32_t k, int32_t prefix_len, float softmax_scale, void* out,
+                                   int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+
+/* ---------------------------------------------------- fused decode step --- */
+/* Steps 1-4 for one decode token per sequence, in one call: scores (written to
+ * `scores`, [batch][ld]), top-k (idx, n_sel) and attention (out, lse), with the
+ * score histogram built while scoring.  Same argument rules as the single steps. */
+dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* q_idx,
+                           int32_t num_q_heads, int32_t prefix_len, int32_t k,
+                           float softmax_scale, int32_t* scores, int32_t ld, int32_t* idx,
+                           int32_t* n_sel, void* out, int32_t out_dtype, float* lse,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H */

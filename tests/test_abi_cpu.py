@@ -1,0 +1,157 @@
+"""The C-ABI library on the host: it loads, exports every symbol the header
+declares, and rejects bad arguments before touching the GPU (no GPU here)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+DSA_OK, INVALID, UNSUPPORTED, OOM, BAD_BLOCK, CUDA, TIMEOUT, WORKSPACE = range(8)
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(dsa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for n in ("dsa_index_scores", "dsa_topk_select", "dsa_kv_gather", "dsa_sparse_attn_decode",
+              "dsa_sparse_attn_prefill", "dsa_kv_write", "dsa_kv_alloc_create", "dsa_decode_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from dynamic_sparse_attention_indexer_gb300 import _abi
+    names = declared_functions()
+    assert len(names) >= 18
+    raw = C.CDLL(_abi._build.LIB)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in dsa.h but not exported"
+        assert n in _abi.SIGNATURES, f"{n} has no ctypes signature"
+    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_status_string(OOM) == b"DSA_ERR_OOM"
+
+
+def test_block_allocator(lib):
+    from dynamic_sparse_attention_indexer_gb300 import BlockAllocator, DSAError
+    a = BlockAllocator(10)
+    assert a.num_free == 10
+    assert a.alloc(3) == [0, 1, 2]
+    assert a.alloc(2) == [3, 4]
+    a.free([1, 3])
+    assert a.num_free == 7
+    assert a.alloc(3) == [1, 3, 5]          # lowest free ids first
+    with pytest.raises(DSAError) as e:
+        a.alloc(6)                            # 4 free: OOM takes none
+    assert e.value.status == OOM and a.num_free == 4
+    with pytest.raises(DSAError):
+        a.free([2, 2])                        # duplicate in one call
+    with pytest.raises(DSAError):
+        a.free([9])                           # never allocated
+    with pytest.raises(DSAError):
+        a.free([0, 42])                       # out of range: nothing freed
+    assert a.num_free == 4
+    a.free([0, 1, 2, 3, 4, 5])
+    assert a.num_free == 10
+
+
+def _kv(**over):
+    from dynamic_sparse_attention_indexer_gb300 import _abi
+    f = dict(k_cache=0x10000, v_cache=0x20000, idx_cache=0x30000, block_table=0x40000, context_lens=0x50000,
+             num_blocks=16, block_size=64, num_kv_heads=2, head_dim=128, idx_dim=64, max_blocks_per_seq=8,
+             batch=2, max_context_len=500)
+    f.update(over)
+    return _abi.PagedKV(**f)
+
+
+def _qs(mode=0, n_q=2, seq=0, pos0=0):
+    from dynamic_sparse_attention_indexer_gb300 import _abi
+    return _abi.QuerySet(mode, n_q, seq, pos0)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(block_size=32), UNSUPPORTED),
+    (dict(head_dim=64), UNSUPPORTED),
+    (dict(idx_dim=128), UNSUPPORTED),
+    (dict(k_cache=0), INVALID),
+    (dict(v_cache=0x20008), INVALID),         # misaligned
+    (dict(max_context_len=8 * 64 + 1), INVALID),
+    (dict(batch=0), INVALID),
+])
+def test_index_scores_rejects_bad_cache(lib, over, status):
+    kv = _kv(**over)
+    qs = _qs(n_q=kv.batch)
+    st = lib.dsa_index_scores(C.byref(kv), C.byref(qs), 0x60000, 0, 0x70000, 512, None, 0, None)
+    assert st == status
+    assert lib.dsa_last_error_message()
+
+
+def test_argument_checks(lib):
+    kv = _kv()
+    qs = _qs()
+    # ld too small, ld not a multiple of 4, misaligned scores
+    assert lib.dsa_index_scores(C.byref(kv), C.byref(qs), 0x60000, 0, 0x70000, 496, None, 0, None) == INVALID
+    assert lib.dsa_index_scores(C.byref(kv), C.byref(qs), 0x60000, 0, 0x70000, 514, None, 0, None) == INVALID
+    assert lib.dsa_index_scores(C.byref(kv), C.byref(qs), 0x60000, 0, 0x70004, 512, None, 0, None) == INVALID
+    # decode query set must cover the batch; prefill positions must fit the table
+    assert lib.dsa_index_scores(C.byref(kv), C.byref(_qs(n_q=3)), 0x60000, 0, 0x70000, 512, None, 0,
+                                None) == INVALID
+    assert lib.dsa_index_scores(C.byref(kv), C.byref(_qs(1, 100, 0, 500)), 0x60000, 0, 0x70000, 1024, None,
+                                0, None) == INVALID
+    assert lib.dsa_index_scores(C.byref(kv), C.byref(_qs(1, 10, 2, 0)), 0x60000, 0, 0x70000, 512, None, 0,
+                                None) == INVALID
+    # top-k: k >= 1, prefix >= 0, workspace large enough
+    args = (C.byref(kv), C.byref(qs), 0x70000, 512)
+    assert lib.dsa_topk_select(*args, 0, 0, 0x80000, 0x90000, 0xA0000, 1 << 30, None) == INVALID
+    assert lib.dsa_topk_select(*args, -1, 8, 0x80000, 0x90000, 0xA0000, 1 << 30, None) == INVALID
+    assert lib.dsa_topk_select(*args, 0, 8, 0x80000, 0x90000, None, 0, None) == WORKSPACE
+    assert lib.dsa_topk_select(*args, 0, 8, 0x80000, 0x90000, 0xA0000, 16, None) == WORKSPACE
+    # attention: heads must be a multiple of the KV heads, group <= 16, known out dtype
+    a = (C.byref(kv), 0x60000)
+    assert lib.dsa_sparse_attn_decode(*a, 3, 0x80000, 0x90000, 8, 0, 0.1, 0xB0000, 0, None, 0xA0000,
+                                      1 << 30, None) == INVALID
+    assert lib.dsa_sparse_attn_decode(*a, 34, 0x80000, 0x90000, 8, 0, 0.1, 0xB0000, 0, None, 0xA0000,
+                                      1 << 30, None) == UNSUPPORTED
+    assert lib.dsa_sparse_attn_decode(*a, 8, 0x80000, 0x90000, 8, 0, 0.1, 0xB0000, 7, None, 0xA0000,
+                                      1 << 30, None) == INVALID
+    assert lib.dsa_sparse_attn_decode(*a, 8, 0x80000, 0x90000, 8, 0, float("nan"), 0xB0000, 0, None,
+                                      0xA0000, 1 << 30, None) == INVALID
+    # prefill attention refuses a decode query set
+    assert lib.dsa_sparse_attn_prefill(C.byref(kv), C.byref(qs), 0x60000, 8, 0x80000, 0x90000, 8, 0, 0.1,
+                                       0xB0000, 0, None, None, 0, None) == INVALID
+    # kv_write: negative count, misaligned source
+    assert lib.dsa_kv_write(C.byref(kv), 0x1000, -1, 0x2000, 0x3000, 0x4000, None) == INVALID
+    assert lib.dsa_kv_write(C.byref(kv), 0x1000, 4, 0x2008, 0x3000, 0x4000, None) == INVALID
+    assert lib.dsa_kv_write(C.byref(kv), 0x1000, 0, 0x2008, 0x3000, 0x4000, None) == DSA_OK  # nothing to do
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    """With every argument valid the call reaches the CUDA runtime, which has
+    no device here: a DSA_ERR_CUDA status, never a crash or a host fallback."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    kv = _kv()
+    qs = _qs()
+    assert lib.dsa_index_scores(C.byref(kv), C.byref(qs), 0x60000, 0, 0x70000, 512, None, 0, None) == CUDA
+
+
+def test_workspace_sizes(lib):
+    kv = _kv()
+    qs = _qs()
+    size = lambda op, k=8, hq=8, p=0: lib.dsa_workspace_size(op, C.byref(kv), C.byref(qs), k, hq, p)
+    assert size(0) == 0                       # index_scores needs none
+    topk, step = size(1), size(3)
+    assert topk > 2 * 8192 * 4                # two per-sequence histograms at least
+    assert step >= topk and step == size(2)
+    # the 128K decode workload: 8 sequences, 64/8 heads, prefix 1024, k 2048
+    kv3 = _kv(num_blocks=16384, num_kv_heads=8, max_blocks_per_seq=2048, batch=8, max_context_len=131072)
+    qs3 = _qs(n_q=8)
+    s3 = lib.dsa_workspace_size(3, C.byref(kv3), C.byref(qs3), 2048, 64, 1024)
+    assert 8 * 131072 * 8 <= s3 < 64 << 20    # runs (2 x int32 per position) + partials, well under 64 MB
+    assert lib.dsa_workspace_size(3, C.byref(kv3), C.byref(qs3), 0, 64, 1024) == 0   # invalid k
