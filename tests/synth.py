@@ -149,8 +149,9 @@ def to_numpy(w: dict) -> dict:
     return out
 
 
-def small_spec(name="small", mode="decode", batch=3, lens=(700, 1500, 2113), prefix_len=64,
+def small_spec(name="small", mode="decode", batch=None, lens=(700, 1500, 2113), prefix_len=64,
                hq=16, hkv=2, k=256, **kw) -> Spec:
     """A workload the oracle finishes in seconds that still spans several
-    blocks, chunks and tiles, with a ragged tail."""
-    return Spec(name, mode, batch, tuple(lens), prefix_len, hq, hkv, k, **kw)
+    blocks, chunks and tiles, with a ragged tail (batch = len(lens))."""
+    assert batch is None or batch == len(lens)
+    return Spec(name, mode, len(lens), tuple(lens), prefix_len, hq, hkv, k, **kw)
