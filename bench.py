@@ -1,0 +1,399 @@
+"""DSA decode benchmark on GB300: tokens/s and achieved HBM bandwidth.
+
+One step = one full DSA decode step of one attention layer over the batch:
+indexer scores -> top-k (prefix forced in) -> fused gather + GQA attention,
+for the decode workload B=8, context 131072, prefix 1024, 64/8 heads,
+head_dim 128, int8 indexer dim 64, top-k 2048, 1% of K rows scaled x4.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Inputs are synthetic and seeded; they are resident in HBM before timing.
+Consecutive steps rotate over 4 independent KV caches ("layers", 17.6 GB in
+all), so no step finds its data in the 129 MB L2.  Multi-GPU runs (torchrun)
+give every rank its own batch (weak scaling, no collective on the data path).
+The reference arm (--impl reference) times the CPU oracle on a bounded sample
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+for _p in (ROOT, os.path.join(ROOT, "tests")):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
+
+CONFIG_ID = 3
+LAYERS = 4
+METRIC = "DSA decode tokens/s & achieved HBM GB/s (% of roofline) at 128K ctx, 1xGB300"
+
+
+# ------------------------------------------------------------ helpers ------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(spec, lens, n_sel):
+    """Bytes the method must move per step (HBM): non-prefix indexer keys and
+    their block-table entries, the indexer query, selected K and V rows (prefix
+    + selection, every KV head), Q, the output, and the index list."""
+    P, hkv, hq = spec.prefix_len, spec.num_kv_heads, spec.num_q_heads
+    idx_bytes = sum(max(0, L - P) * 64 + math.ceil(L / 64) * 4 for L in lens) + 64 * len(lens)
+    rows = sum(min(P, L) + int(n) for L, n in zip(lens, n_sel))
+    kv_bytes = rows * hkv * 2 * 128 * 2
+    qo_bytes = 2 * len(lens) * hq * 128 * 2 + len(lens) * hq * 4
+    sel_bytes = len(lens) * spec.k * 4
+    return {"indexer": idx_bytes, "attention": kv_bytes + qo_bytes + sel_bytes, "step":
+            idx_bytes + kv_bytes + qo_bytes + sel_bytes}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def reduce_over_ranks(values: dict, op: str):
+    """Max ("max") or sum ("sum") of scalar values over all ranks (no-op
+    without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return dict(values)
+    keys = sorted(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(values[k]) for k in keys], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return {k: float(v) for k, v in zip(keys, t.cpu().tolist())}
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------- oracle timing -----
+def oracle_sequence_inputs(w, b):
+    """Per-sequence CPU copies (not timed): indexer, K and V blocks of seq b."""
+    import numpy as np
+    import torch
+    L = int(w["context_lens"][b].item())
+    nblk = math.ceil(L / 64)
+    ids = w["block_table"][b, :nblk].long()
+    local_bt = np.arange(nblk, dtype=np.int64)
+    icache = w["idx_cache"].index_select(0, ids).cpu().numpy().astype(np.int64)
+    kc = w["k_cache"].index_select(0, ids).cpu().to(torch.float32).numpy()
+    vc = w["v_cache"].index_select(0, ids).cpu().to(torch.float32).numpy()
+    return {"q": w["q"][b].cpu().to(torch.float64).numpy(), "q_idx": w["q_idx"][b].cpu().numpy().astype(np.int64),
+            "idx_cache": icache, "k_cache": kc, "v_cache": vc, "bt": local_bt, "pos": L - 1}
+
+
+def time_oracle(seq_inputs, spec):
+    """Seconds the oracle takes for the given decode tokens (single thread)."""
+    import oracle.dsa_oracle as O
+    t0 = time.perf_counter()
+    for d in seq_inputs:
+        O.dsa_query(d["q"], d["q_idx"], d["k_cache"], d["v_cache"], d["idx_cache"], d["bt"], d["pos"],
+                    spec.prefix_len, spec.k, spec.num_kv_heads, 1.0 / math.sqrt(128))
+    return time.perf_counter() - t0
+
+
+def cpu_threads_used():
+    # numpy's BLAS is limited to one thread before numpy loads (see main); the
+    # int64 scoring and the sort are single threaded in numpy anyway.
+    return 1
+
+
+# --------------------------------------------------------------- arms ------
+def run_reference(args, rank, world):
+    """The CPU oracle, as it stands, on a bounded sample of the workload."""
+    import torch
+    import synth
+    if rank != 0:
+        return
+    spec = synth.CONFIGS[CONFIG_ID]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = synth.make_workload(spec, 1000 + CONFIG_ID, dev)
+    n = max(1, args.steps) + max(0, args.warmup)
+    inputs = [oracle_sequence_inputs(w, i % spec.batch) for i in range(min(n, spec.batch))]
+    del w
+    for i in range(args.warmup):
+        time_oracle([inputs[i % len(inputs)]], spec)
+    secs = 0.0
+    for i in range(args.steps):
+        secs += time_oracle([inputs[(args.warmup + i) % len(inputs)]], spec)
+    value = args.steps / secs
+    sample = f"{args.steps} decode tokens (one sequence each) of the workload, full oracle per token"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_block(spec),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads_used(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_block(spec):
+    return {"workload": spec.name, "batch": spec.batch, "context": 131072, "prefix": spec.prefix_len,
+            "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": 128, "idx_dim": 64,
+            "top_k": spec.k, "block_size": 64, "seed": 1000 + CONFIG_ID,
+            "l2": f"inputs larger than L2: steps rotate over {LAYERS} independent KV caches (no flush)"}
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import dynamic_sparse_attention_indexer_gb300 as dsa
+    import harness as H
+    import synth
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    spec = synth.CONFIGS[CONFIG_ID]
+    P, k, hq = spec.prefix_len, spec.k, spec.num_q_heads
+
+    # --- resident inputs: LAYERS independent caches; one query batch per layer
+    layers = []
+    for l in range(LAYERS):
+        w = synth.make_workload(spec, 1000 + CONFIG_ID + 7919 * l + 104729 * rank, dev)
+        kv = H.paged_kv(w)
+        B = kv.batch
+        ld = H.round4(w["max_context_len"])
+        bufs = {"scores": torch.empty((B, ld), dtype=torch.int32, device=dev),
+                "idx": torch.empty((B, k), dtype=torch.int32, device=dev),
+                "n_sel": torch.empty(B, dtype=torch.int32, device=dev),
+                "out": torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev),
+                "lse": torch.empty((B, hq), dtype=torch.float32, device=dev)}
+        ws = dsa.make_workspace(dsa.workspace_size(dsa.OP_DECODE_STEP, kv, dsa.decode_queries(kv), k, hq, P), dev)
+        layers.append((w, kv, bufs, ws))
+    lens = [int(x) for x in layers[0][0]["context_lens"].tolist()]
+    B = len(lens)
+
+    def step(l):
+        w, kv, b, ws = layers[l]
+        dsa.decode_step(kv, w["q"], w["q_idx"], P, k, b["scores"], b["idx"], b["n_sel"], b["out"], b["lse"], ws)
+
+    # eager warm-up (first call sets kernel attributes), then one graph per layer
+    for l in range(LAYERS):
+        step(l)
+    torch.cuda.synchronize()
+    assert dsa.check_device_status(dev) == 0
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for l in range(LAYERS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(l)
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % LAYERS].replay()
+    torch.cuda.synchronize()
+
+    # --- timed region: exactly K steps
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[(args.warmup + i) % LAYERS].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = clocks.stop()
+    local_ms = e0.elapsed_time(e1)
+    n_sel = [int(x) for x in layers[0][2]["n_sel"].tolist()]
+    assert dsa.check_device_status(dev) == 0
+
+    # --- per-call breakdown on the launching stream (same rotation, same K)
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        durations = []
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                a.record(stream)
+                fn(i % LAYERS)
+                b.record(stream)
+                b.synchronize()
+                durations.append(a.elapsed_time(b))
+        return durations
+
+    def attn_call(l):
+        w, kv, b, ws = layers[l]
+        dsa.sparse_attn_decode(kv, w["q"], b["idx"], b["n_sel"], k, P, b["out"], b["lse"], ws)
+
+    def index_call(l):
+        w, kv, b, ws = layers[l]
+        dsa.index_scores(kv, dsa.decode_queries(kv), w["q_idx"], P, b["scores"])
+
+    n_bd = max(8, min(args.steps, 200))
+    timed(attn_call, 4)
+    attn_ms = statistics.mean(timed(attn_call, n_bd))
+    index_ms = statistics.mean(timed(index_call, n_bd))
+    step(0)
+    torch.cuda.synchronize()
+
+    # --- end to end through the public API with host buffers
+    w0, kv0, b0, ws0 = layers[0]
+    q_host = [layers[l][0]["q"].cpu().pin_memory() for l in range(LAYERS)]
+    qi_host = [layers[l][0]["q_idx"].cpu().pin_memory() for l in range(LAYERS)]
+    out_host = torch.empty(b0["out"].shape, dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty(b0["lse"].shape, dtype=torch.float32).pin_memory()
+    n_e2e = max(8, min(args.steps, 500))
+
+    def e2e_step(i):
+        l = i % LAYERS
+        w, kv, b, ws = layers[l]
+        w["q"].copy_(q_host[l], non_blocking=True)
+        w["q_idx"].copy_(qi_host[l], non_blocking=True)
+        graphs[l].replay()
+        out_host.copy_(b["out"], non_blocking=True)
+        lse_host.copy_(b["lse"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            e2e_step(i)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            e2e_step(i)
+        e2e_s = time.perf_counter() - t0
+    h2d = q_host[0].numel() * 2 + qi_host[0].numel()
+    d2h = out_host.numel() * 2 + lse_host.numel() * 4
+
+    # --- aggregate over ranks (max time, summed tokens)
+    agg = reduce_over_ranks({"ms": local_ms, "e2e_s": e2e_s, "attn_ms": attn_ms, "index_ms": index_ms}, "max")
+    tokens = reduce_over_ranks({"tok": float(B * args.steps), "e2e_tok": float(B * n_e2e)}, "sum")
+
+    # --- CPU baseline (rank 0, N = 1 only): the oracle on a bounded sample
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_seq = min(args.cpu_sample, B)
+        inputs = [oracle_sequence_inputs(w0, b) for b in range(n_seq)]
+        secs = time_oracle(inputs, spec)
+        cpu = {"value": n_seq / secs, "unit": "tokens/s", "cores": cpu_threads_used(), "kind": "oracle",
+               "sample": f"{n_seq} of the {B} decode tokens of one step (full oracle per token), {secs:.1f} s"}
+
+    if rank != 0:
+        return
+    ab = algorithmic_bytes(spec, lens, n_sel)
+    peak, peak_kind = measured_peaks()
+    ms_step = agg["ms"] / args.steps
+    attn_gbs = ab["attention"] / (agg["attn_ms"] * 1e-3) / 1e9
+    step_gbs = ab["step"] / (ms_step * 1e-3) / 1e9
+    traffic = args.attn_traffic if args.attn_traffic > 0 else None
+    launches_per_step = 4  # indexer+histogram, compaction, attention, split combine
+    line = {
+        "metric": METRIC, "value": tokens["tok"] / (agg["ms"] * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(spec),
+        "hbm": {"step_bytes": ab["step"], "achieved_gbs": step_gbs, "peak_gbs": peak,
+                "frac": step_gbs / peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": "sparse_attn_kernel + attn_combine_kernel (dsa_sparse_attn_decode)",
+                     "bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
+                     "traffic": traffic, "algorithmic_bytes": ab["attention"], "ms": agg["attn_ms"],
+                     "peak_kind": peak_kind},
+        "indexer": {"ms": agg["index_ms"], "achieved_gbs": ab["indexer"] / (agg["index_ms"] * 1e-3) / 1e9},
+        "clocks": clock_info,
+        "e2e": {"value": tokens["e2e_tok"] / agg["e2e_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-traffic", type=float, default=0.0,
+                    help="DRAM bytes per attention launch from an ncu capture (0 = not measured)")
+    args = ap.parse_args()
+    assert args.warmup >= 0 and args.steps >= 1
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", init_method="env://")
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("MKL_NUM_THREADS", "1")
+    main()
