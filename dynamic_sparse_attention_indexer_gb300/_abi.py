@@ -47,6 +47,7 @@ SIGNATURES = {
                                         c_i32, c_p, c_p, C.c_size_t, c_p]),
     "dsa_decode_step": (c_i32, [PKV, c_p, c_p, c_i32, c_i32, c_i32, C.c_float, c_p, c_i32, c_p, c_p,
                                 c_p, c_i32, c_p, c_p, C.c_size_t, c_p]),
+    "dsa_topk_select_decode_noalloc": (c_i32, [PKV, c_p, c_i32, c_i32, c_i32, c_p, c_p, c_p]),
 }
 
 _LIB = None

@@ -242,6 +242,42 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
 
 }  // namespace
 
+namespace dsa {
+
+// Argument checks and scratch layout of a decode top-k, for entry points that
+// bring their own scratch (the allocation-free variant).  On success *st points
+// into `base`, *bytes is the scratch size and *clear_bytes the leading part
+// (histograms and counters) that must be zero when the call starts.
+dsa_status prepare_decode_topk(const dsa_paged_kv* kv_, const int32_t* scores, int32_t ld, int32_t prefix,
+                               int32_t k, const int32_t* idx, const int32_t* n_sel, KV* kv_out, size_t* bytes,
+                               size_t* clear_bytes) {
+  KV kv{};
+  QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  const dsa_query_set qs_ = {DSA_MODE_DECODE, kv.batch, 0, 0};
+  DSA_TRY(check_qs(&qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  DSA_TRY(check_scores(scores, ld, kv, qs));
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  const Layout L = layout(kv, qs, k, kv.hkv, prefix);
+  *kv_out = kv;
+  *bytes = L.sel_end;
+  *clear_bytes = L.sel;  // hist, ticket_h and ticket_c come first
+  return DSA_OK;
+}
+
+SelState decode_topk_state(const KV& kv, int32_t k, int32_t prefix, void* base) {
+  const dsa_query_set qs_ = {DSA_MODE_DECODE, kv.batch, 0, 0};
+  QS qs{qs_.mode, qs_.n_q, qs_.seq, qs_.pos0};
+  return sel_state(layout(kv, qs, k, kv.hkv, prefix), base);
+}
+
+dsa_status set_error(dsa_status s, const char* msg) { return fail(s, "%s", msg); }
+
+dsa_status setup_device() { return ensure_setup(); }
+
+}  // namespace dsa
+
 extern "C" {
 
 const char* dsa_status_string(dsa_status s) {

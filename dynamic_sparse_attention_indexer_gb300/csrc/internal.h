@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/dsa.h"
+
 namespace dsa {
 
 struct KV {
@@ -89,5 +91,13 @@ cudaError_t read_clear_status_index(int* code, cudaStream_t st);
 cudaError_t read_clear_status_topk(int* code, cudaStream_t st);
 cudaError_t read_clear_status_attn(int* code, cudaStream_t st);
 cudaError_t read_clear_status_misc(int* code, cudaStream_t st);
+
+// Used by the allocation-free top-k entry point (defined in api.cpp).
+dsa_status prepare_decode_topk(const dsa_paged_kv* kv, const int32_t* scores, int32_t ld, int32_t prefix,
+                               int32_t k, const int32_t* idx, const int32_t* n_sel, KV* kv_out, size_t* bytes,
+                               size_t* clear_bytes);
+SelState decode_topk_state(const KV& kv, int32_t k, int32_t prefix, void* base);
+dsa_status set_error(dsa_status s, const char* msg);
+dsa_status setup_device();
 
 }  // namespace dsa

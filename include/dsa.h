@@ -201,6 +201,31 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
                            int32_t* n_sel, void* out, int32_t out_dtype, float* lse,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------- decode top-k without scratch --- */
+/* The article has no counterpart to this call.  It is for callers that cannot
+ * allocate device memory: for example a plugin running inside a serving process
+ * whose device memory is all owned by the host framework's pool and which is
+ * handed no allocator, or a latency-critical path that cannot take cudaMalloc's
+ * implicit synchronisation and unbounded cost.  It returns exactly what
+ * dsa_topk_select returns in decode mode (query b = newest token of sequence
+ * b); the caller passes inputs and outputs only.  Its scratch is a static
+ * device array of DSA_TOPK_STATIC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library keeps until the process exits; the call makes no
+ * cudaMalloc, cudaFree or other allocating call.
+ *   - Scratch needed: about batch * (33 KB + 8 bytes * max_context_len); larger
+ *     sizes return DSA_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and sets kernel attributes: make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array, which keeps the last call's contents;
+ *     each call first zeroes the histograms and counters it relies on.  Calls
+ *     whose work overlaps on the GPU (other streams, other host threads) race
+ *     on the array and give wrong results: serialise them. */
+#define DSA_TOPK_STATIC_SCRATCH_BYTES (16u << 20)
+dsa_status dsa_topk_select_decode_noalloc(const dsa_paged_kv* kv, const int32_t* scores, int32_t ld,
+                                          int32_t prefix_len, int32_t k, int32_t* idx, int32_t* n_sel,
+                                          cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
