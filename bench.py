@@ -259,18 +259,27 @@ def run_gpu(args, rank, world, local_rank):
     n_sel = [int(x) for x in layers[0][2]["n_sel"].tolist()]
     assert dsa.check_device_status(dev) == 0
 
-    # --- per-call breakdown on the launching stream (same rotation, same K)
-    def timed(fn, n):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        durations = []
+    # --- per-call breakdown on the launching stream: each call is captured once
+    # per layer into a graph, replayed; time per launch = graph time / launches.
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            for i in range(n):
-                a.record(stream)
-                fn(i % LAYERS)
-                b.record(stream)
-                b.synchronize()
-                durations.append(a.elapsed_time(b))
-        return durations
+            with torch.cuda.graph(g, stream=stream):
+                for l in range(LAYERS):
+                    fn(l)
+        return g
+
+    def per_launch_ms(g, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / (reps * LAYERS)
 
     def attn_call(l):
         w, kv, b, ws = layers[l]
@@ -280,10 +289,9 @@ def run_gpu(args, rank, world, local_rank):
         w, kv, b, ws = layers[l]
         dsa.index_scores(kv, dsa.decode_queries(kv), w["q_idx"], P, b["scores"])
 
-    n_bd = max(8, min(args.steps, 200))
-    timed(attn_call, 4)
-    attn_ms = statistics.mean(timed(attn_call, n_bd))
-    index_ms = statistics.mean(timed(index_call, n_bd))
+    reps = max(8, min(args.steps // LAYERS, 250))
+    attn_ms = per_launch_ms(graph_of(attn_call), reps)
+    index_ms = per_launch_ms(graph_of(index_call), reps)
     step(0)
     torch.cuda.synchronize()
 
@@ -337,7 +345,7 @@ def run_gpu(args, rank, world, local_rank):
     attn_gbs = ab["attention"] / (agg["attn_ms"] * 1e-3) / 1e9
     step_gbs = ab["step"] / (ms_step * 1e-3) / 1e9
     traffic = args.attn_traffic if args.attn_traffic > 0 else None
-    launches_per_step = 4  # indexer+histogram, compaction, attention, split combine
+    launches_per_step = 3  # indexer + histogram, compaction, attention (splits merged in-kernel)
     line = {
         "metric": METRIC, "value": tokens["tok"] / (agg["ms"] * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -345,7 +353,7 @@ def run_gpu(args, rank, world, local_rank):
         "config": config_block(spec),
         "hbm": {"step_bytes": ab["step"], "achieved_gbs": step_gbs, "peak_gbs": peak,
                 "frac": step_gbs / peak, "peak_kind": peak_kind},
-        "roofline": {"kernel": "sparse_attn_kernel + attn_combine_kernel (dsa_sparse_attn_decode)",
+        "roofline": {"kernel": "sparse_attn_kernel (dsa_sparse_attn_decode, per launch in a graph)",
                      "bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                      "traffic": traffic, "algorithmic_bytes": ab["attention"], "ms": agg["attn_ms"],
                      "peak_kind": peak_kind},

@@ -87,6 +87,10 @@ dsa_status check_qs(const dsa_query_set* qs, const dsa::KV& kv, dsa::QS* out) {
   if (!qs) return fail(DSA_ERR_INVALID_ARG, "query set is NULL");
   if (qs->mode == DSA_MODE_DECODE) {
     if (qs->n_q != kv.batch) return fail(DSA_ERR_INVALID_ARG, "decode: n_q (%d) must equal batch (%d)", qs->n_q, kv.batch);
+    if (kv.batch > dsa::kMaxDecodeBatch)
+      return fail(DSA_ERR_UNSUPPORTED, "decode: batch %d above %d", kv.batch, dsa::kMaxDecodeBatch);
+    if (kv.max_ctx > dsa::kCompactChunk * 1024)
+      return fail(DSA_ERR_UNSUPPORTED, "decode: max_context_len above %d", dsa::kCompactChunk * 1024);
   } else if (qs->mode == DSA_MODE_PREFILL) {
     if (qs->n_q < 1) return fail(DSA_ERR_INVALID_ARG, "prefill: n_q must be >= 1");
     if (qs->seq < 0 || qs->seq >= kv.batch) return fail(DSA_ERR_INVALID_ARG, "prefill: seq %d outside [0, batch)", qs->seq);
@@ -116,14 +120,19 @@ dsa_status check_scores(const int32_t* scores, int32_t ld, const dsa::KV& kv, co
   return DSA_OK;
 }
 
+// Workspace regions.  Decode top-k: [coarse histograms | done counters | sel |
+// chunk records | runs | resolved rows]; attention: [partials | pair tickets].
+// The histograms and the counters must be zero when a call starts; every call
+// leaves them zero again.
 struct Layout {
-  size_t hist = 0, ticket_h = 0, ticket_c = 0, sel = 0, chunk_cnt = 0, run_pos = 0, run_info = 0;
-  size_t part_o = 0, part_ml = 0;
-  size_t sel_end = 0, total = 0;
-  int n_chunks = 0, rps = 0, max_splits = 1;
+  size_t coarse = 0, done_idx = 0, done_cmp = 0, sel = 0, chunk_rec = 0, run_pos = 0, run_score = 0, rowbase = 0;
+  size_t part_o = 0, part_ml = 0, pair_cnt = 0;
+  size_t sel_end = 0, attn_begin = 0, total = 0;
+  int n_chunks = 0;
 };
 
 Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
+  (void)prefix;
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -134,38 +143,48 @@ Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
   if (qs.mode == DSA_MODE_DECODE) {
     const size_t B = (size_t)kv.batch;
     L.n_chunks = (kv.max_ctx + dsa::kCompactChunk - 1) / dsa::kCompactChunk;
-    L.hist = take(B * 8192 * 4);
-    L.ticket_h = take(B * 4);
-    L.ticket_c = take(B * 4);
+    L.coarse = take(B * dsa::kCoarseBinsHost * 4);
+    L.done_idx = take(B * 4);
+    L.done_cmp = take(B * 4);
     L.sel = take(B * 16);
-    L.chunk_cnt = take(B * L.n_chunks * 8);
+    L.chunk_rec = take(B * L.n_chunks * dsa::kRecInts * 4);
     L.run_pos = take(B * L.n_chunks * dsa::kCompactChunk * 4);
-    L.run_info = take(B * L.n_chunks * dsa::kCompactChunk * 4);
+    L.run_score = take(B * L.n_chunks * dsa::kCompactChunk * 4);
   }
   L.sel_end = off;
-  const int64_t rows_max = (int64_t)prefix + k;
-  dsa::attn_split_plan(qs.n_q * kv.hkv, (int)rows_max, qs.mode, &L.rps, &L.max_splits);
-  if (L.max_splits > 1) {
-    const size_t heads = (size_t)qs.n_q * hq;
-    L.part_o = take(heads * L.max_splits * 128 * 4);
-    L.part_ml = take(heads * L.max_splits * 8);
-  }
+  L.attn_begin = off;
+  L.rowbase = take((size_t)qs.n_q * (size_t)k * 4);
+  const size_t G = (size_t)(hq / kv.hkv);
+  L.part_o = take((size_t)dsa::kMaxAttnCtas * 2 * G * 128 * 4);
+  L.part_ml = take((size_t)dsa::kMaxAttnCtas * 2 * G * 8);
+  L.pair_cnt = take((size_t)qs.n_q * kv.hkv * 4);
   L.total = off;
   return L;
 }
 
-dsa::SelState sel_state(const Layout& L, void* ws) {
+dsa::SelState sel_state(const Layout& L, void* ws, bool with_rowbase) {
   char* w = static_cast<char*>(ws);
   dsa::SelState s;
-  s.hist = reinterpret_cast<int*>(w + L.hist);
-  s.ticket_h = reinterpret_cast<int*>(w + L.ticket_h);
-  s.ticket_c = reinterpret_cast<int*>(w + L.ticket_c);
+  s.coarse = reinterpret_cast<int*>(w + L.coarse);
+  s.done_idx = reinterpret_cast<int*>(w + L.done_idx);
+  s.done_cmp = reinterpret_cast<int*>(w + L.done_cmp);
   s.sel = reinterpret_cast<int4*>(w + L.sel);
-  s.chunk_cnt = reinterpret_cast<int2*>(w + L.chunk_cnt);
+  s.chunk_rec = reinterpret_cast<int*>(w + L.chunk_rec);
   s.run_pos = reinterpret_cast<int*>(w + L.run_pos);
-  s.run_info = reinterpret_cast<int*>(w + L.run_info);
+  s.run_score = reinterpret_cast<int*>(w + L.run_score);
+  s.rowbase = with_rowbase ? reinterpret_cast<int*>(w + L.rowbase) : nullptr;
   s.n_chunks = L.n_chunks;
   return s;
+}
+
+dsa::AttnWs attn_ws(const Layout& L, void* ws) {
+  char* w = static_cast<char*>(ws);
+  dsa::AttnWs a;
+  a.rowbase = reinterpret_cast<int*>(w + L.rowbase);
+  a.part_o = reinterpret_cast<float*>(w + L.part_o);
+  a.part_ml = reinterpret_cast<float2*>(w + L.part_ml);
+  a.pair_cnt = reinterpret_cast<int*>(w + L.pair_cnt);
+  return a;
 }
 
 dsa_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
@@ -179,6 +198,13 @@ dsa_status check_k_prefix(int32_t k, int32_t prefix) {
   if (k < 1) return fail(DSA_ERR_INVALID_ARG, "k (%d) must be >= 1", k);
   if (prefix < 0) return fail(DSA_ERR_INVALID_ARG, "prefix_len (%d) must be >= 0", prefix);
   if ((int64_t)prefix + k > (int64_t(1) << 24)) return fail(DSA_ERR_UNSUPPORTED, "prefix_len + k above 2^24");
+  return DSA_OK;
+}
+
+// The attention kernel walks (query, KV head, 64-row tile) triples in 32-bit.
+dsa_status check_tiles(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_t prefix) {
+  if ((int64_t)qs.n_q * kv.hkv * (((int64_t)prefix + k + 63) / 64) >= (int64_t(1) << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "n_q * num_kv_heads * ceil((prefix_len + k) / 64) must stay below 2^31");
   return DSA_OK;
 }
 
@@ -210,6 +236,7 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
   DSA_TRY(check_qs(qs_, kv, &qs));
   DSA_TRY(check_k_prefix(k, prefix));
   DSA_TRY(check_heads(hq, kv));
+  DSA_TRY(check_tiles(kv, qs, k, prefix));
   if (!q || !aligned16(q) || !out || !aligned16(out))
     return fail(DSA_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
   if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
@@ -217,7 +244,7 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
     return fail(DSA_ERR_INVALID_ARG, "out_dtype %d is neither DSA_OUT_BF16 nor DSA_OUT_F32", out_dtype);
   if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
   const Layout L = layout(kv, qs, k, hq, prefix);
-  DSA_TRY(check_ws(ws, ws_bytes, L.max_splits > 1 ? L.total : 0));
+  DSA_TRY(check_ws(ws, ws_bytes, L.total));
   DSA_TRY(ensure_setup());
   dsa::AttnArgs a;
   a.kv = kv;
@@ -226,16 +253,14 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
   a.hq = hq;
   a.idx = idx;
   a.n_sel = n_sel;
+  a.rowbase = nullptr;
   a.k = k;
   a.prefix = prefix;
   a.scale = scale;
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
-  a.rows_per_split = L.rps;
-  a.max_splits = L.max_splits;
-  a.ws.part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + L.part_o);
-  a.ws.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + L.part_ml);
+  a.ws = attn_ws(L, ws);
   DSA_CUDA("sparse attention launch", dsa::launch_sparse_attn(a, stream));
   return DSA_OK;
 }
@@ -262,14 +287,14 @@ dsa_status prepare_decode_topk(const dsa_paged_kv* kv_, const int32_t* scores, i
   const Layout L = layout(kv, qs, k, kv.hkv, prefix);
   *kv_out = kv;
   *bytes = L.sel_end;
-  *clear_bytes = L.sel;  // hist, ticket_h and ticket_c come first
+  *clear_bytes = L.sel;  // histograms and counters come first
   return DSA_OK;
 }
 
 SelState decode_topk_state(const KV& kv, int32_t k, int32_t prefix, void* base) {
   const dsa_query_set qs_ = {DSA_MODE_DECODE, kv.batch, 0, 0};
   QS qs{qs_.mode, qs_.n_q, qs_.seq, qs_.pos0};
-  return sel_state(layout(kv, qs, k, kv.hkv, prefix), base);
+  return sel_state(layout(kv, qs, k, kv.hkv, prefix), base, false);
 }
 
 dsa_status set_error(dsa_status s, const char* msg) { return fail(s, "%s", msg); }
@@ -321,7 +346,7 @@ size_t dsa_workspace_size(int32_t op, const dsa_paged_kv* kv_, const dsa_query_s
     case DSA_OP_TOPK_SELECT: return L.sel_end;
     case DSA_OP_SPARSE_ATTN:
     case DSA_OP_DECODE_STEP:
-    case DSA_OP_PREFILL_STEP: return L.max_splits > 1 ? L.total : L.sel_end;
+    case DSA_OP_PREFILL_STEP: return L.total;
     default: fail(DSA_ERR_INVALID_ARG, "unknown op %d", op); return 0;
   }
 }
@@ -380,7 +405,7 @@ dsa_status dsa_topk_select(const dsa_paged_kv* kv_, const dsa_query_set* qs_, co
     const Layout L = layout(kv, qs, k, kv.hkv, prefix);
     DSA_TRY(check_ws(ws, ws_bytes, L.sel_end));
     DSA_TRY(ensure_setup());
-    const dsa::SelState s = sel_state(L, ws);
+    const dsa::SelState s = sel_state(L, ws, false);
     DSA_CUDA("top-k histogram launch", dsa::launch_decode_hist(kv, scores, ld, prefix, k, s, stream));
     DSA_CUDA("top-k compaction launch", dsa::launch_decode_compact(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
   } else {
@@ -432,6 +457,7 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t*
   DSA_TRY(check_qs(&qs_, kv, &qs));
   DSA_TRY(check_k_prefix(k, prefix));
   DSA_TRY(check_heads(hq, kv));
+  DSA_TRY(check_tiles(kv, qs, k, prefix));
   if (!q_idx || !aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx must be non-NULL and 16-byte aligned");
   DSA_TRY(check_scores(scores, ld, kv, qs));
   if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
@@ -443,7 +469,7 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t*
   const Layout L = layout(kv, qs, k, hq, prefix);
   DSA_TRY(check_ws(ws, ws_bytes, L.total));
   DSA_TRY(ensure_setup());
-  const dsa::SelState s = sel_state(L, ws);
+  const dsa::SelState s = sel_state(L, ws, true);
   DSA_CUDA("decode index launch", dsa::launch_decode_index(kv, q_idx, prefix, scores, ld, &s, k, stream));
   DSA_CUDA("decode compaction launch", dsa::launch_decode_compact(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
   dsa::AttnArgs a;
@@ -453,16 +479,14 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t*
   a.hq = hq;
   a.idx = idx;
   a.n_sel = n_sel;
+  a.rowbase = s.rowbase;
   a.k = k;
   a.prefix = prefix;
   a.scale = scale;
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
-  a.rows_per_split = L.rps;
-  a.max_splits = L.max_splits;
-  a.ws.part_o = reinterpret_cast<float*>(static_cast<char*>(ws) + L.part_o);
-  a.ws.part_ml = reinterpret_cast<float2*>(static_cast<char*>(ws) + L.part_ml);
+  a.ws = attn_ws(L, ws);
   DSA_CUDA("decode attention launch", dsa::launch_sparse_attn(a, stream));
   return DSA_OK;
 }

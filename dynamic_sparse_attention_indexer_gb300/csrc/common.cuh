@@ -23,11 +23,25 @@ constexpr int kIdxDim = 64;     // indexer dim (int8)
 constexpr int kHistBins = 8192;
 constexpr int kHistOff = 4096;
 
+// Coarse score histogram of the decode top-k: bins 16 scores wide,
+// bin = clamp((s >> 4) + 512, 0, 1023).  Interior bin b holds the scores
+// [(b - 512) * 16, (b - 512) * 16 + 15]; the edge bins 0 and 1023 collect the
+// rest and send the selection to the exact radix fallback.
+constexpr int kCoarseBins = 1024;
+constexpr int kCoarseShift = 4;
+constexpr int kCoarseOff = 512;
+constexpr int kFineBins = 1 << kCoarseShift;
+
 enum : int { kStOk = 0, kStBadBlock = 4, kStTimeout = 6 };
 enum : int { kSelAll = 1, kSelThreshold = 0 };
+// Decode selection modes kept between the scoring and compaction kernels.
+enum : int { kSelCoarse = 0, kSelExact = 2 };
 
 __device__ __forceinline__ int hist_bin(int s) {
   return min(max(s + kHistOff, 0), kHistBins - 1);
+}
+__device__ __forceinline__ int coarse_bin(int s) {
+  return min(max((s >> kCoarseShift) + kCoarseOff, 0), kCoarseBins - 1);
 }
 
 // Record the first error only.
@@ -77,6 +91,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Barrier over the first `count` threads of the CTA (count a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // Waits for phase `parity` of `bar` to complete, for at most ~2 s.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -106,6 +127,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");

@@ -22,25 +22,34 @@ struct QS {
   int mode, n_q, seq, pos0;
 };
 
-// Per-query selection state kept in the workspace between the histogram and
-// the compaction kernels (decode: one entry per sequence).
+// Decode selection state kept in the workspace between the scoring and the
+// compaction kernels, one entry per sequence.
 struct SelState {
-  int* hist;        // [n][kHistBins]   zero between calls
-  int* ticket_h;    // [n]              zero between calls
-  int* ticket_c;    // [n]              zero between calls
-  int4* sel;        // [n]              {mode, tau, n_gt, quota}
-  int2* chunk_cnt;  // [n][n_chunks]    {gt, eq} per compaction chunk
-  int* run_pos;     // [n][n_chunks * kCompactChunk]
-  int* run_info;    // same: (tie rank << 1) | is_tie
+  int* coarse;      // [B][kCoarseBins]        coarse score histogram, zero between calls
+  int* done_idx;    // [B]                     blocks scored so far, zero between calls
+  int* done_cmp;    // [B]                     compaction chunks done, zero between calls
+  int4* sel;        // [B]                     {mode, lo, width, above}: candidates have s >= lo,
+                    //                         `above` of them have s >= lo + width
+  int* chunk_rec;   // [B][n_chunks][kRecInts] per chunk: run length, count >= lo + width, fine bins
+  int* run_pos;     // [B][n_chunks * kCompactChunk] candidate positions, in order, per chunk
+  int* run_score;   // same: their scores
+  int* rowbase;     // [B][k] cache row (KV head 0) of each selected position, or nullptr
   int n_chunks;     // compaction chunks per sequence
 };
 
 constexpr int kCompactChunk = 2048;   // positions per compaction CTA
 constexpr int kCompactThreads = 256;  // 8 positions per thread
+constexpr int kRecInts = 2 + 16;      // run length, count above, 16 fine bins
+constexpr int kMaxDecodeBatch = 2048;
+constexpr int kMaxAttnCtas = 320;     // persistent attention grid cap (partials are sized for it)
+constexpr int kAttnWarps = 4;         // warps per attention CTA, one partial each
+constexpr int kCoarseBinsHost = 1024; // coarse histogram bins (host-side copy of the device constant)
 
 struct AttnWs {
-  float* part_o;    // [n_q][hq][max_splits][128]
-  float2* part_ml;  // [n_q][hq][max_splits]  (max in log2 units, sum)
+  int* rowbase;     // [n_q][k]                   cache row (KV head 0) of every selected position
+  float* part_o;    // [kMaxAttnCtas][2][G][128]  per-CTA segment partials (unnormalised O)
+  float2* part_ml;  // [kMaxAttnCtas][2][G]       (max in log2 units, sum of weights)
+  int* pair_cnt;    // [n_q * Hkv]                            tiles merged per (query, KV head), zero between calls
 };
 
 struct AttnArgs {
@@ -50,18 +59,14 @@ struct AttnArgs {
   int hq;
   const int32_t* idx;
   const int32_t* n_sel;
+  const int32_t* rowbase;  // resolved cache rows of idx (head 0); null: resolved into ws.rowbase first
   int k, prefix;
   float scale;
   void* out;
   int out_dtype;
   float* lse;
-  int rows_per_split, max_splits;  // max_splits == 1: no combine pass
   AttnWs ws;
 };
-
-// Grid planning shared by the workspace sizing and the launches.
-int decode_index_chunk(int batch, int max_ctx);  // positions per indexer CTA
-void attn_split_plan(int pairs, int rows_max, int mode, int* rows_per_split, int* max_splits);
 
 // Kernel launches (return the launch error, if any).
 cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, int* scores, int ld,

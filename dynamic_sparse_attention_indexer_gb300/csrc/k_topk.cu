@@ -11,6 +11,8 @@
 // Prefill (many rows of at most a few ten thousand candidates): one CTA per
 // query row builds its histogram in shared memory, finds the threshold and
 // compacts the row in order with block-wide scans.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
@@ -22,74 +24,174 @@ __device__ int g_status;
 
 constexpr int kPer = kCompactChunk / kCompactThreads;  // 8 consecutive positions per thread
 static_assert(kPer == 8, "compaction assumes 8 positions per thread");
+constexpr int kStageEntries = 4096;                      // merge entries staged in shared memory
+constexpr int kMaxChunks = 1024;                         // compaction chunks per sequence at most
 
 struct CompactParams {
   const int32_t* scores;
   const int32_t* ctx;
-  int ld, prefix, k, max_ctx;
+  const int32_t* bt;
+  int ld, prefix, k, max_ctx, max_blocks, num_blocks, hkv;
   SelState sel;
   int32_t* idx;
   int32_t* n_sel;
 };
 
-// Lays the runs of sequence b end to end (the last compaction CTA of b).
-__device__ void merge_runs(const CompactParams& p, int b, const int4 sel) {
-  __shared__ int s_take[kCompactThreads], s_off[kCompactThreads], s_len[kCompactThreads];
-  __shared__ int scratch[40];
+// Cache row (KV head 0) of position t of sequence b.
+__device__ __forceinline__ int row_base(const CompactParams& p, int b, int t) {
+  return load_block(p.bt, b, p.max_blocks, t >> 6, p.num_blocks, &g_status) * p.hkv * kBlock + (t & 63);
+}
+
+struct MergeSmem {
+  int ent_pos[kStageEntries];
+  int ent_score[kStageEntries];
+  int run_off[kMaxChunks + 1];
+  int fine[kFineBins];
+  int misc[8];
+  int scratch[40];
+};
+
+// Run entry e (flattened over the chunks of sequence b, in position order).
+__device__ __forceinline__ void load_entry(const CompactParams& p, const MergeSmem& sm, int b, int nch, int e,
+                                           bool staged, int* pos, int* score) {
+  if (staged) {
+    *pos = sm.ent_pos[e];
+    *score = sm.ent_score[e];
+    return;
+  }
+  int lo = 0, hi = nch - 1;  // last chunk with run_off <= e
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sm.run_off[mid] <= e) lo = mid; else hi = mid - 1;
+  }
+  const size_t at = ((size_t)b * nch + lo) * kCompactChunk + (e - sm.run_off[lo]);
+  *pos = __ldcg(p.sel.run_pos + at);
+  *score = __ldcg(p.sel.run_score + at);
+}
+
+// The last compaction CTA of sequence b: exact threshold from the fine bins,
+// then every candidate run, in position order, filtered and written out.
+__device__ void merge_runs(const CompactParams& p, int b, const int4 sel, MergeSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nch = p.sel.n_chunks;
-  const int quota = sel.w;
-  int carry_ties = 0, carry_out = 0;
-  int32_t* out = p.idx + (size_t)b * p.k;
+  const int lo = sel.y, width = sel.z, above = sel.w;
+  if (tid < kFineBins) sm.fine[tid] = 0;
+  __syncthreads();
+  // Fine-bin totals and run offsets (chunks in order).
+  int carry = 0;
   for (int base = 0; base < nch; base += kCompactThreads) {
     const int c = base + tid;
-    int2 cnt = make_int2(0, 0);
-    if (c < nch) cnt = __ldcg(p.sel.chunk_cnt + (size_t)b * nch + c);
+    int run_len = 0;
+    if (c < nch) {
+      const int* rec = p.sel.chunk_rec + ((size_t)b * nch + c) * kRecInts;
+      run_len = __ldcg(rec);
+      for (int f = 0; f < width; ++f) {
+        const int v = __ldcg(rec + 2 + f);
+        if (v) atomicAdd(&sm.fine[f], v);
+      }
+    }
     int tot;
-    const int ties_before = block_exclusive_scan(cnt.y, scratch, &tot) + carry_ties;
-    carry_ties += tot;
-    const int take = min(max(quota - ties_before, 0), cnt.y);
-    const int off = block_exclusive_scan(cnt.x + take, scratch, &tot) + carry_out;
-    carry_out += tot;
-    s_take[tid] = take;
-    s_off[tid] = off;
-    s_len[tid] = cnt.x + cnt.y;
-    __syncthreads();
-    const int ngrp = min(kCompactThreads, nch - base);
-    for (int cc = warp; cc < ngrp; cc += kCompactThreads / 32) {
-      const size_t run = ((size_t)b * nch + base + cc) * kCompactChunk;
-      const int len = s_len[cc], tk = s_take[cc], o = s_off[cc];
-      for (int j = lane; j < len; j += 32) {
-        const int pos = __ldcg(p.sel.run_pos + run + j);
-        const int info = __ldcg(p.sel.run_info + run + j);
-        const int e = info >> 1;
-        const int dst = o + (j - e) + min(e, tk);
-        if ((!(info & 1) || e < tk) && dst < p.k) out[dst] = pos;  // bound holds unless the workspace was dirty
+    const int ex = block_exclusive_scan(run_len, sm.scratch, &tot);
+    if (c < nch) sm.run_off[c] = carry + ex;
+    carry += tot;
+  }
+  __syncthreads();
+  const int E = carry;
+  if (tid == 0) {
+    sm.run_off[nch] = E;
+    // The k-th largest lies in fine bin f*: fewer than k - above candidates sit above it.
+    const int kk = p.k - above;
+    int cum = 0, fstar = 0;
+    for (int f = width - 1; f >= 0; --f) {
+      if (cum + sm.fine[f] >= kk) {
+        fstar = f;
+        break;
+      }
+      cum += sm.fine[f];
+    }
+    sm.misc[0] = lo + fstar;        // tau
+    sm.misc[1] = p.k - above - cum;  // quota of ties at tau
+  }
+  __syncthreads();
+  const int tau = sm.misc[0], quota = sm.misc[1];
+  const bool staged = E <= kStageEntries;
+  if (staged) {
+    for (int c = warp; c < nch; c += kCompactThreads / 32) {
+      const size_t run = ((size_t)b * nch + c) * kCompactChunk;
+      const int off = sm.run_off[c], n = sm.run_off[c + 1] - off;
+      for (int j = lane; j < n; j += 32) {
+        sm.ent_pos[off + j] = __ldcg(p.sel.run_pos + run + j);
+        sm.ent_score[off + j] = __ldcg(p.sel.run_score + run + j);
       }
     }
     __syncthreads();
   }
-  carry_out = min(carry_out, p.k);
-  for (int r = carry_out + tid; r < p.k; r += kCompactThreads) out[r] = -1;
+  // Each thread owns a contiguous slice of the entries.
+  const int per = (E + kCompactThreads - 1) / kCompactThreads;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int n_eq = 0;
+  for (int e = e0; e < e1; ++e) {
+    int pos, sc;
+    load_entry(p, sm, b, nch, e, staged, &pos, &sc);
+    n_eq += sc == tau;
+  }
+  int tot;
+  int tie = block_exclusive_scan(n_eq, sm.scratch, &tot);  // ties before this slice
+  int n_take = 0;
+  for (int e = e0, tr = tie; e < e1; ++e) {
+    int pos, sc;
+    load_entry(p, sm, b, nch, e, staged, &pos, &sc);
+    if (sc > tau) ++n_take;
+    else if (sc == tau) n_take += tr++ < quota;
+  }
+  int o = block_exclusive_scan(n_take, sm.scratch, &tot);
+  int32_t* out = p.idx + (size_t)b * p.k;
+  for (int e = e0, tr = tie; e < e1; ++e) {
+    int pos, sc;
+    load_entry(p, sm, b, nch, e, staged, &pos, &sc);
+    const bool take = sc > tau || (sc == tau && tr++ < quota);
+    if (take && o < p.k) {
+      out[o] = pos;
+      if (p.sel.rowbase) p.sel.rowbase[(size_t)b * p.k + o] = row_base(p, b, pos);
+    }
+    o += take;
+  }
+  const int n_out = min(tot, p.k);
+  for (int r = n_out + tid; r < p.k; r += kCompactThreads) out[r] = -1;
   if (tid == 0) {
-    p.n_sel[b] = carry_out;
-    p.sel.ticket_c[b] = 0;
+    p.n_sel[b] = n_out;
+    p.sel.done_cmp[b] = 0;
   }
 }
 
 __global__ void __launch_bounds__(kCompactThreads) decode_compact_kernel(const CompactParams p) {
-  __shared__ int scratch[40];
+  __shared__ MergeSmem sm;
+  __shared__ int s_fine[kFineBins];
   __shared__ int s_last;
   const int tid = threadIdx.x, b = blockIdx.y, c = blockIdx.x;
   const int L = min(__ldg(p.ctx + b), p.max_ctx);
-  const int4 sel = __ldcg(p.sel.sel + b);
-  const bool all = sel.x == kSelAll;
-  const int tau = sel.y;
+  const int n_cand = max(0, L - p.prefix);
   const int t_lo = max(p.prefix, c * kCompactChunk), t_hi = min(L, (c + 1) * kCompactChunk);
-  const int t_base = c * kCompactChunk + tid * kPer;
+  int32_t* out = p.idx + (size_t)b * p.k;
 
+  if (n_cand <= p.k) {  // every candidate is selected: position t goes to slot t - prefix
+    for (int t = t_lo + tid; t < t_hi; t += kCompactThreads) {
+      out[t - p.prefix] = t;
+      if (p.sel.rowbase) p.sel.rowbase[(size_t)b * p.k + (t - p.prefix)] = row_base(p, b, t);
+    }
+    if (c == 0) {
+      for (int r = n_cand + tid; r < p.k; r += kCompactThreads) out[r] = -1;
+      if (tid == 0) p.n_sel[b] = n_cand;
+    }
+    return;
+  }
+
+  const int4 sel = __ldcg(p.sel.sel + b);
+  const int lo = sel.y, hi = sel.y + sel.z;  // candidates: s >= lo; fine bins: lo <= s < hi
+  if (tid < kFineBins) s_fine[tid] = 0;
+  const int t_base = c * kCompactChunk + tid * kPer;
   int v[kPer];
-  if (t_base + kPer <= t_hi && t_base >= t_lo) {
+  if (t_base >= t_lo && t_base + kPer <= t_hi) {
     const int4* src = reinterpret_cast<const int4*>(p.scores + (size_t)b * p.ld + t_base);
     const int4 a = __ldg(src), bb = __ldg(src + 1);
     v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = bb.x, v[5] = bb.y, v[6] = bb.z, v[7] = bb.w;
@@ -97,41 +199,46 @@ __global__ void __launch_bounds__(kCompactThreads) decode_compact_kernel(const C
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int t = t_base + j;
-      v[j] = (t >= t_lo && t < t_hi) ? __ldg(p.scores + (size_t)b * p.ld + t) : 0;
+      v[j] = (t >= t_lo && t < t_hi) ? __ldg(p.scores + (size_t)b * p.ld + t) : INT_MIN;
     }
   }
-  uint32_t gt_m = 0, eq_m = 0;
+  __syncthreads();
+  uint32_t cand = 0;
+  int n_above = 0;
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int t = t_base + j;
-    const bool in = t >= t_lo && t < t_hi;
-    if (in && (all || v[j] > tau)) gt_m |= 1u << j;
-    if (in && !all && v[j] == tau) eq_m |= 1u << j;
-  }
-  const int n_gt = __popc(gt_m), n_eq = __popc(eq_m);
-  int tot_len, tot_eq;
-  const int off = block_exclusive_scan(n_gt + n_eq, scratch, &tot_len);
-  const int eq_off = block_exclusive_scan(n_eq, scratch, &tot_eq);
-  const size_t run = ((size_t)b * p.sel.n_chunks + c) * kCompactChunk;
-  int o = off, e = eq_off;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const bool g = (gt_m >> j) & 1, q = (eq_m >> j) & 1;
-    if (g || q) {
-      p.sel.run_pos[run + o] = t_base + j;
-      p.sel.run_info[run + o] = (e << 1) | (q ? 1 : 0);
-      ++o;
-      e += q;
+    if (t >= t_lo && t < t_hi && v[j] >= lo) {
+      cand |= 1u << j;
+      if (v[j] >= hi) ++n_above;
+      else atomicAdd(&s_fine[v[j] - lo], 1);
     }
   }
-  if (tid == 0) p.sel.chunk_cnt[(size_t)b * p.sel.n_chunks + c] = make_int2(tot_len - tot_eq, tot_eq);
+  int tot_len, tot_above;
+  const int off = block_exclusive_scan(__popc(cand), sm.scratch, &tot_len);
+  block_exclusive_scan(n_above, sm.scratch, &tot_above);
+  const size_t run = ((size_t)b * p.sel.n_chunks + c) * kCompactChunk;
+  int o = off;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j)
+    if ((cand >> j) & 1) {
+      p.sel.run_pos[run + o] = t_base + j;
+      p.sel.run_score[run + o] = v[j];
+      ++o;
+    }
+  int* rec = p.sel.chunk_rec + ((size_t)b * p.sel.n_chunks + c) * kRecInts;
+  if (tid == 0) {
+    rec[0] = tot_len;
+    rec[1] = tot_above;
+  }
+  if (tid < kFineBins) rec[2 + tid] = s_fine[tid];
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(p.sel.ticket_c + b, 1) == (int)gridDim.x - 1;
+  if (tid == 0) s_last = atomicAdd(p.sel.done_cmp + b, 1) == (int)gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  merge_runs(p, b, sel);
+  merge_runs(p, b, sel, sm);
 }
 
 // ---------------------------------------------------------------- prefill ---
@@ -215,10 +322,14 @@ cudaError_t launch_decode_compact(const KV& kv, const int32_t* scores, int ld, i
   CompactParams p;
   p.scores = scores;
   p.ctx = kv.context_lens;
+  p.bt = kv.block_table;
   p.ld = ld;
   p.prefix = prefix;
   p.k = k;
   p.max_ctx = kv.max_ctx;
+  p.max_blocks = kv.max_blocks;
+  p.num_blocks = kv.num_blocks;
+  p.hkv = kv.hkv;
   p.sel = sel;
   p.idx = idx;
   p.n_sel = n_sel;

@@ -18,12 +18,12 @@ struct Sel {
 
 // Finds the histogram bin beta holding the k-th largest score: the count above
 // beta is < k and the count from beta up is >= k.  All threads of the CTA call;
-// blockDim.x must divide kHistBins.  `ld` loads bin i.  Requires sum >= k.
+// blockDim.x must divide NB.  `ld` loads bin i.  Requires sum >= k.
 // Returns beta (or -1 if the counts do not reach k) and the count above it.
-template <class Load>
+template <int NB = kHistBins, class Load>
 __device__ __forceinline__ void hist_threshold_bin(Load ld, int k, int* scratch, int* beta_out,
                                                    int* above_out) {
-  const int per = kHistBins / blockDim.x;
+  const int per = NB / blockDim.x;
   const int base = threadIdx.x * per;
   int local = 0;
   for (int i = 0; i < per; ++i) local += ld(base + i);

@@ -212,7 +212,7 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
  * device array of DSA_TOPK_STATIC_SCRATCH_BYTES inside the library, which every
  * GPU that loads the library keeps until the process exits; the call makes no
  * cudaMalloc, cudaFree or other allocating call.
- *   - Scratch needed: about batch * (33 KB + 8 bytes * max_context_len); larger
+ *   - Scratch needed: about batch * (4 KB + 8 bytes * max_context_len); larger
  *     sizes return DSA_ERR_UNSUPPORTED before anything is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and sets kernel attributes: make that first call

@@ -122,3 +122,72 @@ def oracle_decode_sampled(w: dict, b: int, heads_kv, k: int, P: int):
         out, lse = O.sparse_gqa_attention(q, kc, vc, kbt, att, 1, scale)
         heads[g] = (out, lse)
     return {"scores": s, "idx": idx, "n_sel": n_sel, "heads": heads}
+
+
+def run_prefill(w: dict, out_dtype=torch.bfloat16) -> dict:
+    """index_scores -> topk_select -> sparse_attn_prefill for the queries of
+    sequence w["seq"] at positions pos0 .. pos0 + T - 1."""
+    dev = w["q"].device
+    kv = paged_kv(w)
+    T, k, P, hq = int(w["num_queries"]), int(w["k"]), int(w["prefix_len"]), int(w["num_q_heads"])
+    qs = dsa.query_set(dsa.MODE_PREFILL, T, int(w["seq"]), int(w["pos0"]))
+    ld = round4(int(w["pos0"]) + T)
+    scores = torch.zeros((T, ld), dtype=torch.int32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(T, dtype=torch.int32, device=dev)
+    out = torch.empty((T, hq, 128), dtype=out_dtype, device=dev)
+    lse = torch.empty((T, hq), dtype=torch.float32, device=dev)
+    ws = dsa.make_workspace(dsa.workspace_size(dsa.OP_PREFILL_STEP, kv, qs, k, hq, P), dev)
+    dsa.index_scores(kv, qs, w["q_idx"], P, scores)
+    dsa.topk_select(kv, qs, scores, P, k, idx, n_sel, ws)
+    dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws)
+    status = dsa.check_device_status(dev)
+    assert status == 0, f"device status {status}"
+    return {"scores": scores, "idx": idx, "n_sel": n_sel, "out": out, "lse": lse}
+
+
+def check_prefill_against_oracle(wn: dict, res: dict, rows=None):
+    P = int(wn["prefix_len"])
+    pos0 = int(wn["pos0"])
+    T = int(wn["num_queries"])
+    idx = res["idx"].cpu().numpy()
+    n_sel = res["n_sel"].cpu().numpy()
+    out = res["out"].float().cpu().numpy()
+    lse = res["lse"].cpu().numpy()
+    scores = res["scores"].cpu().numpy()
+    for i in (range(T) if rows is None else rows):
+        r = O.prefill_query(wn, i)
+        pos = pos0 + i
+        if pos >= P:
+            assert np.array_equal(scores[i, P:pos + 1], r["scores"]), f"scores of query {i}"
+        assert int(n_sel[i]) == r["n_sel"], f"n_sel of query {i}"
+        assert np.array_equal(idx[i], r["idx"]), f"idx of query {i}"
+        assert_close(out[i], r["out"], f"out of query {i}")
+        assert_close(lse[i], r["lse"], f"lse of query {i}")
+
+
+def oracle_prefill_sampled(w: dict, i: int, heads_kv, k: int, P: int):
+    """Oracle result of prefill query i of a device-resident workload."""
+    seq = int(w["seq"])
+    pos = int(w["pos0"]) + i
+    cand = O.candidate_positions(P, pos)
+    wv = dict(w)
+    wv["block_table"] = w["block_table"][seq:seq + 1]
+    q_idx = w["q_idx"][i].cpu().numpy().astype(np.int64)
+    if cand.size:
+        icache, ibt = _compact_blocks(wv, 0, cand, "idx_cache")
+        ts, s = O.index_scores(q_idx, icache, ibt, P, pos)
+    else:
+        ts, s = cand, np.zeros(0, dtype=np.int64)
+    idx, n_sel = O.topk_select(ts, s, k)
+    att = O.attended_positions(P, pos, idx, n_sel)
+    hq, hkv = int(w["num_q_heads"]), int(w["num_kv_heads"])
+    G = hq // hkv
+    heads = {}
+    for g in heads_kv:
+        kc, kbt = _compact_blocks(wv, 0, att, "k_cache", head=g)
+        vc, _ = _compact_blocks(wv, 0, att, "v_cache", head=g)
+        q = w["q"][i, g * G:(g + 1) * G].cpu().to(torch.float64).numpy()
+        out, lse = O.sparse_gqa_attention(q, kc, vc, kbt, att, 1, 1.0 / np.sqrt(128))
+        heads[g] = (out, lse)
+    return {"scores": s, "idx": idx, "n_sel": n_sel, "heads": heads}

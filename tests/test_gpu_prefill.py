@@ -1,0 +1,83 @@
+"""Prefill path on the GPU against the CPU oracle: causal int8 indexer GEMM,
+per-row top-k, and sparse GQA attention over each query's own selection."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _prefill_spec(T, pos0=0, P=64, k=100, hq=8, hkv=2, batch_lens=None, seq=0, **kw):
+    lens = batch_lens or (pos0 + T,)
+    return synth.Spec("prefill-small", "prefill", len(lens), tuple(lens), P, hq, hkv, k, num_queries=T,
+                      pos0=pos0, **kw)
+
+
+def _run(spec, seed=5, seq=0, out_dtype=torch.bfloat16):
+    w_cpu = synth.make_workload(spec, seed, "cpu")
+    w_cpu["seq"] = seq
+    w = H.on(w_cpu, DEV)
+    res = H.run_prefill(w, out_dtype=out_dtype)
+    H.check_prefill_against_oracle(synth.to_numpy(w_cpu), res)
+    return res
+
+
+def test_prefill_small_from_position_zero(lib):
+    """Queries inside the prefix, at its edge, and with fewer / more than k candidates."""
+    _run(_prefill_spec(T=400, pos0=0, P=64, k=100))
+
+
+def test_prefill_continuation_chunk(lib):
+    """A chunk of queries that starts deep into the sequence (pos0 > 0)."""
+    _run(_prefill_spec(T=200, pos0=1000, P=100, k=256, hq=16, hkv=2))
+
+
+def test_prefill_second_sequence_of_the_table(lib):
+    spec = _prefill_spec(T=150, pos0=50, P=64, k=64, batch_lens=(700, 200))
+    _run(spec, seq=1)
+
+
+def test_prefill_group_16_and_fp32(lib):
+    _run(_prefill_spec(T=130, pos0=200, P=32, k=50, hq=32, hkv=2), out_dtype=torch.float32)
+
+
+def test_prefill_full_int8_range(lib):
+    _run(_prefill_spec(T=150, pos0=300, P=64, k=90, idx_lo=-128, idx_hi=127))
+
+
+def test_full_prefill_16k(lib):
+    spec = synth.CONFIGS[4]
+    w = synth.make_workload(spec, 1004, DEV)
+    res = H.run_prefill(w)
+    P, k = spec.prefix_len, spec.k
+    idx = res["idx"].cpu().numpy()
+    n_sel = res["n_sel"].cpu().numpy()
+    out = res["out"].float().cpu().numpy()
+    lse = res["lse"].cpu().numpy()
+    G = spec.num_q_heads // spec.num_kv_heads
+    for i in (0, 575, 576, 577, P + k - 1, P + k, 9000, spec.num_queries - 1):
+        r = H.oracle_prefill_sampled(w, i, [0, 3], k, P)
+        if i >= P:
+            assert np.array_equal(res["scores"][i, P:i + 1].cpu().numpy(), r["scores"]), f"scores row {i}"
+        assert int(n_sel[i]) == r["n_sel"]
+        assert np.array_equal(idx[i], r["idx"]), f"idx row {i}"
+        for g, (o, s) in r["heads"].items():
+            H.assert_close(out[i, g * G:(g + 1) * G], o, f"out row {i} kv head {g}")
+            H.assert_close(lse[i, g * G:(g + 1) * G], s, f"lse row {i} kv head {g}")
+    # every row: the count, ascending order, causal range, -1 padding
+    pos = np.arange(spec.num_queries)
+    want = np.minimum(k, np.maximum(0, pos + 1 - P))
+    assert np.array_equal(n_sel, want)
+    valid = np.arange(k)[None, :] < n_sel[:, None]
+    assert np.all(idx[~valid] == -1)
+    sel = np.where(valid, idx, 0)
+    assert np.all(np.where(valid, (sel >= P) & (sel <= pos[:, None]), True))
+    d = np.diff(np.where(valid, idx, np.iinfo(np.int32).max), axis=1)
+    assert np.all(d[valid[:, 1:]] > 0)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
