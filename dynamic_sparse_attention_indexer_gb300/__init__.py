@@ -54,7 +54,7 @@ def _stream(device=None):
 
 
 class PagedKV:
-    """The paged cache: k_cache/v_cache bf16 [num_blocks][Hkv][64][128],
+    """The paged cache: k_cache/v_cache bf16 [num_blocks][64][Hkv][128],
     idx_cache int8 [num_blocks][64][64], block_table int32 [B][max_blocks],
     context_lens int32 [B] (all on one CUDA device)."""
 
@@ -64,11 +64,11 @@ class PagedKV:
         if max_context_len is None:
             max_context_len = int(context_lens.max().item())
         self.max_context_len = int(max_context_len)
-        self.num_kv_heads = int(k_cache.shape[1])
+        self.num_kv_heads = int(k_cache.shape[2])
         self.batch = int(block_table.shape[0])
         self.struct = _abi.PagedKV(
             _ptr(k_cache), _ptr(v_cache), _ptr(idx_cache), _ptr(block_table), _ptr(context_lens),
-            int(k_cache.shape[0]), int(k_cache.shape[2]), self.num_kv_heads, int(k_cache.shape[3]),
+            int(k_cache.shape[0]), int(k_cache.shape[1]), self.num_kv_heads, int(k_cache.shape[3]),
             int(idx_cache.shape[2]), int(block_table.shape[1]), self.batch, self.max_context_len)
 
     @property

@@ -58,6 +58,8 @@ dsa_status check_kv(const dsa_paged_kv* kv, dsa::KV* out) {
   if (kv->idx_dim != 64) return fail(DSA_ERR_UNSUPPORTED, "idx_dim %d: only 64 is supported", kv->idx_dim);
   if (kv->num_blocks < 1 || kv->num_kv_heads < 1 || kv->batch < 1 || kv->max_blocks_per_seq < 1)
     return fail(DSA_ERR_INVALID_ARG, "num_blocks, num_kv_heads, batch and max_blocks_per_seq must be >= 1");
+  if (kv->num_kv_heads != 1 && kv->num_kv_heads != 2 && kv->num_kv_heads != 4 && kv->num_kv_heads != 8)
+    return fail(DSA_ERR_UNSUPPORTED, "num_kv_heads %d: only 1, 2, 4 or 8 are supported", kv->num_kv_heads);
   if ((int64_t)kv->num_blocks * kv->num_kv_heads * 64 >= (int64_t(1) << 31))
     return fail(DSA_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 64 must stay below 2^31 rows");
   if ((int64_t)kv->max_blocks_per_seq * 64 >= (int64_t(1) << 30))
@@ -125,8 +127,8 @@ dsa_status check_scores(const int32_t* scores, int32_t ld, const dsa::KV& kv, co
 // The histograms and the counters must be zero when a call starts; every call
 // leaves them zero again.
 struct Layout {
-  size_t coarse = 0, done_idx = 0, done_cmp = 0, sel = 0, chunk_rec = 0, run_pos = 0, run_score = 0, rowbase = 0;
-  size_t part_o = 0, part_ml = 0, pair_cnt = 0;
+  size_t coarse = 0, done_idx = 0, done_cmp = 0, sel = 0, chunk_rec = 0, run_pos = 0, run_score = 0, slot = 0;
+  size_t part_o = 0, part_ml = 0;
   size_t sel_end = 0, attn_begin = 0, total = 0;
   int n_chunks = 0;
 };
@@ -153,16 +155,14 @@ Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
   }
   L.sel_end = off;
   L.attn_begin = off;
-  L.rowbase = take((size_t)qs.n_q * (size_t)k * 4);
-  const size_t G = (size_t)(hq / kv.hkv);
-  L.part_o = take((size_t)dsa::kMaxAttnCtas * 2 * G * 128 * 4);
-  L.part_ml = take((size_t)dsa::kMaxAttnCtas * 2 * G * 8);
-  L.pair_cnt = take((size_t)qs.n_q * kv.hkv * 4);
+  L.slot = take((size_t)qs.n_q * (size_t)k * 4);
+  L.part_o = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 128 * 4);
+  L.part_ml = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 8);
   L.total = off;
   return L;
 }
 
-dsa::SelState sel_state(const Layout& L, void* ws, bool with_rowbase) {
+dsa::SelState sel_state(const Layout& L, void* ws, bool with_slot) {
   char* w = static_cast<char*>(ws);
   dsa::SelState s;
   s.coarse = reinterpret_cast<int*>(w + L.coarse);
@@ -172,7 +172,7 @@ dsa::SelState sel_state(const Layout& L, void* ws, bool with_rowbase) {
   s.chunk_rec = reinterpret_cast<int*>(w + L.chunk_rec);
   s.run_pos = reinterpret_cast<int*>(w + L.run_pos);
   s.run_score = reinterpret_cast<int*>(w + L.run_score);
-  s.rowbase = with_rowbase ? reinterpret_cast<int*>(w + L.rowbase) : nullptr;
+  s.slot = with_slot ? reinterpret_cast<int*>(w + L.slot) : nullptr;
   s.n_chunks = L.n_chunks;
   return s;
 }
@@ -180,10 +180,9 @@ dsa::SelState sel_state(const Layout& L, void* ws, bool with_rowbase) {
 dsa::AttnWs attn_ws(const Layout& L, void* ws) {
   char* w = static_cast<char*>(ws);
   dsa::AttnWs a;
-  a.rowbase = reinterpret_cast<int*>(w + L.rowbase);
+  a.slot = reinterpret_cast<int*>(w + L.slot);
   a.part_o = reinterpret_cast<float*>(w + L.part_o);
   a.part_ml = reinterpret_cast<float2*>(w + L.part_ml);
-  a.pair_cnt = reinterpret_cast<int*>(w + L.pair_cnt);
   return a;
 }
 
@@ -201,10 +200,11 @@ dsa_status check_k_prefix(int32_t k, int32_t prefix) {
   return DSA_OK;
 }
 
-// The attention kernel walks (query, KV head, 64-row tile) triples in 32-bit.
+// The attention kernel walks (query, tile of 128 / num_kv_heads rows) pairs in 32-bit.
 dsa_status check_tiles(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_t prefix) {
-  if ((int64_t)qs.n_q * kv.hkv * (((int64_t)prefix + k + 63) / 64) >= (int64_t(1) << 31))
-    return fail(DSA_ERR_UNSUPPORTED, "n_q * num_kv_heads * ceil((prefix_len + k) / 64) must stay below 2^31");
+  const int64_t rows = 128 / kv.hkv;
+  if ((int64_t)qs.n_q * (((int64_t)prefix + k + rows - 1) / rows) >= (int64_t(1) << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "n_q * ceil((prefix_len + k) / (128 / num_kv_heads)) must stay below 2^31");
   return DSA_OK;
 }
 
@@ -253,7 +253,7 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
   a.hq = hq;
   a.idx = idx;
   a.n_sel = n_sel;
-  a.rowbase = nullptr;
+  a.slot = nullptr;
   a.k = k;
   a.prefix = prefix;
   a.scale = scale;
@@ -479,7 +479,7 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t*
   a.hq = hq;
   a.idx = idx;
   a.n_sel = n_sel;
-  a.rowbase = s.rowbase;
+  a.slot = s.slot;
   a.k = k;
   a.prefix = prefix;
   a.scale = scale;

@@ -33,7 +33,7 @@ struct SelState {
   int* chunk_rec;   // [B][n_chunks][kRecInts] per chunk: run length, count >= lo + width, fine bins
   int* run_pos;     // [B][n_chunks * kCompactChunk] candidate positions, in order, per chunk
   int* run_score;   // same: their scores
-  int* rowbase;     // [B][k] cache row (KV head 0) of each selected position, or nullptr
+  int* slot;        // [B][k] cache slot (block * 64 + row) of each selected position, or nullptr
   int n_chunks;     // compaction chunks per sequence
 };
 
@@ -42,14 +42,12 @@ constexpr int kCompactThreads = 256;  // 8 positions per thread
 constexpr int kRecInts = 2 + 16;      // run length, count above, 16 fine bins
 constexpr int kMaxDecodeBatch = 2048;
 constexpr int kMaxAttnCtas = 320;     // persistent attention grid cap (partials are sized for it)
-constexpr int kAttnWarps = 4;         // warps per attention CTA, one partial each
 constexpr int kCoarseBinsHost = 1024; // coarse histogram bins (host-side copy of the device constant)
 
 struct AttnWs {
-  int* rowbase;     // [n_q][k]                   cache row (KV head 0) of every selected position
-  float* part_o;    // [kMaxAttnCtas][2][G][128]  per-CTA segment partials (unnormalised O)
-  float2* part_ml;  // [kMaxAttnCtas][2][G]       (max in log2 units, sum of weights)
-  int* pair_cnt;    // [n_q * Hkv]                            tiles merged per (query, KV head), zero between calls
+  int* slot;        // [n_q][k]                    cache slot of every selected position
+  float* part_o;    // [kMaxAttnCtas][2][Hq][128]  per-CTA partials of split queries (unnormalised O)
+  float2* part_ml;  // [kMaxAttnCtas][2][Hq]       (max in log2 units, sum of weights)
 };
 
 struct AttnArgs {
@@ -59,7 +57,7 @@ struct AttnArgs {
   int hq;
   const int32_t* idx;
   const int32_t* n_sel;
-  const int32_t* rowbase;  // resolved cache rows of idx (head 0); null: resolved into ws.rowbase first
+  const int32_t* slot;     // cache slots of idx; null: resolved into ws.slot first
   int k, prefix;
   float scale;
   void* out;

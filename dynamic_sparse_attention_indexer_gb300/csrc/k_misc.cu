@@ -25,6 +25,7 @@ struct WriteParams {
 };
 
 // One CTA per token: Hkv x 16 chunks of K, the same of V, 4 chunks of the indexer key.
+// A slot's K (and V) row holds all KV heads contiguously, so both copies are straight runs.
 __global__ void kv_write_kernel(const WriteParams p) {
   const int j = blockIdx.x;
   const int slot = __ldg(p.slots + j);
@@ -38,9 +39,8 @@ __global__ void kv_write_kernel(const WriteParams p) {
     if (c < 2 * kv_chunks) {
       const bool is_v = c >= kv_chunks;
       const int cc = is_v ? c - kv_chunks : c;
-      const int g = cc >> 4, ch = cc & 15;
-      const __nv_bfloat16* src = (is_v ? p.v : p.k) + ((size_t)j * p.hkv + g) * kHeadDim + ch * 8;
-      __nv_bfloat16* dst = (is_v ? p.vc : p.kc) + (((size_t)blk * p.hkv + g) * kBlock + row) * kHeadDim + ch * 8;
+      const __nv_bfloat16* src = (is_v ? p.v : p.k) + (size_t)j * p.hkv * kHeadDim + cc * 8;
+      __nv_bfloat16* dst = (is_v ? p.vc : p.kc) + (size_t)slot * p.hkv * kHeadDim + cc * 8;
       *reinterpret_cast<int4*>(dst) = __ldg(reinterpret_cast<const int4*>(src));
     } else {
       const int ch = c - 2 * kv_chunks;
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(128) kv_gather_kernel(const GatherParams p) {
       blk = load_block(p.bt, seq, p.max_blocks, t >> 6, p.num_blocks, &g_status);
     else
       set_status(&g_status, kStBadBlock);
-    const size_t src = (((size_t)blk * p.hkv + g) * kBlock + (t & 63)) * kHeadDim + ch * 8;
+    const size_t src = (((size_t)blk * kBlock + (t & 63)) * p.hkv + g) * kHeadDim + ch * 8;
     kval = __ldg(reinterpret_cast<const int4*>(p.kc + src));
     vval = __ldg(reinterpret_cast<const int4*>(p.vc + src));
   }

@@ -37,9 +37,9 @@ struct CompactParams {
   int32_t* n_sel;
 };
 
-// Cache row (KV head 0) of position t of sequence b.
-__device__ __forceinline__ int row_base(const CompactParams& p, int b, int t) {
-  return load_block(p.bt, b, p.max_blocks, t >> 6, p.num_blocks, &g_status) * p.hkv * kBlock + (t & 63);
+// Cache slot (block * 64 + row) of position t of sequence b.
+__device__ __forceinline__ int slot_of(const CompactParams& p, int b, int t) {
+  return load_block(p.bt, b, p.max_blocks, t >> 6, p.num_blocks, &g_status) * kBlock + (t & 63);
 }
 
 struct MergeSmem {
@@ -152,7 +152,7 @@ __device__ void merge_runs(const CompactParams& p, int b, const int4 sel, MergeS
     const bool take = sc > tau || (sc == tau && tr++ < quota);
     if (take && o < p.k) {
       out[o] = pos;
-      if (p.sel.rowbase) p.sel.rowbase[(size_t)b * p.k + o] = row_base(p, b, pos);
+      if (p.sel.slot) p.sel.slot[(size_t)b * p.k + o] = slot_of(p, b, pos);
     }
     o += take;
   }
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kCompactThreads) decode_compact_kernel(const C
   if (n_cand <= p.k) {  // every candidate is selected: position t goes to slot t - prefix
     for (int t = t_lo + tid; t < t_hi; t += kCompactThreads) {
       out[t - p.prefix] = t;
-      if (p.sel.rowbase) p.sel.rowbase[(size_t)b * p.k + (t - p.prefix)] = row_base(p, b, t);
+      if (p.sel.slot) p.sel.slot[(size_t)b * p.k + (t - p.prefix)] = slot_of(p, b, t);
     }
     if (c == 0) {
       for (int r = n_cand + tid; r < p.k; r += kCompactThreads) out[r] = -1;

@@ -30,7 +30,9 @@
  *   - Launch failures return DSA_ERR_CUDA with the CUDA error text.
  *
  * Data layout (row-major, innermost last)
- *   k_cache, v_cache : bf16 [num_blocks][num_kv_heads][64][128]   one 64 x 128 block per head
+ *   k_cache, v_cache : bf16 [num_blocks][64][num_kv_heads][128]   64 consecutive positions per
+ *                      block; a block row holds every KV head of its position, so the K (or V)
+ *                      of one position is one contiguous num_kv_heads * 256-byte piece
  *   idx_cache        : int8 [num_blocks][64][64]                   indexer key per position
  *   block_table      : int32 [batch][max_blocks_per_seq]           position t of sequence b is
  *                      row t % 64 of block block_table[b][t / 64]

@@ -13,7 +13,8 @@ below refer to that article.  Where the article leaves a step open, the
 reading taken is stated in the function that takes it.
 
 Data layout (shared with the CUDA path only through the seeded generator):
-  k_cache, v_cache : [num_blocks][Hkv][64][d]   (blocks of 64 consecutive positions)
+  k_cache, v_cache : [num_blocks][64][Hkv][d]   (blocks of 64 consecutive positions;
+                     within a block, position-major, the KV heads of a position adjacent)
   idx_cache        : [num_blocks][64][D]        int8 indexer keys
   block_table      : [B][max_blocks]            int32, block id of positions [64j, 64j+64)
 
@@ -39,15 +40,16 @@ def fetch_rows(cache: np.ndarray, bt_row: np.ndarray, positions: np.ndarray,
 
     Section 2.2: the cache is cut into fixed blocks, each holding the values
     of consecutive positions; position t lives in block ``bt_row[t // 64]``
-    at row ``t % 64``.  With ``head`` given the cache is [blk][Hkv][64][d]
-    (K or V), otherwise [blk][64][D] (indexer keys).
+    at row ``t % 64``.  With ``head`` given the cache is [blk][64][Hkv][d]
+    (K or V: one block row holds every KV head of its position), otherwise
+    [blk][64][D] (indexer keys).
     """
     positions = np.asarray(positions, dtype=np.int64)
     blocks = np.asarray(bt_row, dtype=np.int64)[positions // BLOCK]
     rows = positions % BLOCK
     if head is None:
         return cache[blocks, rows]
-    return cache[blocks, head, rows]
+    return cache[blocks, rows, head]
 
 
 # --------------------------------------------------------------------------
@@ -211,11 +213,12 @@ def prefill_query(w: dict, i: int, scale: float | None = None) -> dict:
 # --------------------------------------------------------------------------
 def kv_write(k_cache, v_cache, idx_cache, slot_mapping, k_new, v_new, idx_new):
     """Scatter new tokens into their slots; slot = block_id * 64 + row.
-    Returns updated copies (inputs untouched)."""
+    k_new, v_new: [ntok][Hkv][d]; idx_new: [ntok][D].  Returns updated copies
+    (inputs untouched)."""
     kc, vc, ic = k_cache.copy(), v_cache.copy(), idx_cache.copy()
     for j, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
         blk, row = divmod(int(slot), BLOCK)
-        kc[blk, :, row] = k_new[j]
-        vc[blk, :, row] = v_new[j]
+        kc[blk, row] = k_new[j]
+        vc[blk, row] = v_new[j]
         ic[blk, row] = idx_new[j]
     return kc, vc, ic

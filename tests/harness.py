@@ -92,7 +92,7 @@ def _compact_blocks(w: dict, b: int, positions: np.ndarray, cache: str, head=Non
     ids = torch.as_tensor(bt[jblocks], device=w[cache].device)
     src = w[cache].index_select(0, ids)
     if head is not None:
-        src = src[:, head:head + 1]
+        src = src[:, :, head:head + 1]  # [blk][64][Hkv][d]: keep one KV head
     local_bt = np.full(bt.shape, -1, dtype=np.int64)
     local_bt[jblocks] = np.arange(len(jblocks))
     t = src.cpu()

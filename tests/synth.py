@@ -102,14 +102,14 @@ def make_workload(spec: Spec, seed: int, device="cpu") -> dict:
         off += n
 
     hkv, hq = spec.num_kv_heads, spec.num_q_heads
-    k_cache = _randn_bf16((pool, hkv, BLOCK, HEAD_DIM), _gen(seed, "k_cache", device), device,
+    k_cache = _randn_bf16((pool, BLOCK, hkv, HEAD_DIM), _gen(seed, "k_cache", device), device,
                           chunk_rows=max(1, (1 << 24) // (hkv * BLOCK * HEAD_DIM)))
-    v_cache = _randn_bf16((pool, hkv, BLOCK, HEAD_DIM), _gen(seed, "v_cache", device), device,
+    v_cache = _randn_bf16((pool, BLOCK, hkv, HEAD_DIM), _gen(seed, "v_cache", device), device,
                           chunk_rows=max(1, (1 << 24) // (hkv * BLOCK * HEAD_DIM)))
     if spec.outlier_frac > 0:
-        # One independent Bernoulli draw per (block, kv head, row), i.e. per
-        # (sequence, kv head, position); K only, before use (x4 is exact in bf16).
-        mask = torch.rand((pool, hkv, BLOCK), generator=_gen(seed, "outliers", device),
+        # One independent Bernoulli draw per (block, row, kv head), i.e. per
+        # (sequence, position, kv head); K only, before use (x4 is exact in bf16).
+        mask = torch.rand((pool, BLOCK, hkv), generator=_gen(seed, "outliers", device),
                           device=device) < spec.outlier_frac
         k_cache[mask] = (k_cache[mask].float() * spec.outlier_scale).to(torch.bfloat16)
     idx_cache = torch.randint(spec.idx_lo, spec.idx_hi + 1, (pool, BLOCK, IDX_DIM),

@@ -78,6 +78,8 @@ def _qs(mode=0, n_q=2, seq=0, pos0=0):
     (dict(block_size=32), UNSUPPORTED),
     (dict(head_dim=64), UNSUPPORTED),
     (dict(idx_dim=128), UNSUPPORTED),
+    (dict(num_kv_heads=3), UNSUPPORTED),
+    (dict(num_kv_heads=16), UNSUPPORTED),
     (dict(k_cache=0), INVALID),
     (dict(v_cache=0x20008), INVALID),         # misaligned
     (dict(max_context_len=8 * 64 + 1), INVALID),
@@ -148,7 +150,7 @@ def test_workspace_sizes(lib):
     assert size(0) == 0                       # index_scores needs none
     topk, step = size(1), size(3)
     assert topk >= 2 * 1024 * 4 + 2 * 2048 * 8  # coarse histograms and one run chunk per sequence
-    assert step > topk and step == size(2)     # plus the attention partials and pair tickets
+    assert step > topk and step == size(2)     # plus the selected slots and the attention partials
     # the 128K decode workload: 8 sequences, 64/8 heads, prefix 1024, k 2048
     kv3 = _kv(num_blocks=16384, num_kv_heads=8, max_blocks_per_seq=2048, batch=8, max_context_len=131072)
     qs3 = _qs(n_q=8)

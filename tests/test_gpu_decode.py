@@ -46,9 +46,15 @@ def test_decode_edge_shapes(lib, lens, prefix, k):
     _run(synth.small_spec(batch=len(lens), lens=lens, prefix_len=prefix, k=k, hq=8, hkv=2))
 
 
-@pytest.mark.parametrize("hq,hkv", [(4, 4), (32, 2), (16, 16)])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (32, 2), (8, 8), (16, 1), (64, 8), (8, 1)])
 def test_decode_group_sizes(lib, hq, hkv):
     _run(synth.small_spec(hq=hq, hkv=hkv, lens=(900, 1800)))
+
+
+def test_decode_one_query_over_the_whole_grid(lib):
+    """A single sequence whose attended rows are cut over every CTA of the
+    persistent grid: over a hundred partials per head merged."""
+    _run(synth.small_spec(lens=(9000,), prefix_len=1024, k=2048, hq=64, hkv=8))
 
 
 def test_decode_fp32_output(lib):

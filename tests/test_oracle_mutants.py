@@ -28,7 +28,7 @@ MUTANTS = {
     "lse_without_max": ("lse = m[:, 0] + np.log(l)", "lse = np.log(l)"),
     "row_off_by_one": ("rows = positions % BLOCK", "rows = (positions + 1) % BLOCK"),
     "descending_output": ("chosen = np.sort(chosen)", "chosen = np.sort(chosen)[::-1]"),
-    "kv_head_ignored": ("return cache[blocks, head, rows]", "return cache[blocks, 0, rows]"),
+    "kv_head_ignored": ("return cache[blocks, rows, head]", "return cache[blocks, rows, 0]"),
     "gqa_interleaved_heads": (
         "o, s = softmax_attention(q_heads[g * group:(g + 1) * group], kr, vr, scale)",
         "o, s = softmax_attention(q_heads[g::num_kv_heads], kr, vr, scale)"),

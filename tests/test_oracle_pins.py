@@ -46,8 +46,8 @@ def _tiny_idx_cache(rows_by_pos, nblk, D, bt_row):
 
 
 def _encoded_kv(nblk, hkv, d):
-    """K/V cache whose value encodes (block, head, row, col) exactly."""
-    blk, g, r, c = np.meshgrid(np.arange(nblk), np.arange(hkv), np.arange(O.BLOCK),
+    """K/V cache [blk][64][Hkv][d] whose value encodes (block, head, row, col) exactly."""
+    blk, r, g, c = np.meshgrid(np.arange(nblk), np.arange(O.BLOCK), np.arange(hkv),
                                np.arange(d), indexing="ij")
     return (blk * 1_000_000 + g * 100_000 + r * 1000 + c).astype(np.float64)
 
@@ -367,16 +367,16 @@ def test_gather_closed_form():
 
 def check_kv_write(mod=O):
     rng = np.random.default_rng(4)
-    kc = np.zeros((3, 2, 64, 8))
-    vc = np.zeros((3, 2, 64, 8))
+    kc = np.zeros((3, 64, 2, 8))
+    vc = np.zeros((3, 64, 2, 8))
     ic = np.zeros((3, 64, 4), dtype=np.int64)
     slots = np.array([5, 64 * 2 + 63, 64 + 1])
     kn = rng.standard_normal((3, 2, 8))
     vn = rng.standard_normal((3, 2, 8))
     inn = rng.integers(-8, 9, size=(3, 4))
     k2, v2, i2 = mod.kv_write(kc, vc, ic, slots, kn, vn, inn)
-    ok = np.array_equal(k2[0, :, 5], kn[0]) and np.array_equal(k2[2, :, 63], kn[1])
-    ok &= np.array_equal(v2[1, :, 1], vn[2]) and np.array_equal(i2[2, 63], inn[1])
+    ok = np.array_equal(k2[0, 5], kn[0]) and np.array_equal(k2[2, 63], kn[1])
+    ok &= np.array_equal(v2[1, 1], vn[2]) and np.array_equal(i2[2, 63], inn[1])
     ok &= np.count_nonzero(k2) == kn.size and np.count_nonzero(kc) == 0
     return bool(ok)
 
