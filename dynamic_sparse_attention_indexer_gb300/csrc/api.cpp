@@ -91,8 +91,8 @@ dsa_status check_qs(const dsa_query_set* qs, const dsa::KV& kv, dsa::QS* out) {
     if (qs->n_q != kv.batch) return fail(DSA_ERR_INVALID_ARG, "decode: n_q (%d) must equal batch (%d)", qs->n_q, kv.batch);
     if (kv.batch > dsa::kMaxDecodeBatch)
       return fail(DSA_ERR_UNSUPPORTED, "decode: batch %d above %d", kv.batch, dsa::kMaxDecodeBatch);
-    if (kv.max_ctx > dsa::kCompactChunk * 1024)
-      return fail(DSA_ERR_UNSUPPORTED, "decode: max_context_len above %d", dsa::kCompactChunk * 1024);
+    if (kv.max_ctx > dsa::kMaxDecodeCtx)
+      return fail(DSA_ERR_UNSUPPORTED, "decode: max_context_len above %d", dsa::kMaxDecodeCtx);
   } else if (qs->mode == DSA_MODE_PREFILL) {
     if (qs->n_q < 1) return fail(DSA_ERR_INVALID_ARG, "prefill: n_q must be >= 1");
     if (qs->seq < 0 || qs->seq >= kv.batch) return fail(DSA_ERR_INVALID_ARG, "prefill: seq %d outside [0, batch)", qs->seq);
@@ -122,15 +122,13 @@ dsa_status check_scores(const int32_t* scores, int32_t ld, const dsa::KV& kv, co
   return DSA_OK;
 }
 
-// Workspace regions.  Decode top-k: [coarse histograms | done counters | sel |
-// chunk records | runs | resolved rows]; attention: [partials | pair tickets].
-// The histograms and the counters must be zero when a call starts; every call
-// leaves them zero again.
+// Workspace regions.  Decode top-k: [coarse histograms]; attention: [selected
+// slots | partials].  The histograms must be zero when a call starts; every
+// call leaves them zero again.
 struct Layout {
-  size_t coarse = 0, done_idx = 0, done_cmp = 0, sel = 0, chunk_rec = 0, run_pos = 0, run_score = 0, slot = 0;
+  size_t coarse = 0, slot = 0;
   size_t part_o = 0, part_ml = 0;
   size_t sel_end = 0, attn_begin = 0, total = 0;
-  int n_chunks = 0;
 };
 
 Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
@@ -144,14 +142,7 @@ Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
   };
   if (qs.mode == DSA_MODE_DECODE) {
     const size_t B = (size_t)kv.batch;
-    L.n_chunks = (kv.max_ctx + dsa::kCompactChunk - 1) / dsa::kCompactChunk;
     L.coarse = take(B * dsa::kCoarseBinsHost * 4);
-    L.done_idx = take(B * 4);
-    L.done_cmp = take(B * 4);
-    L.sel = take(B * 16);
-    L.chunk_rec = take(B * L.n_chunks * dsa::kRecInts * 4);
-    L.run_pos = take(B * L.n_chunks * dsa::kCompactChunk * 4);
-    L.run_score = take(B * L.n_chunks * dsa::kCompactChunk * 4);
   }
   L.sel_end = off;
   L.attn_begin = off;
@@ -166,14 +157,7 @@ dsa::SelState sel_state(const Layout& L, void* ws, bool with_slot) {
   char* w = static_cast<char*>(ws);
   dsa::SelState s;
   s.coarse = reinterpret_cast<int*>(w + L.coarse);
-  s.done_idx = reinterpret_cast<int*>(w + L.done_idx);
-  s.done_cmp = reinterpret_cast<int*>(w + L.done_cmp);
-  s.sel = reinterpret_cast<int4*>(w + L.sel);
-  s.chunk_rec = reinterpret_cast<int*>(w + L.chunk_rec);
-  s.run_pos = reinterpret_cast<int*>(w + L.run_pos);
-  s.run_score = reinterpret_cast<int*>(w + L.run_score);
   s.slot = with_slot ? reinterpret_cast<int*>(w + L.slot) : nullptr;
-  s.n_chunks = L.n_chunks;
   return s;
 }
 
@@ -287,7 +271,7 @@ dsa_status prepare_decode_topk(const dsa_paged_kv* kv_, const int32_t* scores, i
   const Layout L = layout(kv, qs, k, kv.hkv, prefix);
   *kv_out = kv;
   *bytes = L.sel_end;
-  *clear_bytes = L.sel;  // histograms and counters come first
+  *clear_bytes = L.sel_end;  // the histograms
   return DSA_OK;
 }
 
@@ -407,7 +391,7 @@ dsa_status dsa_topk_select(const dsa_paged_kv* kv_, const dsa_query_set* qs_, co
     DSA_TRY(ensure_setup());
     const dsa::SelState s = sel_state(L, ws, false);
     DSA_CUDA("top-k histogram launch", dsa::launch_decode_hist(kv, scores, ld, prefix, k, s, stream));
-    DSA_CUDA("top-k compaction launch", dsa::launch_decode_compact(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
+    DSA_CUDA("top-k selection launch", dsa::launch_decode_select(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
   } else {
     DSA_TRY(ensure_setup());
     DSA_CUDA("top-k launch", dsa::launch_prefill_topk(qs, scores, ld, prefix, k, idx, n_sel, stream));
@@ -471,7 +455,7 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t*
   DSA_TRY(ensure_setup());
   const dsa::SelState s = sel_state(L, ws, true);
   DSA_CUDA("decode index launch", dsa::launch_decode_index(kv, q_idx, prefix, scores, ld, &s, k, stream));
-  DSA_CUDA("decode compaction launch", dsa::launch_decode_compact(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
+  DSA_CUDA("decode selection launch", dsa::launch_decode_select(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
   dsa::AttnArgs a;
   a.kv = kv;
   a.qs = qs;

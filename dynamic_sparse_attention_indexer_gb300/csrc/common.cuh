@@ -36,8 +36,6 @@ constexpr int kFineBins = 1 << kCoarseShift;
 
 enum : int { kStOk = 0, kStBadBlock = 4, kStTimeout = 6 };
 enum : int { kSelAll = 1, kSelThreshold = 0 };
-// Decode selection modes kept between the scoring and compaction kernels.
-enum : int { kSelCoarse = 0, kSelExact = 2 };
 
 __device__ __forceinline__ int hist_bin(int s) {
   return min(max(s + kHistOff, 0), kHistBins - 1);
@@ -129,19 +127,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// With cluster_x > 1 the grid is launched in clusters of cluster_x CTAs along x.
 template <typename... Params, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args&&... args) {
+                       int cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -23,26 +23,16 @@ struct QS {
 };
 
 // Decode selection state kept in the workspace between the scoring and the
-// compaction kernels, one entry per sequence.
+// selection kernels.
 struct SelState {
-  int* coarse;      // [B][kCoarseBins]        coarse score histogram, zero between calls
-  int* done_idx;    // [B]                     blocks scored so far, zero between calls
-  int* done_cmp;    // [B]                     compaction chunks done, zero between calls
-  int4* sel;        // [B]                     {mode, lo, width, above}: candidates have s >= lo,
-                    //                         `above` of them have s >= lo + width
-  int* chunk_rec;   // [B][n_chunks][kRecInts] per chunk: run length, count >= lo + width, fine bins
-  int* run_pos;     // [B][n_chunks * kCompactChunk] candidate positions, in order, per chunk
-  int* run_score;   // same: their scores
-  int* slot;        // [B][k] cache slot (block * 64 + row) of each selected position, or nullptr
-  int n_chunks;     // compaction chunks per sequence
+  int* coarse;  // [B][kCoarseBins] coarse score histogram of each sequence; zero between calls
+  int* slot;    // [B][k] cache slot (block * 64 + row) of each selected position, or nullptr
 };
 
-constexpr int kCompactChunk = 2048;   // positions per compaction CTA
-constexpr int kCompactThreads = 256;  // 8 positions per thread
-constexpr int kRecInts = 2 + 16;      // run length, count above, 16 fine bins
 constexpr int kMaxDecodeBatch = 2048;
-constexpr int kMaxAttnCtas = 320;     // persistent attention grid cap (partials are sized for it)
-constexpr int kCoarseBinsHost = 1024; // coarse histogram bins (host-side copy of the device constant)
+constexpr int kMaxDecodeCtx = 1 << 21;  // longest decode context (positions)
+constexpr int kMaxAttnCtas = 320;       // persistent attention grid cap (partials are sized for it)
+constexpr int kCoarseBinsHost = 1024;   // coarse histogram bins (host-side copy of the device constant)
 
 struct AttnWs {
   int* slot;        // [n_q][k]                    cache slot of every selected position
@@ -71,8 +61,8 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
                                 const SelState* sel, int k, cudaStream_t st);
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                const SelState& sel, cudaStream_t st);
-cudaError_t launch_decode_compact(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
-                                  const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st);
+cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
+                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st);
 cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix,
                                  int* scores, int ld, cudaStream_t st);
 cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k,

@@ -188,14 +188,9 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.group;
-  pdl_wait();
-  pdl_trigger();
   if (range_begin(p.tiles, gridDim.x, blockIdx.x) >= range_begin(p.tiles, gridDim.x, blockIdx.x + 1)) return;
 
-  // Rows past a tile's valid count keep whatever an earlier tile left (finite
-  // cache values); the ring starts cleared so that no stale bits are NaN.
-  for (int i = tid; i < kStages * kStageBytes / 16; i += blockDim.x)
-    reinterpret_cast<int4*>(smem)[i] = make_int4(0, 0, 0, 0);
+  // Set-up that touches no global memory runs before the wait on the previous kernel.
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], kProducerThreads);
@@ -206,13 +201,20 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   if (warp < kProducerWarps) {
     // ---------------------------------------------------------- producers
     // Copy c of a tile (K of row c / 2 if c is even, V if odd) is issued by
     // thread (c % 4) * 32 + (c / 4) % 32, so the copies spread over the warps.
+    // Rows from the valid count up to the next multiple of 16 (the rest of the
+    // last 16-row chunk the consumers read) get the last valid row again, so
+    // that every row the math touches holds finite cache values; their
+    // probabilities are zero.
     const int pt = lane * kProducerWarps + warp;
     const int n_copies = 2 * p.rows;
+    auto filled = [&](const Tile& tl) { return min((tl.nvalid + 15) & ~15, p.rows); };
     Cursor cur;
     cursor_init(cur, p);
     Tile t;
@@ -222,7 +224,8 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int c = pt + u * kProducerThreads;
-        raw[u] = (c < n_copies && (c >> 1) < tl.nvalid) ? fetch_raw(p, tl.qf, tl.r0 + (c >> 1)) : 0;
+        raw[u] = (c < n_copies && (c >> 1) < filled(tl)) ? fetch_raw(p, tl.qf, tl.r0 + min(c >> 1, tl.nvalid - 1))
+                                                          : 0;
       }
     };
     if (have) fetch(t);
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int c = pt + u * kProducerThreads;
-        if (c < n_copies && (c >> 1) < t.nvalid) bytes += p.piece;
+        if (c < n_copies && (c >> 1) < filled(t)) bytes += p.piece;
       }
       if (first && pt == 0) {
         if (seg > 0 && !mbar_wait(q_empty, (seg - 1) & 1)) {
@@ -256,9 +259,9 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int c = pt + u * kProducerThreads;
-        if (c < n_copies && (c >> 1) < t.nvalid) {
+        if (c < n_copies && (c >> 1) < filled(t)) {
           const int r = c >> 1;
-          const size_t sl = (size_t)resolve(p, t.qf, t.r0 + r, raw[u]);
+          const size_t sl = (size_t)resolve(p, t.qf, t.r0 + min(r, t.nvalid - 1), raw[u]);
           const __nv_bfloat16* src = ((c & 1) ? p.vc : p.kc) + sl * p.hkv * kHeadDim;
           bulk_g2s(st + (c & 1) * p.rows * p.pitch + r * p.pitch, src, p.piece, &full[s]);
         }
@@ -443,18 +446,16 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 // boundary between CTAs c and c + 1 of the attention grid.  A query cut by the
 // nb boundaries c_lo .. c_hi - 1 has n = nb + 1 partials (one per CTA
 // c_lo .. c_hi); the block of its j-th boundary merges the query heads
-// h = j, j + nb, j + 2 nb, ...  Two dependent rounds of loads: the (max, sum)
-// of every partial (one warp per head, lanes over partials), then the partial
-// outputs, up to 32 in flight per thread.
+// h = j, j + nb, j + 2 nb, ..., four at a time, one thread per (head, column).
+// A thread issues the loads of all its partials at once (up to 32 in flight)
+// and merges them in one pass: no barrier, one round trip per 32 partials.
 constexpr int kCombThreads = 512;
-constexpr int kCombHeads = kCombThreads / 32;  // heads weighed at once (one warp each)
+constexpr int kCombHeads = kCombThreads / kHeadDim;  // heads merged at once
+constexpr int kCombBatch = 32;                      // partials in flight per thread
 
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnParams p, int grid_ctas) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float s_w[kCombHeads][kMaxAttnCtas];  // weight of partial i, normalised
-  __shared__ float s_lse[kCombHeads];
-  __shared__ int s_slot[kMaxAttnCtas];             // partial slot of CTA c_lo + i
   const int T = p.tiles, TP = p.tiles_per_q;
   const int x = range_begin(T, grid_ctas, blockIdx.x + 1);  // first tile of CTA blockIdx.x + 1
   const int qi = x / TP;
@@ -462,57 +463,44 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnPa
   const int first = qi * TP;
   const int c_lo = cta_of(T, grid_ctas, first), c_hi = cta_of(T, grid_ctas, first + TP - 1);
   const int j = (int)blockIdx.x - c_lo, nb = c_hi - c_lo, n = nb + 1;
-  if (j >= p.hq) return;
-  const int my_heads = (p.hq - j + nb - 1) / nb;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < n; i += kCombThreads) {
-    const int c = c_lo + i;
-    s_slot[i] = c * 2 + (range_begin(T, grid_ctas, c) >= first ? 0 : 1);
-  }
-  __syncthreads();
-  auto slot_of = [&](int i) { return (size_t)s_slot[i]; };
-  for (int r0 = 0; r0 < my_heads; r0 += kCombHeads) {
-    const int nh = min(kCombHeads, my_heads - r0);
-    if (warp < nh) {
-      const int h = j + (r0 + warp) * nb;
-      float M = -INFINITY;
-      for (int i = lane; i < n; i += 32) M = fmaxf(M, __ldcg(&p.part_ml[slot_of(i) * p.hq + h]).x);
+  const int d = threadIdx.x & (kHeadDim - 1);
+  // The partial of CTA c for this query sits in slot 0 if the query's segment
+  // starts the CTA's range, else in slot 1.
+  const int c_first = range_begin(T, grid_ctas, c_lo) >= first ? 0 : 1;  // slot of CTA c_lo
+  for (int h = j + (int)(threadIdx.x / kHeadDim) * nb; h < p.hq; h += kCombHeads * nb) {
+    float M = -INFINITY, Lsum = 0.f, acc = 0.f;
+    for (int i0 = 0; i0 < n; i0 += kCombBatch) {
+      float2 ml[kCombBatch];
+      float v[kCombBatch];
 #pragma unroll
-      for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float Ms = M == -INFINITY ? 0.f : M;
-      float L = 0.f;
-      for (int i = lane; i < n; i += 32) {
-        const float2 ml = __ldcg(&p.part_ml[slot_of(i) * p.hq + h]);  // L1 hit: loaded just above
-        const float w = exp2f(ml.x - Ms);
-        s_w[warp][i] = w;
-        L += w * ml.y;
+      for (int u = 0; u < kCombBatch; ++u) {
+        const int i = i0 + u;
+        if (i < n) {
+          const size_t sl = (size_t)(c_lo + i) * 2 + (i == 0 ? c_first : 0);
+          ml[u] = __ldg(&p.part_ml[sl * p.hq + h]);
+          v[u] = __ldg(&p.part_o[(sl * p.hq + h) * kHeadDim + d]);
+        }
       }
+      float Mb = M;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      const float inv = 1.f / L;
-      __syncwarp();
-      for (int i = lane; i < n; i += 32) s_w[warp][i] *= inv;
-      if (lane == 0) s_lse[warp] = (Ms + log2f(L)) * 0.69314718055994531f;
+      for (int u = 0; u < kCombBatch; ++u)
+        if (i0 + u < n) Mb = fmaxf(Mb, ml[u].x);
+      const float Ms = Mb == -INFINITY ? 0.f : Mb;
+      const float a = exp2f(M - Ms);  // rescale of what earlier batches summed
+      Lsum *= a;
+      acc *= a;
+#pragma unroll
+      for (int u = 0; u < kCombBatch; ++u)
+        if (i0 + u < n) {
+          const float w = exp2f(ml[u].x - Ms);
+          Lsum += w * ml[u].y;
+          acc += w * v[u];
+        }
+      M = Mb;
     }
-    __syncthreads();
-    const int d = tid & (kHeadDim - 1);
-    for (int w = tid >> 7; w < nh; w += kCombThreads / kHeadDim) {
-      const int h = j + (r0 + w) * nb;
-      float acc = 0.f;
-      for (int i0 = 0; i0 < n; i0 += 32) {
-        float v[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u)
-          v[u] = i0 + u < n ? __ldcg(&p.part_o[(slot_of(i0 + u) * p.hq + h) * kHeadDim + d]) : 0.f;
-#pragma unroll
-        for (int u = 0; u < 32; ++u)
-          if (i0 + u < n) acc += s_w[w][i0 + u] * v[u];
-      }
-      const size_t head = (size_t)qi * p.hq + h;
-      write_out(p, head, d, acc);
-      if (d == 0 && p.lse) p.lse[head] = s_lse[w];
-    }
-    __syncthreads();
+    const size_t head = (size_t)qi * p.hq + h;
+    write_out(p, head, d, acc / Lsum);
+    if (d == 0 && p.lse) p.lse[head] = ((M == -INFINITY ? 0.f : M) + log2f(Lsum)) * 0.69314718055994531f;
   }
 }
 
@@ -589,18 +577,18 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e;
   if (!a.slot) {  // stand-alone call: resolve the selected positions first
     const long long n = (long long)a.qs.n_q * a.k;
-    e = launch_pdl(resolve_slots_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, a.idx, a.n_sel,
+    e = launch_pdl(resolve_slots_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, 1, a.idx, a.n_sel,
                    a.kv.block_table, a.qs.mode, a.qs.seq, a.qs.n_q, a.k, a.kv.max_blocks, a.kv.num_blocks,
                    a.ws.slot);
     if (e != cudaSuccess) return e;
   }
   const dim3 block(kProducerThreads + 32 * a.kv.hkv);
   if (p.group <= 8)
-    e = launch_pdl(sparse_attn_kernel<1>, dim3(grid), block, kSmemBytes, st, p);
+    e = launch_pdl(sparse_attn_kernel<1>, dim3(grid), block, kSmemBytes, st, 1, p);
   else
-    e = launch_pdl(sparse_attn_kernel<2>, dim3(grid), block, kSmemBytes, st, p);
+    e = launch_pdl(sparse_attn_kernel<2>, dim3(grid), block, kSmemBytes, st, 1, p);
   if (e != cudaSuccess || grid < 2) return e;
-  return launch_pdl(attn_combine_kernel, dim3(grid - 1), dim3(kCombThreads), 0, st, p, grid);
+  return launch_pdl(attn_combine_kernel, dim3(grid - 1), dim3(kCombThreads), 0, st, 1, p, grid);
 }
 
 cudaError_t read_clear_status_attn(int* code, cudaStream_t st) {

@@ -3,18 +3,17 @@
 //
 // Decode: one int8 dot product of 64 per position, a pure HBM stream of 64 B
 // per position.  Whole 4 KB cache blocks are staged into shared memory with
-// mbarrier-tracked bulk copies, several blocks in flight per CTA; each thread
-// scores one position with __dp4a.  The fused variant also builds the score
-// histogram the top-k needs (shared-memory bins merged into a per-sequence
-// global histogram); the last CTA of a sequence turns it into the selection
-// threshold, so no extra pass over the scores is needed.
+// mbarrier-tracked bulk copies by a producer warp, ten 16 KB stages in flight
+// per SM; consumer warps score one position per thread with __dp4a.  The fused
+// variant also builds the coarse score histogram the top-k needs (per-warp
+// shared-memory bins added into a per-sequence global histogram), so the
+// selection needs no extra pass over the scores to find its threshold window.
 //
 // Prefill: the causal [T x 64] . [64 x L] int8 product on the tensor cores
 // (mma.sync m16n8k32 s8, exact int32), 128 x 128 output tiles, fully masked
 // tiles skipped.
 #include "common.cuh"
 #include "internal.h"
-#include "select.cuh"
 
 namespace dsa {
 namespace {
@@ -23,21 +22,28 @@ __device__ int g_status;
 
 // ---------------------------------------------------------------- decode ---
 // Persistent scoring: the candidate blocks of all sequences, [P / 64, ceil(L_b / 64))
-// for each b, are laid end to end and cut into one contiguous range per CTA.  A CTA
-// stages whole 4 KB blocks into shared memory with bulk copies (groups of up to four
-// blocks of one sequence, five groups in flight), each thread scores one position.
-constexpr int kIdxThreads = 256;
-constexpr int kIdxStages = 5;
+// for each b, are laid end to end and cut into one contiguous range per CTA (one
+// CTA per SM).  Warp roles: lanes 0-3 of warp 0 stage groups of up to four
+// whole 4 KB blocks of one sequence with bulk copies into a ring of
+// kIdxStages 16 KB stages (mbarrier full / empty per stage); the eight
+// consumer warps score one position per thread with __dp4a and release the
+// stage, with no CTA-wide barrier per group.  Every warp walks the same group
+// sequence, computed from the block ranges.  With the histogram, each consumer
+// warp counts its scores into its own shared 1024-bin coarse histogram and adds
+// it to the sequence's global histogram when its sequence changes (fire-and-
+// forget atomics; the selection kernel reads the completed histogram).
+constexpr int kIdxConsumers = 8;                               // consumer warps
+constexpr int kIdxThreads = 32 * (1 + kIdxConsumers);          // 288
+constexpr int kIdxStages = 10;
 constexpr int kGroupBlocks = 4;                                // cache blocks per stage
 constexpr int kIdxBlockBytes = kBlock * kIdxDim;               // 4096
 constexpr int kIdxStageBytes = kGroupBlocks * kIdxBlockBytes;  // 16 KB
-constexpr int kMaxRange = 1024;                                // candidate blocks per CTA at most
-constexpr int kScratchInts = 264;
+constexpr int kMaxRange = 2048;                                // candidate blocks per CTA at most
+constexpr int kScratchInts = 64;
 
 constexpr int idx_smem_bytes() {
-  return kIdxStages * kIdxStageBytes + 16 * kIdxStages /*meta*/ + 8 * kIdxStages /*bars*/ +
-         4 * (2 * kMaxDecodeBatch + 1) /*seg_start, len*/ + 4 * kMaxRange /*ids*/ + 4 * kCoarseBins /*hist*/ +
-         4 * kScratchInts;
+  return kIdxStages * kIdxStageBytes + 16 * kIdxStages /*bars*/ + 4 * (2 * kMaxDecodeBatch + 1) /*seg_start, len*/ +
+         4 * kMaxRange /*ids*/ + 4 * kIdxConsumers * kCoarseBins /*hist*/ + 4 * kScratchInts + 16;
 }
 
 struct DecodeIndexParams {
@@ -46,8 +52,8 @@ struct DecodeIndexParams {
   const int32_t* ctx;
   const int8_t* q_idx;
   int* scores;
+  int* coarse;  // [B][kCoarseBins] global histograms, or nullptr
   int ld, max_blocks, num_blocks, prefix, max_ctx, batch, k;
-  SelState sel;
 };
 
 // Candidate blocks of every sequence and their prefix sums: seg_start[b] is the
@@ -72,206 +78,189 @@ __device__ void candidate_blocks(const int32_t* __restrict__ ctx, int batch, int
   __syncthreads();
 }
 
-// Selection of sequence b from its complete coarse histogram (the CTA whose
-// counts completed it); leaves the histogram and the counter at zero.
-__device__ void decode_finish(const SelState& st, int b, const int* cand_scores, int n_cand, int k,
-                              int* scratch) {
-  int* gh = st.coarse + (size_t)b * kCoarseBins;
-  int beta, above;
-  hist_threshold_bin<kCoarseBins>([gh](int i) { return __ldcg(gh + i); }, k, scratch, &beta, &above);
-  if (beta > 0 && beta < kCoarseBins - 1) {
-    if (threadIdx.x == 0) st.sel[b] = make_int4(kSelCoarse, (beta - kCoarseOff) * kFineBins, kFineBins, above);
-  } else {
-    int tau, n_gt;
-    block_radix_select(cand_scores, n_cand, k, scratch, &tau, &n_gt);
-    if (threadIdx.x == 0) st.sel[b] = make_int4(kSelExact, tau, 1, n_gt);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) gh[i] = 0;
-  if (threadIdx.x == 0) st.done_idx[b] = 0;
+// The group sequence of a CTA range: groups of up to kGroupBlocks consecutive
+// candidate blocks of one sequence.
+struct GroupCursor {
+  int f, f_end, b;
+};
+struct Group {
+  int b, jb, count;  // sequence, block-table index of the first block, blocks
+};
+__device__ __forceinline__ bool next_group(GroupCursor& c, const int* seg_start, int jb_base, Group* g) {
+  if (c.f >= c.f_end) return false;
+  while (seg_start[c.b + 1] <= c.f) ++c.b;  // skip sequences without candidates
+  g->b = c.b;
+  g->jb = c.f - seg_start[c.b] + jb_base;
+  g->count = min(kGroupBlocks, min(c.f_end, seg_start[c.b + 1]) - c.f);
+  c.f += g->count;
+  return true;
 }
 
-// Adds this CTA's histogram of sequence b (covering `counted` candidates) to the
-// sequence's and, if that completes it, computes the selection.
-__device__ void flush_hist(const SelState& st, int* hist, int b, int counted, const int* cand_scores, int n_cand,
-                           int k, int* scratch) {
-  __syncthreads();
-  int* gh = st.coarse + (size_t)b * kCoarseBins;
-  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) {
-    const int h = hist[i];
+// Adds a consumer warp's histogram of sequence b to the global one and clears it.
+__device__ __forceinline__ void flush_warp_hist(int* whist, int* gh, int lane) {
+  for (int i = lane; i < kCoarseBins; i += 32) {
+    const int h = whist[i];
     if (h) {
       atomicAdd(gh + i, h);
-      hist[i] = 0;
+      whist[i] = 0;
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) scratch[263] = (atomicAdd(st.done_idx + b, counted) + counted == n_cand);
-  __syncthreads();
-  const bool last = scratch[263] != 0;
-  __syncthreads();
-  if (last) {
-    __threadfence();
-    decode_finish(st, b, cand_scores, n_cand, k, scratch);
-    __syncthreads();
-  }
+  __syncwarp();
 }
 
 template <bool kHist>
-__global__ void __launch_bounds__(kIdxThreads) decode_index_kernel(const DecodeIndexParams p) {
+__global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const DecodeIndexParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  int4* meta = reinterpret_cast<int4*>(smem + kIdxStages * kIdxStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(meta + kIdxStages);
-  int* seg_start = reinterpret_cast<int*>(bars + kIdxStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kIdxStages * kIdxStageBytes);
+  uint64_t* empty = full + kIdxStages;
+  int* seg_start = reinterpret_cast<int*>(empty + kIdxStages);
   int* len = seg_start + kMaxDecodeBatch + 1;
   int* ids = len + kMaxDecodeBatch;
   int* hist = ids + kMaxRange;
-  int* scratch = hist + kCoarseBins;
+  int* scratch = hist + kIdxConsumers * kCoarseBins;
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = p.prefix, jb_base = P / kBlock;
+  pdl_wait();
+  pdl_trigger();
   candidate_blocks(p.ctx, p.batch, p.max_ctx, P, seg_start, len, scratch);
   const long long T = seg_start[p.batch];
   const int f_begin = (int)(T * blockIdx.x / gridDim.x), f_end = (int)(T * (blockIdx.x + 1) / gridDim.x);
   if (f_begin >= f_end) return;
-
-  // Block ids of the whole range, loaded in parallel (validated against the pool).
+  int b_first = 0;  // sequence of the range's first block
   {
-    int b = 0;
-    for (int f = f_begin + tid; f < f_end; f += kIdxThreads) {
-      int lo = 0, hi = p.batch - 1;  // last b with seg_start[b] <= f
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (seg_start[mid] <= f) lo = mid; else hi = mid - 1;
-      }
-      b = lo;
-      ids[f - f_begin] = load_block(p.bt, b, p.max_blocks, f - seg_start[b] + jb_base, p.num_blocks, &g_status);
+    int lo = 0, hi = p.batch - 1;  // last b with seg_start[b] <= f_begin
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (seg_start[mid] <= f_begin) lo = mid; else hi = mid - 1;
     }
+    b_first = lo;
+  }
+  // Block ids of the whole range, loaded in parallel (validated against the pool).
+  for (int f = f_begin + tid; f < f_end; f += kIdxThreads) {
+    int lo = b_first, hi = p.batch - 1;  // last b with seg_start[b] <= f
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (seg_start[mid] <= f) lo = mid; else hi = mid - 1;
+    }
+    ids[f - f_begin] = load_block(p.bt, lo, p.max_blocks, f - seg_start[lo] + jb_base, p.num_blocks, &g_status);
   }
   if (kHist)
-    for (int i = tid; i < kCoarseBins; i += kIdxThreads) hist[i] = 0;
+    for (int i = tid; i < kIdxConsumers * kCoarseBins; i += kIdxThreads) hist[i] = 0;
   if (tid == 0) {
-    for (int s = 0; s < kIdxStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kIdxStages; ++s) {
+      mbar_init(&full[s], kGroupBlocks);
+      mbar_init(&empty[s], kIdxConsumers);
+    }
     mbar_fence_init();
   }
   __syncthreads();
+  GroupCursor cur{f_begin, f_end, b_first};
+  Group g;
 
-  // Producer state (thread 0): next block to issue and its sequence.
-  int f_next = f_begin, b_next = 0;
-  if (tid == 0) {
-    int lo = 0, hi = p.batch - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (seg_start[mid] <= f_next) lo = mid; else hi = mid - 1;
+  if (warp == 0) {
+    // ---- producer: lane i < 4 copies block i of each group
+    if (lane >= kGroupBlocks) return;
+    for (int n = 0; next_group(cur, seg_start, jb_base, &g); ++n) {
+      const int s = n % kIdxStages;
+      if (n >= kIdxStages && !mbar_wait(&empty[s], ((n / kIdxStages) - 1) & 1)) {
+        set_status(&g_status, kStTimeout);
+        return;
+      }
+      const bool mine = lane < g.count;
+      mbar_arrive_expect_tx(&full[s], mine ? kIdxBlockBytes : 0);
+      if (mine) {
+        const int f = cur.f - g.count + lane;  // flattened block of this lane
+        bulk_g2s(stages + s * kIdxStageBytes + lane * kIdxBlockBytes,
+                 p.idx_cache + (size_t)ids[f - f_begin] * kIdxBlockBytes, kIdxBlockBytes, &full[s]);
+      }
     }
-    b_next = lo;
+    return;
   }
-  int n_groups_issued = 0;  // thread 0
-  auto issue = [&]() {      // thread 0 only; returns false at the end of the range
-    if (f_next >= f_end) return false;
-    while (seg_start[b_next + 1] <= f_next) ++b_next;  // skip sequences without candidates
-    const int s = n_groups_issued % kIdxStages;
-    const int count = min(kGroupBlocks, min(f_end, seg_start[b_next + 1]) - f_next);
-    meta[s] = make_int4(b_next, f_next - seg_start[b_next] + jb_base, count, 0);
-    mbar_arrive_expect_tx(&bars[s], count * kIdxBlockBytes);
-    for (int i = 0; i < count; ++i)
-      bulk_g2s(stages + s * kIdxStageBytes + i * kIdxBlockBytes,
-               p.idx_cache + (size_t)ids[f_next - f_begin + i] * kIdxBlockBytes, kIdxBlockBytes, &bars[s]);
-    f_next += count;
-    ++n_groups_issued;
-    return true;
-  };
-  if (tid == 0)
-    for (int s = 0; s < kIdxStages; ++s)
-      if (!issue()) break;
 
-  const int slot = tid >> 6, r = tid & 63;
+  // ---- consumers: warp cw scores rows 32 (cw % 2) .. + 31 of block cw / 2 of each
+  // group.  Four lanes share a row, lane l taking the 16-byte chunk l % 4 of the
+  // key (so its query chunk is fixed and the warp's shared-memory reads are 512
+  // contiguous bytes), and a two-step shuffle sums the four partial dot products.
+  const int cw = warp - 1;
+  const int blk = cw >> 1, row0 = (cw & 1) * 32;
+  int* whist = hist + cw * kCoarseBins;
   int qb = -1;
-  int4 q[4];
-  int hist_b = -1, counted = 0;  // sequence whose counts sit in `hist`, candidates counted
-  for (int g = 0;; ++g) {
-    // All threads learn whether group g exists: thread 0 issued it before this point.
-    if (tid == 0) scratch[262] = g < n_groups_issued;
-    __syncthreads();
-    if (!scratch[262]) break;
-    const int s = g % kIdxStages;
-    const bool ok = mbar_wait(&bars[s], (g / kIdxStages) & 1);
-    if (!ok) set_status(&g_status, kStTimeout);
-    const int4 m = meta[s];
-    const int b = m.x, L = len[m.x];
-    const int n_cand = L - P;
-    const bool want_hist = kHist && n_cand > p.k;
+  int4 qc = make_int4(0, 0, 0, 0);  // chunk lane % 4 of the current sequence's query
+  int hist_b = -1;                  // sequence whose counts sit in whist
+  for (int n = 0; next_group(cur, seg_start, jb_base, &g); ++n) {
+    const int s = n % kIdxStages;
+    const int b = g.b, L = len[b];
+    const bool want_hist = kHist && L - P > p.k;
     if (kHist && b != hist_b) {
-      if (hist_b >= 0 && counted > 0)
-        flush_hist(p.sel, hist, hist_b, counted, p.scores + (size_t)hist_b * p.ld + P, len[hist_b] - P, p.k,
-                   scratch);
+      if (hist_b >= 0) flush_warp_hist(whist, p.coarse + (size_t)hist_b * kCoarseBins, lane);
       hist_b = want_hist ? b : -1;
-      counted = 0;
     }
-    const int t = (m.y + slot) * kBlock + r;
-    const bool valid = ok && slot < m.z && t >= P && t < L;
-    if (valid) {
-      if (b != qb) {
-        const int4* src = reinterpret_cast<const int4*>(p.q_idx + (size_t)b * kIdxDim);
-        q[0] = __ldg(src), q[1] = __ldg(src + 1), q[2] = __ldg(src + 2), q[3] = __ldg(src + 3);
-        qb = b;
-      }
-      const int4* row = reinterpret_cast<const int4*>(stages + s * kIdxStageBytes + slot * kIdxBlockBytes + r * kIdxDim);
-      int acc = 0;
+    if (b != qb) {
+      qc = __ldg(reinterpret_cast<const int4*>(p.q_idx + (size_t)b * kIdxDim) + (lane & 3));
+      qb = b;
+    }
+    if (!mbar_wait(&full[s], (n / kIdxStages) & 1)) {
+      set_status(&g_status, kStTimeout);
+      break;
+    }
+    if (blk < g.count) {
+      const uint8_t* base = stages + s * kIdxStageBytes + blk * kIdxBlockBytes + row0 * kIdxDim;
+      int mine = 0;  // score of row row0 + lane
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int jj = (j + (r >> 1)) & 3;  // rotate 16-B chunks: conflict-free smem reads
-        const int4 kv = row[jj];
-        const int4 qv = jj == 0 ? q[0] : jj == 1 ? q[1] : jj == 2 ? q[2] : q[3];
-        acc = dot4(kv.x, qv.x, acc);
-        acc = dot4(kv.y, qv.y, acc);
-        acc = dot4(kv.z, qv.z, acc);
-        acc = dot4(kv.w, qv.w, acc);
+      for (int i = 0; i < 4; ++i) {
+        const int4 kv = *reinterpret_cast<const int4*>(base + (8 * i + (lane >> 2)) * kIdxDim + (lane & 3) * 16);
+        int acc = dot4(kv.x, qc.x, 0);
+        acc = dot4(kv.y, qc.y, acc);
+        acc = dot4(kv.z, qc.z, acc);
+        acc = dot4(kv.w, qc.w, acc);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        const int v = __shfl_sync(0xffffffffu, acc, 4 * (lane & 7));  // row 8 i + lane % 8
+        if ((lane >> 3) == i) mine = v;
       }
-      p.scores[(size_t)b * p.ld + t] = acc;
-      if (want_hist) atomicAdd(&hist[coarse_bin(acc)], 1);
+      const int t = (g.jb + blk) * kBlock + row0 + lane;
+      if (t >= P && t < L) {
+        p.scores[(size_t)b * p.ld + t] = mine;
+        if (want_hist) atomicAdd(&whist[coarse_bin(mine)], 1);
+      }
     }
-    if (want_hist) {
-      // Candidates of this group: positions [max(P, first), min(L, last + 1)).
-      const int first = max(P, m.y * kBlock), last = min(L, (m.y + m.z) * kBlock);
-      counted += last - first;
-    }
-    if (__syncthreads_or(!ok)) {
-      // A wait ran out: give the copies in flight a bounded chance to land, then leave.
-      if (tid == 0)
-        for (int gg = g; gg < n_groups_issued; ++gg) mbar_wait(&bars[gg % kIdxStages], (gg / kIdxStages) & 1);
-      return;
-    }
-    if (tid == 0) issue();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
-  if (kHist && hist_b >= 0 && counted > 0)
-    flush_hist(p.sel, hist, hist_b, counted, p.scores + (size_t)hist_b * p.ld + P, len[hist_b] - P, p.k, scratch);
+  if (kHist && hist_b >= 0) flush_warp_hist(whist, p.coarse + (size_t)hist_b * kCoarseBins, lane);
 }
 
 // Coarse histogram of existing scores (the stand-alone top-k call): one CTA per
-// chunk of kCompactChunk positions of a sequence.
+// chunk of kHistChunk positions of a sequence, added to the sequence's global
+// histogram with fire-and-forget atomics.
+constexpr int kHistChunk = 2048;
 struct DecodeHistParams {
   const int32_t* scores;
   const int32_t* ctx;
+  int* coarse;
   int ld, prefix, k, max_ctx;
-  SelState sel;
 };
 
 __global__ void __launch_bounds__(256) decode_hist_kernel(const DecodeHistParams p) {
   __shared__ int hist[kCoarseBins];
-  __shared__ int scratch[kScratchInts];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y, c = blockIdx.x;
   const int L = min(__ldg(p.ctx + b), p.max_ctx);
   const int n_cand = L - p.prefix;
-  if (n_cand <= p.k) return;  // the compaction takes every candidate
-  const int t_lo = max(p.prefix, c * kCompactChunk), t_hi = min(L, (c + 1) * kCompactChunk);
+  if (n_cand <= p.k) return;  // the selection takes every candidate
+  const int t_lo = max(p.prefix, c * kHistChunk), t_hi = min(L, (c + 1) * kHistChunk);
   if (t_lo >= t_hi) return;
   for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int32_t* row = p.scores + (size_t)b * p.ld;
   for (int t = t_lo + threadIdx.x; t < t_hi; t += blockDim.x) atomicAdd(&hist[coarse_bin(__ldg(row + t))], 1);
-  flush_hist(p.sel, hist, b, t_hi - t_lo, row + p.prefix, n_cand, p.k, scratch);
+  __syncthreads();
+  int* gh = p.coarse + (size_t)b * kCoarseBins;
+  for (int i = threadIdx.x; i < kCoarseBins; i += blockDim.x)
+    if (hist[i]) atomicAdd(gh + i, hist[i]);
 }
 
 // --------------------------------------------------------------- prefill ---
@@ -389,7 +378,7 @@ cudaError_t setup_index_kernels() {
 static int index_grid(const KV& kv, int prefix) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const int base = (dev >= 0 && dev < 64 && g_index_grid[dev] > 0) ? g_index_grid[dev] : 304;
+  const int base = (dev >= 0 && dev < 64 && g_index_grid[dev] > 0) ? g_index_grid[dev] : 148;
   // Upper bound of the candidate blocks; every CTA range must fit kMaxRange ids.
   const long long per_seq = (kv.max_ctx + kBlock - 1) / kBlock - prefix / kBlock;
   const long long t_max = (long long)kv.batch * (per_seq > 0 ? per_seq : 0);
@@ -405,6 +394,7 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
   p.ctx = kv.context_lens;
   p.q_idx = q_idx;
   p.scores = scores;
+  p.coarse = sel ? sel->coarse : nullptr;
   p.ld = ld;
   p.max_blocks = kv.max_blocks;
   p.num_blocks = kv.num_blocks;
@@ -412,13 +402,9 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
   p.max_ctx = kv.max_ctx;
   p.batch = kv.batch;
   p.k = k;
-  if (sel) p.sel = *sel;
   const int grid = index_grid(kv, prefix);
-  if (sel)
-    decode_index_kernel<true><<<grid, kIdxThreads, idx_smem_bytes(), st>>>(p);
-  else
-    decode_index_kernel<false><<<grid, kIdxThreads, idx_smem_bytes(), st>>>(p);
-  return cudaGetLastError();
+  if (sel) return launch_pdl(decode_index_kernel<true>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1, p);
+  return launch_pdl(decode_index_kernel<false>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1, p);
 }
 
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
@@ -426,14 +412,13 @@ cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int 
   DecodeHistParams p;
   p.scores = scores;
   p.ctx = kv.context_lens;
+  p.coarse = sel.coarse;
   p.ld = ld;
   p.prefix = prefix;
   p.k = k;
   p.max_ctx = kv.max_ctx;
-  p.sel = sel;
-  dim3 grid((kv.max_ctx + kCompactChunk - 1) / kCompactChunk, kv.batch);
-  decode_hist_kernel<<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  dim3 grid((kv.max_ctx + kHistChunk - 1) / kHistChunk, kv.batch);
+  return launch_pdl(decode_hist_kernel, grid, dim3(256), 0, st, 1, p);
 }
 
 cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix, int* scores,

@@ -1,12 +1,10 @@
 // Step 2 of DSA (§2.1 top-k, §2.4 prefix never selected): turn scores and the
 // selection threshold into the ascending list of selected positions.
 //
-// Decode (few queries, long rows): many CTAs per sequence.  Each compaction CTA
-// owns 2048 positions and writes, in position order, every candidate at or
-// above the threshold together with its rank among the ties of its chunk.  The
-// last CTA of a sequence (ticket counter, no spin) lays the runs end to end:
-// ties before a chunk decide how many of its ties are kept, so the lower
-// positions win, and the result is deterministic and ascending.
+// Decode (few queries, long rows): one cluster of CTAs per sequence, the CTAs
+// exchanging their counts through distributed shared memory (below).  The
+// result is deterministic and ascending; among equal scores the lower
+// positions win.
 //
 // Prefill (many rows of at most a few ten thousand candidates): one CTA per
 // query row builds its histogram in shared memory, finds the threshold and
@@ -22,223 +20,303 @@ namespace {
 
 __device__ int g_status;
 
-constexpr int kPer = kCompactChunk / kCompactThreads;  // 8 consecutive positions per thread
-static_assert(kPer == 8, "compaction assumes 8 positions per thread");
-constexpr int kStageEntries = 4096;                      // merge entries staged in shared memory
-constexpr int kMaxChunks = 1024;                         // compaction chunks per sequence at most
+// Decode selection: one thread-block cluster of kSelCluster CTAs per sequence.
+// CTA rank r owns the r-th of kSelCluster equal parts of the candidates
+// [prefix, L).  Every CTA reads the sequence's coarse histogram (built by the
+// scoring kernel, bins 16 scores wide) and finds the bin that holds the k-th
+// largest score: the window [lo, lo + 16) and the number `above` of candidates
+// above it (an edge bin sends the sequence to an exact radix select over its
+// scores, window one score wide).  Then:
+//   1. every CTA counts, in its part, the candidates in each one-score-wide
+//      fine bin of the window and those above it;
+//   2. the counts of all ranks are exchanged through distributed shared
+//      memory; each CTA derives the exact threshold tau (the k-th largest
+//      score), the number of ties at tau to keep (quota), and how many
+//      selected positions and ties at tau lie in the parts before its own;
+//   3. each CTA writes its selected positions, in order, at that offset (ties
+//      at tau are kept while their rank over the whole sequence is below the
+//      quota, so the lower positions win).
+// Step 1 also keeps the part's candidates at or above the window (about 2% of
+// the positions at 128K) in position order in shared memory, with their cache
+// slots, so step 3 reads only those; a part with more than kSelCap of them
+// rescans its scores (L2-resident, 4 bytes per position).  No global atomics,
+// no fences, no hand-off between CTAs beyond two cluster barriers.
+constexpr int kSelCluster = 8;
+constexpr int kSelThreads = 512;
+constexpr int kSelPer = 32;                          // consecutive positions per thread per round
+constexpr int kSelRound = kSelThreads * kSelPer;     // 16384 positions per round
+constexpr int kCounts = 1 + kFineBins;               // above, fine bins
 
-struct CompactParams {
+struct SelectParams {
   const int32_t* scores;
   const int32_t* ctx;
   const int32_t* bt;
-  int ld, prefix, k, max_ctx, max_blocks, num_blocks, hkv;
-  SelState sel;
+  int* coarse;  // [B][kCoarseBins], zeroed again here after use
+  int ld, prefix, k, max_ctx, max_blocks, num_blocks;
   int32_t* idx;
   int32_t* n_sel;
+  int32_t* slot;  // cache slots of the selected positions, or nullptr
 };
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Barrier over every thread of the cluster; orders shared-memory writes before
+// it with reads after it, across the cluster's CTAs.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Cache slot (block * 64 + row) of position t of sequence b.
-__device__ __forceinline__ int slot_of(const CompactParams& p, int b, int t) {
+__device__ __forceinline__ int slot_of(const SelectParams& p, int b, int t) {
   return load_block(p.bt, b, p.max_blocks, t >> 6, p.num_blocks, &g_status) * kBlock + (t & 63);
 }
 
-struct MergeSmem {
-  int ent_pos[kStageEntries];
-  int ent_score[kStageEntries];
-  int run_off[kMaxChunks + 1];
-  int fine[kFineBins];
-  int misc[8];
-  int scratch[40];
-};
-
-// Run entry e (flattened over the chunks of sequence b, in position order).
-__device__ __forceinline__ void load_entry(const CompactParams& p, const MergeSmem& sm, int b, int nch, int e,
-                                           bool staged, int* pos, int* score) {
-  if (staged) {
-    *pos = sm.ent_pos[e];
-    *score = sm.ent_score[e];
-    return;
-  }
-  int lo = 0, hi = nch - 1;  // last chunk with run_off <= e
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (sm.run_off[mid] <= e) lo = mid; else hi = mid - 1;
-  }
-  const size_t at = ((size_t)b * nch + lo) * kCompactChunk + (e - sm.run_off[lo]);
-  *pos = __ldcg(p.sel.run_pos + at);
-  *score = __ldcg(p.sel.run_score + at);
+// Reads an int of CTA `rank`'s shared memory at the address of `p` in this CTA.
+__device__ __forceinline__ int ld_remote(const int* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
 }
 
-// The last compaction CTA of sequence b: exact threshold from the fine bins,
-// then every candidate run, in position order, filtered and written out.
-__device__ void merge_runs(const CompactParams& p, int b, const int4 sel, MergeSmem& sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nch = p.sel.n_chunks;
-  const int lo = sel.y, width = sel.z, above = sel.w;
-  if (tid < kFineBins) sm.fine[tid] = 0;
-  __syncthreads();
-  // Fine-bin totals and run offsets (chunks in order).
-  int carry = 0;
-  for (int base = 0; base < nch; base += kCompactThreads) {
-    const int c = base + tid;
-    int run_len = 0;
-    if (c < nch) {
-      const int* rec = p.sel.chunk_rec + ((size_t)b * nch + c) * kRecInts;
-      run_len = __ldcg(rec);
-      for (int f = 0; f < width; ++f) {
-        const int v = __ldcg(rec + 2 + f);
-        if (v) atomicAdd(&sm.fine[f], v);
-      }
-    }
-    int tot;
-    const int ex = block_exclusive_scan(run_len, sm.scratch, &tot);
-    if (c < nch) sm.run_off[c] = carry + ex;
-    carry += tot;
-  }
-  __syncthreads();
-  const int E = carry;
-  if (tid == 0) {
-    sm.run_off[nch] = E;
-    // The k-th largest lies in fine bin f*: fewer than k - above candidates sit above it.
-    const int kk = p.k - above;
-    int cum = 0, fstar = 0;
-    for (int f = width - 1; f >= 0; --f) {
-      if (cum + sm.fine[f] >= kk) {
-        fstar = f;
-        break;
-      }
-      cum += sm.fine[f];
-    }
-    sm.misc[0] = lo + fstar;        // tau
-    sm.misc[1] = p.k - above - cum;  // quota of ties at tau
-  }
-  __syncthreads();
-  const int tau = sm.misc[0], quota = sm.misc[1];
-  const bool staged = E <= kStageEntries;
-  if (staged) {
-    for (int c = warp; c < nch; c += kCompactThreads / 32) {
-      const size_t run = ((size_t)b * nch + c) * kCompactChunk;
-      const int off = sm.run_off[c], n = sm.run_off[c + 1] - off;
-      for (int j = lane; j < n; j += 32) {
-        sm.ent_pos[off + j] = __ldcg(p.sel.run_pos + run + j);
-        sm.ent_score[off + j] = __ldcg(p.sel.run_score + run + j);
-      }
-    }
-    __syncthreads();
-  }
-  // Each thread owns a contiguous slice of the entries.
-  const int per = (E + kCompactThreads - 1) / kCompactThreads;
-  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-  int n_eq = 0;
-  for (int e = e0; e < e1; ++e) {
-    int pos, sc;
-    load_entry(p, sm, b, nch, e, staged, &pos, &sc);
-    n_eq += sc == tau;
-  }
-  int tot;
-  int tie = block_exclusive_scan(n_eq, sm.scratch, &tot);  // ties before this slice
-  int n_take = 0;
-  for (int e = e0, tr = tie; e < e1; ++e) {
-    int pos, sc;
-    load_entry(p, sm, b, nch, e, staged, &pos, &sc);
-    if (sc > tau) ++n_take;
-    else if (sc == tau) n_take += tr++ < quota;
-  }
-  int o = block_exclusive_scan(n_take, sm.scratch, &tot);
-  int32_t* out = p.idx + (size_t)b * p.k;
-  for (int e = e0, tr = tie; e < e1; ++e) {
-    int pos, sc;
-    load_entry(p, sm, b, nch, e, staged, &pos, &sc);
-    const bool take = sc > tau || (sc == tau && tr++ < quota);
-    if (take && o < p.k) {
-      out[o] = pos;
-      if (p.sel.slot) p.sel.slot[(size_t)b * p.k + o] = slot_of(p, b, pos);
-    }
-    o += take;
-  }
-  const int n_out = min(tot, p.k);
-  for (int r = n_out + tid; r < p.k; r += kCompactThreads) out[r] = -1;
-  if (tid == 0) {
-    p.n_sel[b] = n_out;
-    p.sel.done_cmp[b] = 0;
+// Scores of positions t .. t + 31 (t a multiple of 32) kept where lo_t <= t' < hi_t,
+// INT_MIN elsewhere; never reads past the row's ld entries.
+__device__ __forceinline__ void load_scores(const int32_t* row, int ld, int t, int lo_t, int hi_t, int* v) {
+#pragma unroll
+  for (int q = 0; q < kSelPer / 4; ++q) {
+    const int tq = t + 4 * q;
+    int4 x = make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+    if (tq < ld && tq + 4 > lo_t && tq < hi_t) x = __ldg(reinterpret_cast<const int4*>(row + tq));
+    v[4 * q] = tq >= lo_t && tq < hi_t ? x.x : INT_MIN;
+    v[4 * q + 1] = tq + 1 >= lo_t && tq + 1 < hi_t ? x.y : INT_MIN;
+    v[4 * q + 2] = tq + 2 >= lo_t && tq + 2 < hi_t ? x.z : INT_MIN;
+    v[4 * q + 3] = tq + 3 >= lo_t && tq + 3 < hi_t ? x.w : INT_MIN;
   }
 }
 
-__global__ void __launch_bounds__(kCompactThreads) decode_compact_kernel(const CompactParams p) {
-  __shared__ MergeSmem sm;
-  __shared__ int s_fine[kFineBins];
-  __shared__ int s_last;
-  const int tid = threadIdx.x, b = blockIdx.y, c = blockIdx.x;
+// Candidates at or above the window kept in shared memory per CTA (position,
+// score, slot); a part with more falls back to rescanning its scores.
+constexpr int kSelCap = 4096;
+constexpr int kSelSmem = kSelCap * 3 * 4;
+
+
+__global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) int s_ent[];     // [kSelCap] positions | scores | slots
+  __shared__ int s_counts[kCounts];                // this rank's: above, fine bins
+  __shared__ int s_all[kSelCluster][kCounts];      // every rank's
+  __shared__ int s_misc[4];                        // tau, quota, ties before, output base
+  __shared__ int s_scratch[264];
+  int* e_pos = s_ent;
+  int* e_sc = s_ent + kSelCap;
+  int* e_slot = s_ent + 2 * kSelCap;
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, b = blockIdx.y;
+  const int r = (int)cluster_rank();
   const int L = min(__ldg(p.ctx + b), p.max_ctx);
   const int n_cand = max(0, L - p.prefix);
-  const int t_lo = max(p.prefix, c * kCompactChunk), t_hi = min(L, (c + 1) * kCompactChunk);
+  const int tb = p.prefix + (int)((long long)n_cand * r / kSelCluster);
+  const int te = p.prefix + (int)((long long)n_cand * (r + 1) / kSelCluster);
   int32_t* out = p.idx + (size_t)b * p.k;
+  int32_t* out_slot = p.slot ? p.slot + (size_t)b * p.k : nullptr;
 
-  if (n_cand <= p.k) {  // every candidate is selected: position t goes to slot t - prefix
-    for (int t = t_lo + tid; t < t_hi; t += kCompactThreads) {
+  if (n_cand <= p.k) {  // every candidate is selected: position t goes to entry t - prefix
+    for (int t = tb + tid; t < te; t += kSelThreads) {
       out[t - p.prefix] = t;
-      if (p.sel.slot) p.sel.slot[(size_t)b * p.k + (t - p.prefix)] = slot_of(p, b, t);
+      if (out_slot) out_slot[t - p.prefix] = slot_of(p, b, t);
     }
-    if (c == 0) {
-      for (int r = n_cand + tid; r < p.k; r += kCompactThreads) out[r] = -1;
+    if (r == 0) {
+      for (int j = n_cand + tid; j < p.k; j += kSelThreads) out[j] = -1;
       if (tid == 0) p.n_sel[b] = n_cand;
     }
-    return;
+    return;  // the whole cluster takes this branch: no cluster barrier is pending
   }
 
-  const int4 sel = __ldcg(p.sel.sel + b);
-  const int lo = sel.y, hi = sel.y + sel.z;  // candidates: s >= lo; fine bins: lo <= s < hi
-  if (tid < kFineBins) s_fine[tid] = 0;
-  const int t_base = c * kCompactChunk + tid * kPer;
-  int v[kPer];
-  if (t_base >= t_lo && t_base + kPer <= t_hi) {
-    const int4* src = reinterpret_cast<const int4*>(p.scores + (size_t)b * p.ld + t_base);
-    const int4 a = __ldg(src), bb = __ldg(src + 1);
-    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = bb.x, v[5] = bb.y, v[6] = bb.z, v[7] = bb.w;
+  const int32_t* row = p.scores + (size_t)b * p.ld;
+  int* gh = p.coarse + (size_t)b * kCoarseBins;
+  int beta, above_win;
+  hist_threshold_bin<kCoarseBins>([gh](int i) { return __ldcg(gh + i); }, p.k, s_scratch, &beta, &above_win);
+  int lo, width;
+  if (beta > 0 && beta < kCoarseBins - 1) {
+    lo = (beta - kCoarseOff) << kCoarseShift;
+    width = kFineBins;
+  } else {  // the k-th largest lies outside the histogram's range: exact radix select
+    int tau, n_gt;
+    block_radix_select(row + p.prefix, n_cand, p.k, s_scratch, &tau, &n_gt);
+    lo = tau;
+    width = 1;
+  }
+  const int hi = lo + width;
+  if (tid < kCounts) s_counts[tid] = 0;
+  __syncthreads();
+  const int a0 = tb & ~(kSelPer - 1);
+  // 1. this part's candidates (s >= lo), in position order, into shared memory;
+  //    counts per fine bin of the window and above it.
+  int n_keep = 0, my_above = 0;
+  for (int t0 = a0; t0 < te; t0 += kSelRound) {
+    const int t = t0 + tid * kSelPer;  // 32 positions inside one 64-position block
+    int v[kSelPer];
+    load_scores(row, p.ld, t, tb, te, v);
+    const int slot0 = (out_slot && t < te) ? slot_of(p, b, t) : 0;  // issued beside the score loads
+    uint32_t cmask = 0;
+#pragma unroll
+    for (int j = 0; j < kSelPer; ++j) cmask |= (uint32_t)(v[j] >= lo) << j;
+    int tot;
+    int o = block_exclusive_scan(__popc(cmask), s_scratch, &tot) + n_keep;
+    n_keep += tot;
+    if (__any_sync(0xffffffffu, cmask != 0)) {
+#pragma unroll
+      for (int j = 0; j < kSelPer; ++j)
+        if ((cmask >> j) & 1) {
+          if (v[j] >= hi) ++my_above;
+          else atomicAdd(&s_counts[1 + v[j] - lo], 1);
+          if (o < kSelCap) {
+            e_pos[o] = t + j;
+            e_sc[o] = v[j];
+            e_slot[o] = slot0 + j;
+          }
+          ++o;
+        }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
+  if (lane == 0 && my_above) atomicAdd(&s_counts[0], my_above);
+  cluster_sync();  // every rank's counts are final; every rank has read the histogram
+  if (r == 0)      // leave the histogram zero for the next call
+    for (int i = tid; i < kCoarseBins; i += kSelThreads) gh[i] = 0;
+  // 2. gather every rank's counts, then no rank reads another's memory again
+  if (tid < kSelCluster * kCounts) {
+    const int rr = tid / kCounts, f = tid - rr * kCounts;
+    s_all[rr][f] = ld_remote(&s_counts[f], rr);
+  }
+  cluster_sync();
+  if (tid < 32) {
+    // Warp 0, lanes as fine bins: totals, suffix sums from the top of the window.
+    int fine_f = 0;
+    if (lane < width)
+      for (int rr = 0; rr < kSelCluster; ++rr) fine_f += s_all[rr][1 + lane];
+    int above = lane < kSelCluster ? s_all[lane][0] : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+    int suf = fine_f;  // candidates in fine bins lane .. width - 1
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += y;
+    }
+    // The k-th largest lies in fine bin f*, the highest bin whose suffix reaches
+    // k - above; cum = candidates above it inside the window.
+    const int kk = p.k - above;
+    const uint32_t reach = __ballot_sync(0xffffffffu, lane < width && suf >= kk);
+    const int fstar = reach ? 31 - __clz(reach) : 0;
+    const int cum = __shfl_sync(0xffffffffu, suf, min(fstar + 1, 31)) * (fstar + 1 < 32 ? 1 : 0);
+    const int quota = kk - cum;
+    // Lanes as ranks: candidates above tau and at tau in each part, then the
+    // ties and the selected entries in the parts before this CTA's.
+    int gt = 0, eq = 0;
+    if (lane < kSelCluster) {
+      gt = s_all[lane][0];
+      for (int f = fstar + 1; f < width; ++f) gt += s_all[lane][1 + f];
+      eq = s_all[lane][1 + fstar];
+    }
+    int eq_incl = eq;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, eq_incl, o);
+      if (lane >= o) eq_incl += y;
+    }
+    const int ties_before = eq_incl - eq;
+    const int taken = gt + min(max(quota - ties_before, 0), eq);
+    int tk_incl = taken;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, tk_incl, o);
+      if (lane >= o) tk_incl += y;
+    }
+    if (lane == r) {
+      s_misc[2] = ties_before;
+      s_misc[3] = tk_incl - taken;
+    }
+    if (lane == 0) {
+      s_misc[0] = lo + fstar;
+      s_misc[1] = quota;
+    }
+  }
+  __syncthreads();
+  const int tau = s_misc[0], quota = s_misc[1];
+  int carry_ties = s_misc[2], carry_out = s_misc[3];
+  // 3. ordered write of this part's selection
+  if (n_keep <= kSelCap) {
+    // From the kept candidates: thread i takes entries [i * per, (i + 1) * per).
+    const int per = (n_keep + kSelThreads - 1) / kSelThreads;
+    const int e0 = min(n_keep, tid * per), e1 = min(n_keep, e0 + per);
+    int n_eq = 0;
+    for (int e = e0; e < e1; ++e) n_eq += e_sc[e] == tau;
+    int tot;
+    int tr = block_exclusive_scan(n_eq, s_scratch, &tot) + carry_ties;
+    int n_take = 0;
+    for (int e = e0, q = tr; e < e1; ++e) {
+      const int sc = e_sc[e];
+      n_take += sc > tau || (sc == tau && q++ < quota);
+    }
+    int o = block_exclusive_scan(n_take, s_scratch, &tot) + carry_out;
+    carry_out += tot;
+    for (int e = e0; e < e1; ++e) {
+      const int sc = e_sc[e];
+      const bool take = sc > tau || (sc == tau && tr++ < quota);
+      if (take) {
+        if (o < p.k) {
+          out[o] = e_pos[e];
+          if (out_slot) out_slot[o] = e_slot[e];
+        }
+        ++o;
+      }
+    }
   } else {
+    // More candidates than the stage holds: rescan the scores of this part.
+    for (int t0 = a0; t0 < te; t0 += kSelRound) {
+      const int t = t0 + tid * kSelPer;
+      int v[kSelPer];
+      load_scores(row, p.ld, t, tb, te, v);
+      const bool mine = t < te && t + kSelPer > tb;
+      const int slot0 = (out_slot && mine) ? slot_of(p, b, t) : 0;  // slot of t; t + j is slot0 + j
+      uint32_t gt_m = 0, eq_m = 0;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int t = t_base + j;
-      v[j] = (t >= t_lo && t < t_hi) ? __ldg(p.scores + (size_t)b * p.ld + t) : INT_MIN;
+      for (int j = 0; j < kSelPer; ++j) {
+        gt_m |= (uint32_t)(v[j] > tau) << j;
+        eq_m |= (uint32_t)(v[j] == tau) << j;
+      }
+      int tot;
+      int tr = block_exclusive_scan(__popc(eq_m), s_scratch, &tot) + carry_ties;
+      carry_ties += tot;
+      uint32_t keep = gt_m;
+#pragma unroll
+      for (int j = 0; j < kSelPer; ++j)
+        if ((eq_m >> j) & 1) {
+          if (tr < quota) keep |= 1u << j;
+          ++tr;
+        }
+      int o = block_exclusive_scan(__popc(keep), s_scratch, &tot) + carry_out;
+      carry_out += tot;
+#pragma unroll
+      for (int j = 0; j < kSelPer; ++j)
+        if ((keep >> j) & 1) {
+          if (o < p.k) {
+            out[o] = t + j;
+            if (out_slot) out_slot[o] = slot0 + j;
+          }
+          ++o;
+        }
     }
   }
-  __syncthreads();
-  uint32_t cand = 0;
-  int n_above = 0;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int t = t_base + j;
-    if (t >= t_lo && t < t_hi && v[j] >= lo) {
-      cand |= 1u << j;
-      if (v[j] >= hi) ++n_above;
-      else atomicAdd(&s_fine[v[j] - lo], 1);
-    }
+  if (r == kSelCluster - 1) {  // the last part ends the list: pad, count
+    for (int j = carry_out + tid; j < p.k; j += kSelThreads) out[j] = -1;
+    if (tid == 0) p.n_sel[b] = min(carry_out, p.k);
   }
-  int tot_len, tot_above;
-  const int off = block_exclusive_scan(__popc(cand), sm.scratch, &tot_len);
-  block_exclusive_scan(n_above, sm.scratch, &tot_above);
-  const size_t run = ((size_t)b * p.sel.n_chunks + c) * kCompactChunk;
-  int o = off;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j)
-    if ((cand >> j) & 1) {
-      p.sel.run_pos[run + o] = t_base + j;
-      p.sel.run_score[run + o] = v[j];
-      ++o;
-    }
-  int* rec = p.sel.chunk_rec + ((size_t)b * p.sel.n_chunks + c) * kRecInts;
-  if (tid == 0) {
-    rec[0] = tot_len;
-    rec[1] = tot_above;
-  }
-  if (tid < kFineBins) rec[2 + tid] = s_fine[tid];
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(p.sel.done_cmp + b, 1) == (int)gridDim.x - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  merge_runs(p, b, sel, sm);
 }
 
 // ---------------------------------------------------------------- prefill ---
@@ -315,27 +393,28 @@ __global__ void __launch_bounds__(kRowThreads) prefill_topk_kernel(const RowTopk
 
 }  // namespace
 
-cudaError_t setup_topk_kernels() { return cudaSuccess; }
+cudaError_t setup_topk_kernels() {
+  return cudaFuncSetAttribute(decode_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+}
 
-cudaError_t launch_decode_compact(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
-                                  const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
-  CompactParams p;
+cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
+                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
+  SelectParams p;
   p.scores = scores;
   p.ctx = kv.context_lens;
   p.bt = kv.block_table;
+  p.coarse = sel.coarse;
   p.ld = ld;
   p.prefix = prefix;
   p.k = k;
   p.max_ctx = kv.max_ctx;
   p.max_blocks = kv.max_blocks;
   p.num_blocks = kv.num_blocks;
-  p.hkv = kv.hkv;
-  p.sel = sel;
   p.idx = idx;
   p.n_sel = n_sel;
-  dim3 grid(sel.n_chunks, kv.batch);
-  decode_compact_kernel<<<grid, kCompactThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  p.slot = sel.slot;
+  return launch_pdl(decode_select_kernel, dim3(kSelCluster, kv.batch), dim3(kSelThreads), kSelSmem, st, kSelCluster,
+                    p);
 }
 
 cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k, int32_t* idx,

@@ -64,7 +64,7 @@ extern "C" dsa_status dsa_topk_select_decode_noalloc(const dsa_paged_kv* kv_, co
   cudaError_t e = cudaMemsetAsync(base, 0, clear_bytes, stream);
   const dsa::SelState st = dsa::decode_topk_state(kv, k, prefix, base);
   if (e == cudaSuccess) e = dsa::launch_decode_hist(kv, scores, ld, prefix, k, st, stream);
-  if (e == cudaSuccess) e = dsa::launch_decode_compact(kv, scores, ld, prefix, k, st, idx, n_sel, stream);
+  if (e == cudaSuccess) e = dsa::launch_decode_select(kv, scores, ld, prefix, k, st, idx, n_sel, stream);
   if (e != cudaSuccess) return dsa::set_error(DSA_ERR_CUDA, cudaGetErrorString(e));
   return DSA_OK;
 }

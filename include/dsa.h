@@ -214,8 +214,9 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
  * device array of DSA_TOPK_STATIC_SCRATCH_BYTES inside the library, which every
  * GPU that loads the library keeps until the process exits; the call makes no
  * cudaMalloc, cudaFree or other allocating call.
- *   - Scratch needed: about batch * (4 KB + 8 bytes * max_context_len); larger
- *     sizes return DSA_ERR_UNSUPPORTED before anything is launched.
+ *   - Scratch needed: about 4.2 KB per sequence (a 1024-bin histogram, a
+ *     counter and the selection window), so up to about 1000 sequences fit;
+ *     larger batches return DSA_ERR_UNSUPPORTED before anything is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and sets kernel attributes: make that first call
  *     before any stream capture.
@@ -223,7 +224,7 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
  *     each call first zeroes the histograms and counters it relies on.  Calls
  *     whose work overlaps on the GPU (other streams, other host threads) race
  *     on the array and give wrong results: serialise them. */
-#define DSA_TOPK_STATIC_SCRATCH_BYTES (16u << 20)
+#define DSA_TOPK_STATIC_SCRATCH_BYTES (4u << 20)
 dsa_status dsa_topk_select_decode_noalloc(const dsa_paged_kv* kv, const int32_t* scores, int32_t ld,
                                           int32_t prefix_len, int32_t k, int32_t* idx, int32_t* n_sel,
                                           cudaStream_t stream);

@@ -79,11 +79,10 @@ def test_no_alloc_topk_rejects_sizes_beyond_the_static_scratch(lib):
     spec = synth.small_spec(lens=(700,), k=64)
     w, kv, scores = _scores(spec, 3)
     big = dsa.PagedKV(w["k_cache"], w["v_cache"], w["idx_cache"],
-                                 w["block_table"].repeat(64, 1), w["context_lens"].repeat(64), 700)
-    big.struct.max_context_len = 8192 * 8      # 64 sequences x 64K positions
-    big.struct.max_blocks_per_seq = 8192 * 8 // 64
+                      w["block_table"].repeat(2048, 1), w["context_lens"].repeat(2048), 700)
+    assert big.batch == 2048                   # 2048 sequences: about 8.4 MB of scratch
     scores_big = torch.empty((1, 4), dtype=torch.int32, device=DEV)
-    st = lib.dsa_topk_select_decode_noalloc(C.byref(big.struct), scores_big.data_ptr(), 8192 * 8, 64, 64,
+    st = lib.dsa_topk_select_decode_noalloc(C.byref(big.struct), scores_big.data_ptr(), 704, 64, 64,
                                             scores_big.data_ptr(), scores_big.data_ptr(), None)
     assert st == UNSUPPORTED
     assert b"static" in lib.dsa_last_error_message()
