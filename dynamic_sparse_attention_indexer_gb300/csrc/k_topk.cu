@@ -20,15 +20,18 @@ namespace {
 
 __device__ int g_status;
 
-// Decode selection: one thread-block cluster of kSelCluster CTAs per sequence.
-// CTA rank r owns the r-th of kSelCluster equal parts of the candidates
+// Decode selection: one thread-block cluster of C CTAs per sequence (C = 1 ..
+// 16, chosen from the longest context so that a CTA reads about one round of
+// 8192 scores).  CTA rank r owns the r-th of C equal parts of the candidates
 // [prefix, L).  Every CTA reads the sequence's coarse histogram (built by the
 // scoring kernel, bins 16 scores wide) and finds the bin that holds the k-th
-// largest score: the window [lo, lo + 16) and the number `above` of candidates
-// above it (an edge bin sends the sequence to an exact radix select over its
+// largest score: the window [lo, lo + 16) and the number of candidates above
+// it (an edge bin sends the sequence to an exact radix select over its
 // scores, window one score wide).  Then:
 //   1. every CTA counts, in its part, the candidates in each one-score-wide
-//      fine bin of the window and those above it;
+//      fine bin of the window and those above it, and keeps the part's
+//      candidates at or above the window (about 2% of the positions at 128K)
+//      in position order in shared memory, with their cache slots;
 //   2. the counts of all ranks are exchanged through distributed shared
 //      memory; each CTA derives the exact threshold tau (the k-th largest
 //      score), the number of ties at tau to keep (quota), and how many
@@ -36,16 +39,18 @@ __device__ int g_status;
 //   3. each CTA writes its selected positions, in order, at that offset (ties
 //      at tau are kept while their rank over the whole sequence is below the
 //      quota, so the lower positions win).
-// Step 1 also keeps the part's candidates at or above the window (about 2% of
-// the positions at 128K) in position order in shared memory, with their cache
-// slots, so step 3 reads only those; a part with more than kSelCap of them
-// rescans its scores (L2-resident, 4 bytes per position).  No global atomics,
-// no fences, no hand-off between CTAs beyond two cluster barriers.
-constexpr int kSelCluster = 8;
+// A part with more than kSelCap kept candidates rescans its scores in step 3.
+// Global loads that do not depend on one another (the first round of scores,
+// their cache slots, the histogram) are issued together, and the next round's
+// scores are loaded while the current one is processed: on this GPU a
+// dependent global access costs on the order of a microsecond.  No global
+// atomics, no fences, no hand-off between CTAs beyond two cluster barriers.
 constexpr int kSelThreads = 512;
-constexpr int kSelPer = 32;                          // consecutive positions per thread per round
-constexpr int kSelRound = kSelThreads * kSelPer;     // 16384 positions per round
+constexpr int kSelPer = 16;                          // consecutive positions per thread per round
+constexpr int kSelRound = kSelThreads * kSelPer;     // 8192 positions per round
 constexpr int kCounts = 1 + kFineBins;               // above, fine bins
+constexpr int kSelCap = 4096;                        // kept candidates per CTA in shared memory
+constexpr int kSelSmem = kSelCap * 3 * 4;
 
 struct SelectParams {
   const int32_t* scores;
@@ -72,7 +77,6 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ int slot_of(const SelectParams& p, int b, int t) {
   return load_block(p.bt, b, p.max_blocks, t >> 6, p.num_blocks, &g_status) * kBlock + (t & 63);
 }
-
 // Reads an int of CTA `rank`'s shared memory at the address of `p` in this CTA.
 __device__ __forceinline__ int ld_remote(const int* p, uint32_t rank) {
   uint32_t a;
@@ -82,7 +86,7 @@ __device__ __forceinline__ int ld_remote(const int* p, uint32_t rank) {
   return v;
 }
 
-// Scores of positions t .. t + 31 (t a multiple of 32) kept where lo_t <= t' < hi_t,
+// Scores of positions t .. t + 15 (t a multiple of 16) kept where lo_t <= t' < hi_t,
 // INT_MIN elsewhere; never reads past the row's ld entries.
 __device__ __forceinline__ void load_scores(const int32_t* row, int ld, int t, int lo_t, int hi_t, int* v) {
 #pragma unroll
@@ -97,16 +101,12 @@ __device__ __forceinline__ void load_scores(const int32_t* row, int ld, int t, i
   }
 }
 
-// Candidates at or above the window kept in shared memory per CTA (position,
-// score, slot); a part with more falls back to rescanning its scores.
-constexpr int kSelCap = 4096;
-constexpr int kSelSmem = kSelCap * 3 * 4;
-
-
+template <int C>
 __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const SelectParams p) {
   extern __shared__ __align__(16) int s_ent[];     // [kSelCap] positions | scores | slots
+  __shared__ int s_hist[kCoarseBins];
   __shared__ int s_counts[kCounts];                // this rank's: above, fine bins
-  __shared__ int s_all[kSelCluster][kCounts];      // every rank's
+  __shared__ int s_all[C][kCounts];                // every rank's
   __shared__ int s_misc[4];                        // tau, quota, ties before, output base
   __shared__ int s_scratch[264];
   int* e_pos = s_ent;
@@ -115,11 +115,11 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, b = blockIdx.y;
-  const int r = (int)cluster_rank();
+  const int r = C > 1 ? (int)cluster_rank() : 0;
   const int L = min(__ldg(p.ctx + b), p.max_ctx);
   const int n_cand = max(0, L - p.prefix);
-  const int tb = p.prefix + (int)((long long)n_cand * r / kSelCluster);
-  const int te = p.prefix + (int)((long long)n_cand * (r + 1) / kSelCluster);
+  const int tb = p.prefix + (int)((long long)n_cand * r / C);
+  const int te = p.prefix + (int)((long long)n_cand * (r + 1) / C);
   int32_t* out = p.idx + (size_t)b * p.k;
   int32_t* out_slot = p.slot ? p.slot + (size_t)b * p.k : nullptr;
 
@@ -137,8 +137,17 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
 
   const int32_t* row = p.scores + (size_t)b * p.ld;
   int* gh = p.coarse + (size_t)b * kCoarseBins;
+  const int a0 = tb & ~(kSelPer - 1);
+  // First round of scores and slots, then the histogram: all in flight together.
+  int v[kSelPer];
+  int t = a0 + tid * kSelPer;  // 16 positions inside one 64-position block
+  load_scores(row, p.ld, t, tb, te, v);
+  int slot0 = (out_slot && t < te) ? slot_of(p, b, t) : 0;  // slot of t; t + j is slot0 + j
+  for (int i = tid; i < kCoarseBins; i += kSelThreads) s_hist[i] = __ldcg(gh + i);
+  if (tid < kCounts) s_counts[tid] = 0;
+  __syncthreads();
   int beta, above_win;
-  hist_threshold_bin<kCoarseBins>([gh](int i) { return __ldcg(gh + i); }, p.k, s_scratch, &beta, &above_win);
+  hist_threshold_bin<kCoarseBins>([&](int i) { return s_hist[i]; }, p.k, s_scratch, &beta, &above_win);
   int lo, width;
   if (beta > 0 && beta < kCoarseBins - 1) {
     lo = (beta - kCoarseOff) << kCoarseShift;
@@ -150,17 +159,17 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
     width = 1;
   }
   const int hi = lo + width;
-  if (tid < kCounts) s_counts[tid] = 0;
-  __syncthreads();
-  const int a0 = tb & ~(kSelPer - 1);
   // 1. this part's candidates (s >= lo), in position order, into shared memory;
   //    counts per fine bin of the window and above it.
   int n_keep = 0, my_above = 0;
   for (int t0 = a0; t0 < te; t0 += kSelRound) {
-    const int t = t0 + tid * kSelPer;  // 32 positions inside one 64-position block
-    int v[kSelPer];
-    load_scores(row, p.ld, t, tb, te, v);
-    const int slot0 = (out_slot && t < te) ? slot_of(p, b, t) : 0;  // issued beside the score loads
+    int vn[kSelPer];  // next round, loaded while this one is processed
+    const int tn = t + kSelRound;
+    int slot_n = 0;
+    if (t0 + kSelRound < te) {
+      load_scores(row, p.ld, tn, tb, te, vn);
+      slot_n = (out_slot && tn < te) ? slot_of(p, b, tn) : 0;
+    }
     uint32_t cmask = 0;
 #pragma unroll
     for (int j = 0; j < kSelPer; ++j) cmask |= (uint32_t)(v[j] >= lo) << j;
@@ -181,25 +190,29 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
           ++o;
         }
     }
+#pragma unroll
+    for (int j = 0; j < kSelPer; ++j) v[j] = vn[j];
+    t = tn;
+    slot0 = slot_n;
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
   if (lane == 0 && my_above) atomicAdd(&s_counts[0], my_above);
-  cluster_sync();  // every rank's counts are final; every rank has read the histogram
-  if (r == 0)      // leave the histogram zero for the next call
+  if (C > 1) cluster_sync(); else __syncthreads();  // every rank's counts are final
+  if (r == 0)  // every rank has read the histogram: leave it zero for the next call
     for (int i = tid; i < kCoarseBins; i += kSelThreads) gh[i] = 0;
-  // 2. gather every rank's counts, then no rank reads another's memory again
-  if (tid < kSelCluster * kCounts) {
+  // 2. every rank's counts
+  if (tid < C * kCounts) {
     const int rr = tid / kCounts, f = tid - rr * kCounts;
-    s_all[rr][f] = ld_remote(&s_counts[f], rr);
+    s_all[rr][f] = C > 1 ? ld_remote(&s_counts[f], rr) : s_counts[f];
   }
-  cluster_sync();
+  __syncthreads();
   if (tid < 32) {
     // Warp 0, lanes as fine bins: totals, suffix sums from the top of the window.
     int fine_f = 0;
-    if (lane < width)
-      for (int rr = 0; rr < kSelCluster; ++rr) fine_f += s_all[rr][1 + lane];
-    int above = lane < kSelCluster ? s_all[lane][0] : 0;
+#pragma unroll
+    for (int rr = 0; rr < C; ++rr) fine_f += lane < width ? s_all[rr][1 + (lane & 15)] : 0;
+    int above = lane < C ? s_all[lane][0] : 0;
 #pragma unroll
     for (int o = 16; o; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
     int suf = fine_f;  // candidates in fine bins lane .. width - 1
@@ -213,14 +226,15 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
     const int kk = p.k - above;
     const uint32_t reach = __ballot_sync(0xffffffffu, lane < width && suf >= kk);
     const int fstar = reach ? 31 - __clz(reach) : 0;
-    const int cum = __shfl_sync(0xffffffffu, suf, min(fstar + 1, 31)) * (fstar + 1 < 32 ? 1 : 0);
+    const int cum = __shfl_sync(0xffffffffu, suf, fstar + 1);  // fstar + 1 <= 16: suffix past the window is 0
     const int quota = kk - cum;
     // Lanes as ranks: candidates above tau and at tau in each part, then the
     // ties and the selected entries in the parts before this CTA's.
     int gt = 0, eq = 0;
-    if (lane < kSelCluster) {
+    if (lane < C) {
       gt = s_all[lane][0];
-      for (int f = fstar + 1; f < width; ++f) gt += s_all[lane][1 + f];
+#pragma unroll
+      for (int f = 0; f < kFineBins; ++f) gt += (f > fstar && f < width) ? s_all[lane][1 + f] : 0;
       eq = s_all[lane][1 + fstar];
     }
     int eq_incl = eq;
@@ -279,16 +293,15 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   } else {
     // More candidates than the stage holds: rescan the scores of this part.
     for (int t0 = a0; t0 < te; t0 += kSelRound) {
-      const int t = t0 + tid * kSelPer;
-      int v[kSelPer];
-      load_scores(row, p.ld, t, tb, te, v);
-      const bool mine = t < te && t + kSelPer > tb;
-      const int slot0 = (out_slot && mine) ? slot_of(p, b, t) : 0;  // slot of t; t + j is slot0 + j
+      const int tt = t0 + tid * kSelPer;
+      int w[kSelPer];
+      load_scores(row, p.ld, tt, tb, te, w);
+      const int s0 = (out_slot && tt < te) ? slot_of(p, b, tt) : 0;
       uint32_t gt_m = 0, eq_m = 0;
 #pragma unroll
       for (int j = 0; j < kSelPer; ++j) {
-        gt_m |= (uint32_t)(v[j] > tau) << j;
-        eq_m |= (uint32_t)(v[j] == tau) << j;
+        gt_m |= (uint32_t)(w[j] > tau) << j;
+        eq_m |= (uint32_t)(w[j] == tau) << j;
       }
       int tot;
       int tr = block_exclusive_scan(__popc(eq_m), s_scratch, &tot) + carry_ties;
@@ -306,17 +319,18 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
       for (int j = 0; j < kSelPer; ++j)
         if ((keep >> j) & 1) {
           if (o < p.k) {
-            out[o] = t + j;
-            if (out_slot) out_slot[o] = slot0 + j;
+            out[o] = tt + j;
+            if (out_slot) out_slot[o] = s0 + j;
           }
           ++o;
         }
     }
   }
-  if (r == kSelCluster - 1) {  // the last part ends the list: pad, count
+  if (r == C - 1) {  // the last part ends the list: pad, count
     for (int j = carry_out + tid; j < p.k; j += kSelThreads) out[j] = -1;
     if (tid == 0) p.n_sel[b] = min(carry_out, p.k);
   }
+  if (C > 1) cluster_sync();  // no CTA leaves while another may still read its counts
 }
 
 // ---------------------------------------------------------------- prefill ---
@@ -393,8 +407,43 @@ __global__ void __launch_bounds__(kRowThreads) prefill_topk_kernel(const RowTopk
 
 }  // namespace
 
+bool g_sel16[64] = {};  // clusters of 16 CTAs can be scheduled on this device
+
 cudaError_t setup_topk_kernels() {
-  return cudaFuncSetAttribute(decode_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+  cudaError_t e = cudaSuccess;
+  auto smem = [&](auto kernel) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+  };
+  smem(decode_select_kernel<1>);
+  smem(decode_select_kernel<2>);
+  smem(decode_select_kernel<4>);
+  smem(decode_select_kernel<8>);
+  smem(decode_select_kernel<16>);
+  if (e != cudaSuccess) return e;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  // Clusters of 16 are beyond the portable size: use them only where the
+  // occupancy query says at least one fits.
+  if (cudaFuncSetAttribute(decode_select_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = kSelSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<16>, &cfg) == cudaSuccess && n > 0 && dev >= 0 &&
+        dev < 64)
+      g_sel16[dev] = true;
+  }
+  cudaGetLastError();  // a refused query leaves no error behind
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
@@ -413,8 +462,21 @@ cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, in
   p.idx = idx;
   p.n_sel = n_sel;
   p.slot = sel.slot;
-  return launch_pdl(decode_select_kernel, dim3(kSelCluster, kv.batch), dim3(kSelThreads), kSelSmem, st, kSelCluster,
-                    p);
+  // CTAs per sequence: about one round of scores each, at most 8 (16 where supported).
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int c_max = (dev >= 0 && dev < 64 && g_sel16[dev]) ? 16 : 8;
+  const long long n_max = (long long)kv.max_ctx - prefix;
+  int c = 1;
+  while (c < c_max && n_max > (long long)c * kSelRound) c *= 2;
+  const dim3 grid(c, kv.batch), block(kSelThreads);
+  switch (c) {
+    case 1: return launch_pdl(decode_select_kernel<1>, grid, block, kSelSmem, st, 1, p);
+    case 2: return launch_pdl(decode_select_kernel<2>, grid, block, kSelSmem, st, 2, p);
+    case 4: return launch_pdl(decode_select_kernel<4>, grid, block, kSelSmem, st, 4, p);
+    case 8: return launch_pdl(decode_select_kernel<8>, grid, block, kSelSmem, st, 8, p);
+    default: return launch_pdl(decode_select_kernel<16>, grid, block, kSelSmem, st, 16, p);
+  }
 }
 
 cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k, int32_t* idx,
