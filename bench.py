@@ -100,6 +100,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def profiled_attention_traffic():
+    """DRAM bytes per attention call from the committed ncu summary, or None
+    once the attention source has changed since the counters were taken."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "decode_128k_kernels_full.md")
+    src = os.path.join(ROOT, "dynamic_sparse_attention_indexer_gb300", "csrc", "k_attn.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256\(k_attn\.cu\): ([0-9a-f]{64})", text)
+    m_bytes = re.search(r"traffic_bytes_per_call: (\d+)", text)
+    if not (m_sha and m_bytes) or m_sha.group(1) != digest:
+        return None
+    return int(m_bytes.group(1))
+
+
 def reduce_over_ranks(values: dict, op: str):
     """Max ("max") or sum ("sum") of scalar values over all ranks (no-op
     without an initialised process group)."""
@@ -182,11 +201,11 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_block(spec):
+def config_block(spec, layers=LAYERS):
     return {"workload": spec.name, "batch": spec.batch, "context": 131072, "prefix": spec.prefix_len,
             "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": 128, "idx_dim": 64,
             "top_k": spec.k, "block_size": 64, "seed": 1000 + CONFIG_ID,
-            "l2": f"inputs larger than L2: steps rotate over {LAYERS} independent KV caches (no flush)"}
+            "l2": f"inputs larger than L2: steps rotate over {layers} independent KV caches (no flush)"}
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -199,7 +218,8 @@ def run_gpu(args, rank, world, local_rank):
     spec = synth.CONFIGS[CONFIG_ID]
     P, k, hq = spec.prefix_len, spec.k, spec.num_q_heads
 
-    # --- resident inputs: LAYERS independent caches; one query batch per layer
+    # --- resident inputs: args.layers independent caches; one query batch per layer
+    LAYERS = args.layers
     layers = []
     for l in range(LAYERS):
         w = synth.make_workload(spec, 1000 + CONFIG_ID + 7919 * l + 104729 * rank, dev)
@@ -221,6 +241,8 @@ def run_gpu(args, rank, world, local_rank):
         dsa.decode_step(kv, w["q"], w["q_idx"], P, k, b["scores"], b["idx"], b["n_sel"], b["out"], b["lse"], ws)
 
     # eager warm-up (first call sets kernel attributes), then one graph per layer
+    # and one graph of a whole pass over the layers (as a serving loop captures
+    # one decode iteration of all its layers)
     for l in range(LAYERS):
         step(l)
     torch.cuda.synchronize()
@@ -233,11 +255,16 @@ def run_gpu(args, rank, world, local_rank):
             with torch.cuda.graph(g, stream=stream):
                 step(l)
             graphs.append(g)
+        cycle = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cycle, stream=stream):
+            for l in range(LAYERS):
+                step(l)
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             graphs[i % LAYERS].replay()
+        cycle.replay()
     torch.cuda.synchronize()
 
     # --- timed region: exactly K steps
@@ -249,8 +276,10 @@ def run_gpu(args, rank, world, local_rank):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(args.steps):
-            graphs[(args.warmup + i) % LAYERS].replay()
+        for _ in range(args.steps // LAYERS):  # exactly args.steps steps
+            cycle.replay()
+        for l in range(args.steps % LAYERS):
+            graphs[l].replay()
         e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -344,16 +373,17 @@ def run_gpu(args, rank, world, local_rank):
     ms_step = agg["ms"] / args.steps
     attn_gbs = ab["attention"] / (agg["attn_ms"] * 1e-3) / 1e9
     step_gbs = ab["step"] / (ms_step * 1e-3) / 1e9
-    traffic = args.attn_traffic if args.attn_traffic > 0 else None
-    launches_per_step = 3  # indexer + histogram, compaction, attention (splits merged in-kernel)
+    traffic = args.attn_traffic if args.attn_traffic > 0 else profiled_attention_traffic()
+    launches_per_step = 4  # indexer (+ histogram), top-k selection, attention, partial merge
     line = {
         "metric": METRIC, "value": tokens["tok"] / (agg["ms"] * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_block(spec),
+        "config": config_block(spec, LAYERS),
         "hbm": {"step_bytes": ab["step"], "achieved_gbs": step_gbs, "peak_gbs": peak,
                 "frac": step_gbs / peak, "peak_kind": peak_kind},
-        "roofline": {"kernel": "sparse_attn_kernel (dsa_sparse_attn_decode, per launch in a graph)",
+        "roofline": {"kernel": "dsa_sparse_attn_decode per call in a graph: resolve_slots_kernel + "
+                               "sparse_attn_kernel + attn_combine_kernel",
                      "bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                      "traffic": traffic, "algorithmic_bytes": ab["attention"], "ms": agg["attn_ms"],
                      "peak_kind": peak_kind},
@@ -375,6 +405,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="independent caches the steps rotate over (4 keeps every step out of L2; "
+                         "1 gives a small case for ncu captures)")
     ap.add_argument("--attn-traffic", type=float, default=0.0,
                     help="DRAM bytes per attention launch from an ncu capture (0 = not measured)")
     args = ap.parse_args()
