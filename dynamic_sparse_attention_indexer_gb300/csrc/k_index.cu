@@ -3,7 +3,7 @@
 //
 // Decode: one int8 dot product of 64 per position, a pure HBM stream of 64 B
 // per position.  Whole 4 KB cache blocks are staged into shared memory with
-// mbarrier-tracked bulk copies by a producer warp, ten 16 KB stages in flight
+// mbarrier-tracked bulk copies by a producer warp, eight 16 KB stages in flight
 // per SM; consumer warps score one position per thread with __dp4a.  The fused
 // variant also builds the coarse score histogram the top-k needs (per-warp
 // shared-memory bins added into a per-sequence global histogram), so the
@@ -34,7 +34,7 @@ __device__ int g_status;
 // forget atomics; the selection kernel reads the completed histogram).
 constexpr int kIdxConsumers = 8;                               // consumer warps
 constexpr int kIdxThreads = 32 * (1 + kIdxConsumers);          // 288
-constexpr int kIdxStages = 10;
+constexpr int kIdxStages = 8;
 constexpr int kGroupBlocks = 4;                                // cache blocks per stage
 constexpr int kIdxBlockBytes = kBlock * kIdxDim;               // 4096
 constexpr int kIdxStageBytes = kGroupBlocks * kIdxBlockBytes;  // 16 KB
@@ -122,6 +122,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = p.prefix, jb_base = P / kBlock;
+  // Shared-memory set-up first: it touches no global memory, so it overlaps
+  // the previous kernel's tail.
+  if (kHist)
+    for (int i = tid; i < kIdxConsumers * kCoarseBins; i += kIdxThreads) hist[i] = 0;
+  if (tid == 0) {
+    for (int s = 0; s < kIdxStages; ++s) {
+      mbar_init(&full[s], kGroupBlocks);
+      mbar_init(&empty[s], kIdxConsumers);
+    }
+    mbar_fence_init();
+  }
   pdl_wait();
   pdl_trigger();
   candidate_blocks(p.ctx, p.batch, p.max_ctx, P, seg_start, len, scratch);
@@ -145,15 +156,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
       if (seg_start[mid] <= f) lo = mid; else hi = mid - 1;
     }
     ids[f - f_begin] = load_block(p.bt, lo, p.max_blocks, f - seg_start[lo] + jb_base, p.num_blocks, &g_status);
-  }
-  if (kHist)
-    for (int i = tid; i < kIdxConsumers * kCoarseBins; i += kIdxThreads) hist[i] = 0;
-  if (tid == 0) {
-    for (int s = 0; s < kIdxStages; ++s) {
-      mbar_init(&full[s], kGroupBlocks);
-      mbar_init(&empty[s], kIdxConsumers);
-    }
-    mbar_fence_init();
   }
   __syncthreads();
   GroupCursor cur{f_begin, f_end, b_first};
