@@ -6,9 +6,8 @@
 // result is deterministic and ascending; among equal scores the lower
 // positions win.
 //
-// Prefill (many rows of at most a few ten thousand candidates): one CTA per
-// query row builds its histogram in shared memory, finds the threshold and
-// compacts the row in order with block-wide scans.
+// Prefill (many rows of at most a few ten thousand candidates): one warp per
+// query row, histogram, threshold and ordered compaction all within the warp.
 #include <climits>
 
 #include "common.cuh"
@@ -334,8 +333,13 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
 }
 
 // ---------------------------------------------------------------- prefill ---
-constexpr int kRowThreads = 512;
-constexpr int kScratchIntsTopk = 264;
+// One warp per query row (many rows of at most a few ten thousand candidates),
+// no CTA-wide barrier: three passes over the row's scores (the row stays in L2
+// after the first): a 1024-bin coarse histogram in the warp's shared memory and
+// the threshold window from it; the counts per one-score bin of the window and
+// above it, which give the exact threshold tau and the tie quota; then an ordered
+// compaction by warp scans.  An edge bin falls back to a warp radix select.
+constexpr int kRowWarps = 8;
 
 struct RowTopkParams {
   const int32_t* scores;
@@ -344,65 +348,194 @@ struct RowTopkParams {
   int32_t* n_sel;
 };
 
-__global__ void __launch_bounds__(kRowThreads) prefill_topk_kernel(const RowTopkParams p) {
-  __shared__ int hist[kHistBins];
-  __shared__ int scratch[kScratchIntsTopk];
-  const int i = blockIdx.x, tid = threadIdx.x;
+// Highest bin b with sum(bins >= b) >= k among nb (256 or 1024) bins in shared
+// memory, and the count above it; one warp.  *bin = -1 when the total is below k.
+__device__ __forceinline__ void warp_hist_threshold(const int* h, int nb, int k, int lane, int* bin, int* above) {
+  const int gs = nb / 32;  // bins per lane group
+  int sum = 0;
+  for (int i = 0; i < gs; ++i) sum += h[gs * lane + ((i + lane) % gs)];
+  int suf = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += y;
+  }
+  const uint32_t reach = __ballot_sync(0xffffffffu, suf >= k);
+  if (!reach) {
+    *bin = -1;
+    *above = 0;
+    return;
+  }
+  const int ls = 31 - __clz(reach);
+  const int above_grp = ls < 31 ? __shfl_sync(0xffffffffu, suf, ls + 1) : 0;
+  int suf2 = lane < gs ? h[gs * ls + lane] : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, suf2, o);
+    if (lane + o < 32) suf2 += y;
+  }
+  const uint32_t reach2 = __ballot_sync(0xffffffffu, lane < gs && above_grp + suf2 >= k);
+  const int b = 31 - __clz(reach2);
+  *bin = gs * ls + b;
+  *above = above_grp + (b < 31 ? __shfl_sync(0xffffffffu, suf2, b + 1) : 0);
+}
+
+// Candidate scores of one row, four per 16-byte chunk c (positions 4c .. 4c + 3),
+// INT_MIN outside [t_lo, t_hi).
+__device__ __forceinline__ int4 row_chunk(const int32_t* row, int c, int t_lo, int t_hi) {
+  int4 x = __ldcg(reinterpret_cast<const int4*>(row) + c);
+  const int t = 4 * c;
+  x.x = t >= t_lo && t < t_hi ? x.x : INT_MIN;
+  x.y = t + 1 >= t_lo && t + 1 < t_hi ? x.y : INT_MIN;
+  x.z = t + 2 >= t_lo && t + 2 < t_hi ? x.z : INT_MIN;
+  x.w = t + 3 >= t_lo && t + 3 < t_hi ? x.w : INT_MIN;
+  return x;
+}
+
+__global__ void __launch_bounds__(32 * kRowWarps) prefill_topk_kernel(const RowTopkParams p) {
+  __shared__ int s_hist[kRowWarps][kCoarseBins];
+  __shared__ int s_fine[kRowWarps][kFineBins];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int i = blockIdx.x * kRowWarps + w;
+  if (i >= p.n_q) return;
+  int* hist = s_hist[w];
+  int* fine = s_fine[w];
   const int pos = p.pos0 + i;
   const int n_cand = max(0, pos - p.prefix + 1);
   int32_t* out = p.idx + (size_t)i * p.k;
-  const int32_t* row = p.scores + (size_t)i * p.ld + p.prefix;  // candidate j is position prefix + j
-  if (n_cand <= p.k) {
-    for (int j = tid; j < p.k; j += kRowThreads) out[j] = j < n_cand ? p.prefix + j : -1;
-    if (tid == 0) p.n_sel[i] = n_cand;
+  if (n_cand <= p.k) {  // every candidate is selected
+    for (int j = lane; j < p.k; j += 32) out[j] = j < n_cand ? p.prefix + j : -1;
+    if (lane == 0) p.n_sel[i] = n_cand;
     return;
   }
-  for (int j = tid; j < kHistBins; j += kRowThreads) hist[j] = 0;
-  __syncthreads();
-  for (int j = tid; j < n_cand; j += kRowThreads) atomicAdd(&hist[hist_bin(__ldg(row + j))], 1);
-  __syncthreads();
-  auto lds = [&](int b) { return hist[b]; };
-  const Sel s = selection_from_hist(lds, row, n_cand, p.k, scratch);
-
-  // Ordered compaction: segments of kRowThreads * 8 candidates, 8 per thread.
+  const int32_t* row = p.scores + (size_t)i * p.ld;
+  const int t_lo = p.prefix, t_hi = pos + 1;
+  const int c0 = t_lo >> 2, c1 = (t_hi + 3) >> 2;  // chunks covering [t_lo, t_hi), all inside the row's ld entries
+  // Pass 1: coarse histogram.
+  for (int b = lane; b < kCoarseBins; b += 32) hist[b] = 0;
+  __syncwarp();
+#pragma unroll 4
+  for (int c = c0 + lane; c < c1; c += 32) {
+    const int4 x = row_chunk(row, c, t_lo, t_hi);
+    if (x.x != INT_MIN) atomicAdd(&hist[coarse_bin(x.x)], 1);
+    if (x.y != INT_MIN) atomicAdd(&hist[coarse_bin(x.y)], 1);
+    if (x.z != INT_MIN) atomicAdd(&hist[coarse_bin(x.z)], 1);
+    if (x.w != INT_MIN) atomicAdd(&hist[coarse_bin(x.w)], 1);
+  }
+  __syncwarp();
+  int beta, above_win;
+  warp_hist_threshold(hist, kCoarseBins, p.k, lane, &beta, &above_win);
+  int lo, width;
+  if (beta > 0 && beta < kCoarseBins - 1) {
+    lo = (beta - kCoarseOff) << kCoarseShift;
+    width = kFineBins;
+  } else {
+    // The k-th largest lies outside the histogram's range: exact radix select,
+    // four passes of 8-bit digits of u = s ^ 0x80000000 (256 bins in `hist`).
+    uint32_t prefix = 0, mask = 0;
+    int kk = p.k;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      __syncwarp();
+      for (int b = lane; b < 256; b += 32) hist[b] = 0;
+      __syncwarp();
+      for (int c = c0 + lane; c < c1; c += 32) {
+        const int4 x = row_chunk(row, c, t_lo, t_hi);
+        const int v4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t uu = (uint32_t)v4[u] ^ 0x80000000u;
+          if (v4[u] != INT_MIN && (uu & mask) == prefix) atomicAdd(&hist[(uu >> shift) & 255], 1);
+        }
+      }
+      __syncwarp();
+      int dsel, acc;
+      warp_hist_threshold(hist, 256, kk, lane, &dsel, &acc);
+      kk -= acc;
+      prefix |= (uint32_t)dsel << shift;
+      mask |= 0xFFu << shift;
+    }
+    lo = (int)(prefix ^ 0x80000000u);
+    width = 1;
+  }
+  // Pass 2: counts per one-score bin of the window and above it.
+  if (lane < kFineBins) fine[lane] = 0;
+  __syncwarp();
+  int my_above = 0;
+#pragma unroll 4
+  for (int c = c0 + lane; c < c1; c += 32) {
+    const int4 x = row_chunk(row, c, t_lo, t_hi);
+    const int v4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int v = v4[u];
+      if (v >= lo + width) ++my_above;
+      else if (v >= lo) atomicAdd(&fine[v - lo], 1);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
+  __syncwarp();
+  // Lanes as fine bins: the k-th largest lies in bin f*, the highest whose
+  // suffix reaches k - above; cum = candidates above it inside the window.
+  const int kk = p.k - my_above;
+  int suf = lane < width ? fine[lane] : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += y;
+  }
+  const uint32_t reach = __ballot_sync(0xffffffffu, lane < width && suf >= kk);
+  const int fstar = reach ? 31 - __clz(reach) : 0;
+  const int cum = __shfl_sync(0xffffffffu, suf, fstar + 1);  // fstar + 1 <= 16: the suffix past the window is 0
+  const int tau = lo + fstar, quota = kk - cum;
+  // Pass 3: ordered compaction, 128 positions (32 chunks) per step.
   int carry_ties = 0, carry_out = 0;
-  for (int seg = 0; seg < n_cand; seg += kRowThreads * 8) {
-    const int j0 = seg + tid * 8;
+  for (int cb = c0; cb < c1; cb += 32) {
+    const int c = cb + lane;
+    int4 x = make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+    if (c < c1) x = row_chunk(row, c, t_lo, t_hi);
+    const int v4[4] = {x.x, x.y, x.z, x.w};
     uint32_t gt_m = 0, eq_m = 0;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = j0 + u;
-      if (j < n_cand) {
-        const int v = __ldg(row + j);
-        if (v > s.tau) gt_m |= 1u << u;
-        if (v == s.tau) eq_m |= 1u << u;
-      }
+    for (int u = 0; u < 4; ++u) {
+      gt_m |= (uint32_t)(v4[u] > tau) << u;
+      eq_m |= (uint32_t)(v4[u] == tau) << u;
     }
-    int tot;
-    const int ties_before = block_exclusive_scan(__popc(eq_m), scratch, &tot) + carry_ties;
-    carry_ties += tot;
-    // Keep ties while the row-wide tie rank is below the quota.
-    uint32_t keep = gt_m;
-    int tr = ties_before;
+    int n_eq = __popc(eq_m), x_eq = n_eq;
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x_eq, o);
+      if (lane >= o) x_eq += y;
+    }
+    int tr = carry_ties + x_eq - n_eq;
+    carry_ties += __shfl_sync(0xffffffffu, x_eq, 31);
+    uint32_t keep = gt_m;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
       if ((eq_m >> u) & 1) {
-        if (tr < s.quota) keep |= 1u << u;
+        if (tr < quota) keep |= 1u << u;
         ++tr;
       }
-    const int off = block_exclusive_scan(__popc(keep), scratch, &tot) + carry_out;
-    carry_out += tot;
-    int o = off;
+    const int n_keep = __popc(keep);
+    int x_k = n_keep;
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x_k, o);
+      if (lane >= o) x_k += y;
+    }
+    int o = carry_out + x_k - n_keep;
+    carry_out += __shfl_sync(0xffffffffu, x_k, 31);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
       if ((keep >> u) & 1) {
-        if (o < p.k) out[o] = p.prefix + j0 + u;
+        if (o < p.k) out[o] = 4 * c + u;
         ++o;
       }
   }
-  carry_out = min(carry_out, p.k);
-  for (int j = carry_out + tid; j < p.k; j += kRowThreads) out[j] = -1;
-  if (tid == 0) p.n_sel[i] = carry_out;
+  const int n_out = min(carry_out, p.k);
+  for (int j = n_out + lane; j < p.k; j += 32) out[j] = -1;
+  if (lane == 0) p.n_sel[i] = n_out;
 }
 
 }  // namespace
@@ -490,7 +623,7 @@ cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int
   p.n_q = qs.n_q;
   p.idx = idx;
   p.n_sel = n_sel;
-  prefill_topk_kernel<<<qs.n_q, kRowThreads, 0, st>>>(p);
+  prefill_topk_kernel<<<(qs.n_q + kRowWarps - 1) / kRowWarps, 32 * kRowWarps, 0, st>>>(p);
   return cudaGetLastError();
 }
 
