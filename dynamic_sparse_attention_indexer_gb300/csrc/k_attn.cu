@@ -70,8 +70,15 @@ struct AttnParams {
   float* lse;
 };
 
-__device__ __forceinline__ int range_begin(int T, int G, int c) { return (int)((long long)T * c / G); }
-__device__ __forceinline__ int cta_of(int T, int G, int x) { return (int)(((long long)(x + 1) * G - 1) / T); }
+// 32-bit division when the products fit (the common case), 64-bit otherwise.
+__device__ __forceinline__ int range_begin(int T, int G, int c) {
+  if ((unsigned long long)T * G < (1ull << 31)) return (int)((unsigned)(T * c) / (unsigned)G);
+  return (int)((long long)T * c / G);
+}
+__device__ __forceinline__ int cta_of(int T, int G, int x) {
+  if ((unsigned long long)T * G < (1ull << 31)) return (int)((unsigned)((x + 1) * G - 1) / (unsigned)T);
+  return (int)(((long long)(x + 1) * G - 1) / T);
+}
 
 struct QueryInfo {
   int qi, seq, n_pre, rows;
@@ -447,11 +454,11 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 // nb boundaries c_lo .. c_hi - 1 has n = nb + 1 partials (one per CTA
 // c_lo .. c_hi); the block of its j-th boundary merges the query heads
 // h = j, j + nb, j + 2 nb, ..., four at a time, one thread per (head, column).
-// A thread issues the loads of all its partials at once (up to 32 in flight)
-// and merges them in one pass: no barrier, one round trip per 32 partials.
+// A thread issues the loads of its partials at once (up to 24 in flight)
+// and merges them in one pass: no barrier, one round trip per 24 partials.
 constexpr int kCombThreads = 512;
 constexpr int kCombHeads = kCombThreads / kHeadDim;  // heads merged at once
-constexpr int kCombBatch = 32;                      // partials in flight per thread
+constexpr int kCombBatch = 24;                      // partials in flight per thread
 
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnParams p, int grid_ctas) {
   pdl_wait();

@@ -51,6 +51,17 @@ def test_decode_group_sizes(lib, hq, hkv):
     _run(synth.small_spec(hq=hq, hkv=hkv, lens=(900, 1800)))
 
 
+@pytest.mark.parametrize("lens", [
+    (12000, 16500),          # top-k cluster of 2 CTAs per sequence (longest context 16.5K)
+    (30000, 9000, 21000),    # 4 CTAs per sequence
+    (60000, 45001),          # 8 CTAs per sequence
+])
+def test_decode_selection_cluster_sizes(lib, lens):
+    """Contexts that make the selection kernel use clusters of 2, 4 and 8 CTAs
+    per sequence (parts exchange their counts through distributed shared memory)."""
+    _run(synth.small_spec(lens=lens, prefix_len=128, k=1024, hq=8, hkv=2))
+
+
 def test_decode_one_query_over_the_whole_grid(lib):
     """A single sequence whose attended rows are cut over every CTA of the
     persistent grid: over a hundred partials per head merged."""
