@@ -461,8 +461,8 @@ constexpr int kCombHeads = kCombThreads / kHeadDim;  // heads merged at once
 constexpr int kCombBatch = 24;                      // partials in flight per thread
 
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnParams p, int grid_ctas) {
-  pdl_wait();
-  pdl_trigger();
+  // The boundary arithmetic reads no memory: it runs before the wait on the
+  // attention kernel, and blocks with no cut query leave without waiting.
   const int T = p.tiles, TP = p.tiles_per_q;
   const int x = range_begin(T, grid_ctas, blockIdx.x + 1);  // first tile of CTA blockIdx.x + 1
   const int qi = x / TP;
@@ -474,6 +474,8 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnPa
   // The partial of CTA c for this query sits in slot 0 if the query's segment
   // starts the CTA's range, else in slot 1.
   const int c_first = range_begin(T, grid_ctas, c_lo) >= first ? 0 : 1;  // slot of CTA c_lo
+  pdl_wait();
+  pdl_trigger();
   for (int h = j + (int)(threadIdx.x / kHeadDim) * nb; h < p.hq; h += kCombHeads * nb) {
     float M = -INFINITY, Lsum = 0.f, acc = 0.f;
     for (int i0 = 0; i0 < n; i0 += kCombBatch) {

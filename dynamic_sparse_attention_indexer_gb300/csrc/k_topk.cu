@@ -19,6 +19,38 @@ namespace {
 
 __device__ int g_status;
 
+// Highest bin b with sum(bins >= b) >= k among nb (256 or 1024) bins in shared
+// memory, and the count above it; one warp.  *bin = -1 when the total is below k.
+__device__ __forceinline__ void warp_hist_threshold(const int* h, int nb, int k, int lane, int* bin, int* above) {
+  const int gs = nb / 32;  // bins per lane group
+  int sum = 0;
+  for (int i = 0; i < gs; ++i) sum += h[gs * lane + ((i + lane) % gs)];
+  int suf = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += y;
+  }
+  const uint32_t reach = __ballot_sync(0xffffffffu, suf >= k);
+  if (!reach) {
+    *bin = -1;
+    *above = 0;
+    return;
+  }
+  const int ls = 31 - __clz(reach);
+  const int above_grp = ls < 31 ? __shfl_sync(0xffffffffu, suf, ls + 1) : 0;
+  int suf2 = lane < gs ? h[gs * ls + lane] : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, suf2, o);
+    if (lane + o < 32) suf2 += y;
+  }
+  const uint32_t reach2 = __ballot_sync(0xffffffffu, lane < gs && above_grp + suf2 >= k);
+  const int b = 31 - __clz(reach2);
+  *bin = gs * ls + b;
+  *above = above_grp + (b < 31 ? __shfl_sync(0xffffffffu, suf2, b + 1) : 0);
+}
+
 // Decode selection: one thread-block cluster of C CTAs per sequence (C = 1 ..
 // 16, chosen from the longest context so that a CTA reads about one round of
 // 8192 scores).  CTA rank r owns the r-th of C equal parts of the candidates
@@ -145,8 +177,13 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   for (int i = tid; i < kCoarseBins; i += kSelThreads) s_hist[i] = __ldcg(gh + i);
   if (tid < kCounts) s_counts[tid] = 0;
   __syncthreads();
-  int beta, above_win;
-  hist_threshold_bin<kCoarseBins>([&](int i) { return s_hist[i]; }, p.k, s_scratch, &beta, &above_win);
+  if (tid < 32) {  // one warp finds the threshold bin
+    int bb, ab;
+    warp_hist_threshold(s_hist, kCoarseBins, p.k, lane, &bb, &ab);
+    if (lane == 0) s_misc[0] = bb;
+  }
+  __syncthreads();
+  const int beta = s_misc[0];
   int lo, width;
   if (beta > 0 && beta < kCoarseBins - 1) {
     lo = (beta - kCoarseOff) << kCoarseShift;
@@ -347,38 +384,6 @@ struct RowTopkParams {
   int32_t* idx;
   int32_t* n_sel;
 };
-
-// Highest bin b with sum(bins >= b) >= k among nb (256 or 1024) bins in shared
-// memory, and the count above it; one warp.  *bin = -1 when the total is below k.
-__device__ __forceinline__ void warp_hist_threshold(const int* h, int nb, int k, int lane, int* bin, int* above) {
-  const int gs = nb / 32;  // bins per lane group
-  int sum = 0;
-  for (int i = 0; i < gs; ++i) sum += h[gs * lane + ((i + lane) % gs)];
-  int suf = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_down_sync(0xffffffffu, suf, o);
-    if (lane + o < 32) suf += y;
-  }
-  const uint32_t reach = __ballot_sync(0xffffffffu, suf >= k);
-  if (!reach) {
-    *bin = -1;
-    *above = 0;
-    return;
-  }
-  const int ls = 31 - __clz(reach);
-  const int above_grp = ls < 31 ? __shfl_sync(0xffffffffu, suf, ls + 1) : 0;
-  int suf2 = lane < gs ? h[gs * ls + lane] : 0;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_down_sync(0xffffffffu, suf2, o);
-    if (lane + o < 32) suf2 += y;
-  }
-  const uint32_t reach2 = __ballot_sync(0xffffffffu, lane < gs && above_grp + suf2 >= k);
-  const int b = 31 - __clz(reach2);
-  *bin = gs * ls + b;
-  *above = above_grp + (b < 31 ? __shfl_sync(0xffffffffu, suf2, b + 1) : 0);
-}
 
 // Candidate scores of one row, four per 16-byte chunk c (positions 4c .. 4c + 3),
 // INT_MIN outside [t_lo, t_hi).
