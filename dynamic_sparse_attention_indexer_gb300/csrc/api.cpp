@@ -184,11 +184,11 @@ dsa_status check_k_prefix(int32_t k, int32_t prefix) {
   return DSA_OK;
 }
 
-// The attention kernel walks (query, tile of 128 / num_kv_heads rows) pairs in 32-bit.
+// The attention kernel walks the attended-row slots of all queries, n_q * (prefix + k), in 32-bit.
 dsa_status check_tiles(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_t prefix) {
-  const int64_t rows = 128 / kv.hkv;
-  if ((int64_t)qs.n_q * (((int64_t)prefix + k + rows - 1) / rows) >= (int64_t(1) << 31))
-    return fail(DSA_ERR_UNSUPPORTED, "n_q * ceil((prefix_len + k) / (128 / num_kv_heads)) must stay below 2^31");
+  (void)kv;
+  if ((int64_t)qs.n_q * ((int64_t)prefix + k) >= (int64_t(1) << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "n_q * (prefix_len + k) must stay below 2^31");
   return DSA_OK;
 }
 

@@ -61,8 +61,8 @@ struct AttnParams {
   int piece;         // bytes of one position's K (or V): hkv * 256
   int pitch;         // shared-memory row pitch: piece + 16
   float scale_log2;
-  int tiles;         // n_q * tiles_per_q (< 2^31, checked on the host)
-  int tiles_per_q;
+  int units;         // n_q * rows_per_q attended-row slots (< 2^31, checked on the host)
+  int rows_per_q;    // prefix + k
   float* part_o;     // [grid][2 slots][hq][128]
   float2* part_ml;   // [grid][2 slots][hq]
   void* out;
@@ -95,11 +95,15 @@ __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi) {
 
 enum : int { kFirst = 1, kLast = 2, kWhole = 4 };
 
-// The tiles a CTA handles, in order, without the empty ones (a segment's last
-// tile is always kept so that the segment closes).  A segment is the run of a
-// query's tiles inside one CTA's range.
+// The work of all queries is the sequence of their attended-row slots, P + k
+// per query (slots past a query's actual row count are empty).  A CTA takes
+// one contiguous range of it and walks it in tiles of up to `rows` rows that
+// break at query boundaries, so every CTA gets the same number of rows to
+// within one.  Empty tiles are skipped, but a segment's last tile is always
+// kept so that the segment closes.  A segment is the run of a query's rows
+// inside one CTA's range.
 struct Cursor {
-  int ti, t_begin, t_end, qi, seg_start;
+  int x, x_begin, x_end, qi, seg_start;
   QueryInfo qf;
   bool fresh;
 };
@@ -109,35 +113,37 @@ struct Tile {
 };
 
 __device__ __forceinline__ void cursor_init(Cursor& c, const AttnParams& p) {
-  c.t_begin = range_begin(p.tiles, gridDim.x, blockIdx.x);
-  c.t_end = range_begin(p.tiles, gridDim.x, blockIdx.x + 1);
-  c.ti = c.t_begin;
+  c.x_begin = range_begin(p.units, gridDim.x, blockIdx.x);
+  c.x_end = range_begin(p.units, gridDim.x, blockIdx.x + 1);
+  c.x = c.x_begin;
   c.qi = -1;
-  c.seg_start = c.t_begin;
+  c.seg_start = c.x_begin;
   c.fresh = false;
 }
 
 __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* t) {
-  const int TP = p.tiles_per_q;
-  while (c.ti < c.t_end) {
-    const int ti = c.ti++;
-    const int qi = ti / TP;
-    const int tt = ti - qi * TP;
+  const int RPQ = p.rows_per_q;
+  while (c.x < c.x_end) {
+    const int x = c.x;
+    const int qi = x / RPQ;
+    const int r = x - qi * RPQ;
+    const int q_end = (qi + 1) * RPQ;
+    c.x = x + min(min(c.x_end, q_end) - x, p.rows);
     if (qi != c.qi) {
       c.qi = qi;
       c.qf = query_info(p, qi);
-      c.seg_start = ti;
+      c.seg_start = x;
       c.fresh = true;
     }
-    const int nvalid = min(max(c.qf.rows - tt * p.rows, 0), p.rows);
-    const bool last = ti == c.t_end - 1 || tt == TP - 1;
+    const int nvalid = min(max(c.qf.rows - r, 0), c.x - x);
+    const bool last = c.x == c.x_end || c.x == q_end;
     if (nvalid == 0 && !last) continue;
     t->qf = c.qf;
-    t->r0 = tt * p.rows;
+    t->r0 = r;
     t->nvalid = nvalid;
     t->flags = (c.fresh ? kFirst : 0) | (last ? kLast : 0) |
-               (last && c.seg_start == qi * TP && tt == TP - 1 ? kWhole : 0);
-    t->slot = c.seg_start == c.t_begin ? 0 : 1;
+               (last && c.seg_start == qi * RPQ && c.x == q_end ? kWhole : 0);
+    t->slot = c.seg_start == c.x_begin ? 0 : 1;
     c.fresh = false;
     return true;
   }
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.group;
-  if (range_begin(p.tiles, gridDim.x, blockIdx.x) >= range_begin(p.tiles, gridDim.x, blockIdx.x + 1)) return;
+  if (range_begin(p.units, gridDim.x, blockIdx.x) >= range_begin(p.units, gridDim.x, blockIdx.x + 1)) return;
 
   // Set-up that touches no global memory runs before the wait on the previous kernel.
   if (tid == 0) {
@@ -463,8 +469,8 @@ constexpr int kCombBatch = 24;                      // partials in flight per th
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnParams p, int grid_ctas) {
   // The boundary arithmetic reads no memory: it runs before the wait on the
   // attention kernel, and blocks with no cut query leave without waiting.
-  const int T = p.tiles, TP = p.tiles_per_q;
-  const int x = range_begin(T, grid_ctas, blockIdx.x + 1);  // first tile of CTA blockIdx.x + 1
+  const int T = p.units, TP = p.rows_per_q;
+  const int x = range_begin(T, grid_ctas, blockIdx.x + 1);  // first row slot of CTA blockIdx.x + 1
   const int qi = x / TP;
   if (x == qi * TP) return;  // no query is cut at this boundary
   const int first = qi * TP;
@@ -572,8 +578,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.piece = a.kv.hkv * kHeadDim * 2;
   p.pitch = p.piece + kRowPad;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.tiles_per_q = (a.prefix + a.k + p.rows - 1) / p.rows;
-  p.tiles = (int)((long long)a.qs.n_q * p.tiles_per_q);
+  p.rows_per_q = a.prefix + a.k;
+  p.units = (int)((long long)a.qs.n_q * p.rows_per_q);
   p.part_o = a.ws.part_o;
   p.part_ml = a.ws.part_ml;
   p.out = a.out;
@@ -582,7 +588,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   int dev = 0;
   cudaGetDevice(&dev);
   int grid = (dev >= 0 && dev < 64 && g_attn_grid[dev] > 0) ? g_attn_grid[dev] : 148;
-  if (grid > p.tiles) grid = p.tiles;
+  if (grid > p.units) grid = p.units;
   cudaError_t e;
   if (!a.slot) {  // stand-alone call: resolve the selected positions first
     const long long n = (long long)a.qs.n_q * a.k;
