@@ -459,14 +459,31 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 // boundary between CTAs c and c + 1 of the attention grid.  A query cut by the
 // nb boundaries c_lo .. c_hi - 1 has n = nb + 1 partials (one per CTA
 // c_lo .. c_hi); the block of its j-th boundary merges the query heads
-// h = j, j + nb, j + 2 nb, ..., four at a time, one thread per (head, column).
-// A thread issues the loads of its partials at once (up to 24 in flight)
-// and merges them in one pass: no barrier, one round trip per 24 partials.
-constexpr int kCombThreads = 512;
-constexpr int kCombHeads = kCombThreads / kHeadDim;  // heads merged at once
-constexpr int kCombBatch = 24;                      // partials in flight per thread
+// h = j, j + nb, j + 2 nb, ..., four at a time.  A head has four warps: warp
+// s of the head takes the partials i = s, s + 4, s + 8, ..., each lane four
+// columns (one 16-byte load per partial), and the four running states
+// (max, sum, accumulator) meet in shared memory.  A thread keeps up to
+// kCombBatch partials in flight, so up to 32 partials are one round trip.
+constexpr int kCombHeads = 4;                                // heads merged at once
+constexpr int kCombSplit = 4;                                // warps per head
+constexpr int kCombThreads = 32 * kCombHeads * kCombSplit;  // 512
+constexpr int kCombBatch = 8;                                // partials in flight per thread
+
+__device__ __forceinline__ void write_out4(const AttnParams& p, size_t head, int lane, float4 v) {
+  if (p.out_dtype == 0) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(p.out)[head * (kHeadDim / 4) + lane] = u;
+  } else {
+    reinterpret_cast<float4*>(p.out)[head * (kHeadDim / 4) + lane] = v;
+  }
+}
 
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnParams p, int grid_ctas) {
+  __shared__ float4 s_acc[kCombHeads][kCombSplit][32];
+  __shared__ float2 s_ml[kCombHeads][kCombSplit];
   // The boundary arithmetic reads no memory: it runs before the wait on the
   // attention kernel, and blocks with no cut query leave without waiting.
   const int T = p.units, TP = p.rows_per_q;
@@ -476,46 +493,72 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnPa
   const int first = qi * TP;
   const int c_lo = cta_of(T, grid_ctas, first), c_hi = cta_of(T, grid_ctas, first + TP - 1);
   const int j = (int)blockIdx.x - c_lo, nb = c_hi - c_lo, n = nb + 1;
-  const int d = threadIdx.x & (kHeadDim - 1);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hg = warp / kCombSplit, sub = warp % kCombSplit;
   // The partial of CTA c for this query sits in slot 0 if the query's segment
   // starts the CTA's range, else in slot 1.
   const int c_first = range_begin(T, grid_ctas, c_lo) >= first ? 0 : 1;  // slot of CTA c_lo
+  const float4* part_o = reinterpret_cast<const float4*>(p.part_o);
   pdl_wait();
   pdl_trigger();
-  for (int h = j + (int)(threadIdx.x / kHeadDim) * nb; h < p.hq; h += kCombHeads * nb) {
-    float M = -INFINITY, Lsum = 0.f, acc = 0.f;
-    for (int i0 = 0; i0 < n; i0 += kCombBatch) {
+  // The trip count depends on hg only, so the four warps of a head meet at
+  // the same named barriers.
+  for (int h = j + hg * nb; h < p.hq; h += kCombHeads * nb) {
+    float M = -INFINITY, Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = sub; i0 < n; i0 += kCombSplit * kCombBatch) {
       float2 ml[kCombBatch];
-      float v[kCombBatch];
+      float4 v[kCombBatch];
 #pragma unroll
       for (int u = 0; u < kCombBatch; ++u) {
-        const int i = i0 + u;
+        const int i = i0 + u * kCombSplit;
         if (i < n) {
-          const size_t sl = (size_t)(c_lo + i) * 2 + (i == 0 ? c_first : 0);
-          ml[u] = __ldg(&p.part_ml[sl * p.hq + h]);
-          v[u] = __ldg(&p.part_o[(sl * p.hq + h) * kHeadDim + d]);
+          const int ph = ((c_lo + i) * 2 + (i == 0 ? c_first : 0)) * p.hq + h;  // < 2 * 320 * 64
+          ml[u] = __ldg(&p.part_ml[ph]);
+          v[u] = __ldg(&part_o[ph * (kHeadDim / 4) + lane]);
         }
       }
       float Mb = M;
 #pragma unroll
       for (int u = 0; u < kCombBatch; ++u)
-        if (i0 + u < n) Mb = fmaxf(Mb, ml[u].x);
+        if (i0 + u * kCombSplit < n) Mb = fmaxf(Mb, ml[u].x);
       const float Ms = Mb == -INFINITY ? 0.f : Mb;
       const float a = exp2f(M - Ms);  // rescale of what earlier batches summed
       Lsum *= a;
-      acc *= a;
+      acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
 #pragma unroll
       for (int u = 0; u < kCombBatch; ++u)
-        if (i0 + u < n) {
+        if (i0 + u * kCombSplit < n) {
           const float w = exp2f(ml[u].x - Ms);
           Lsum += w * ml[u].y;
-          acc += w * v[u];
+          acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
         }
       M = Mb;
     }
-    const size_t head = (size_t)qi * p.hq + h;
-    write_out(p, head, d, acc / Lsum);
-    if (d == 0 && p.lse) p.lse[head] = ((M == -INFINITY ? 0.f : M) + log2f(Lsum)) * 0.69314718055994531f;
+    s_acc[hg][sub][lane] = acc;
+    if (lane == 0) s_ml[hg][sub] = make_float2(M, Lsum);
+    named_bar_sync(1 + hg, 32 * kCombSplit);
+    if (sub == 0) {
+      float Mx = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < kCombSplit; ++s) Mx = fmaxf(Mx, s_ml[hg][s].x);
+      const float Ms = Mx == -INFINITY ? 0.f : Mx;
+      float L = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < kCombSplit; ++s) {
+        const float2 st = s_ml[hg][s];
+        const float4 av = s_acc[hg][s][lane];
+        const float w = exp2f(st.x - Ms);
+        L += w * st.y;
+        o.x += w * av.x; o.y += w * av.y; o.z += w * av.z; o.w += w * av.w;
+      }
+      const float r = 1.f / L;
+      const size_t head = (size_t)qi * p.hq + h;
+      write_out4(p, head, lane, make_float4(o.x * r, o.y * r, o.z * r, o.w * r));
+      if (lane == 0 && p.lse) p.lse[head] = (Ms + log2f(L)) * 0.69314718055994531f;
+    }
+    named_bar_sync(1 + hg, 32 * kCombSplit);  // shared state is rewritten by the next head
   }
 }
 
