@@ -22,10 +22,14 @@ __device__ int g_status;
 // Highest bin b with sum(bins >= b) >= k among nb (256 or 1024) bins in shared
 // memory, and the count above it; one warp.  *bin = -1 when the total is below k.
 __device__ __forceinline__ void warp_hist_threshold(const int* h, int nb, int k, int lane, int* bin, int* above) {
-  const int gs = nb / 32;  // bins per lane group
-  int sum = 0;
-  for (int i = 0; i < gs; ++i) sum += h[gs * lane + ((i + lane) % gs)];
-  int suf = sum;
+  const int gs = nb / 32;  // bins per lane group (8 or 32)
+  // Four independent sums over the group's bins, read in a lane-rotated order
+  // (no bank conflicts).
+  int s4[4] = {0, 0, 0, 0};
+  for (int i = 0; i < gs; i += 4)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) s4[u] += h[gs * lane + ((i + u + lane) & (gs - 1))];
+  int suf = (s4[0] + s4[1]) + (s4[2] + s4[3]);
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_down_sync(0xffffffffu, suf, o);
@@ -108,13 +112,11 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ int slot_of(const SelectParams& p, int b, int t) {
   return load_block(p.bt, b, p.max_blocks, t >> 6, p.num_blocks, &g_status) * kBlock + (t & 63);
 }
-// Reads an int of CTA `rank`'s shared memory at the address of `p` in this CTA.
-__device__ __forceinline__ int ld_remote(const int* p, uint32_t rank) {
+// Writes v to CTA `rank`'s shared memory at the address of `p` in this CTA.
+__device__ __forceinline__ void st_remote(int* p, uint32_t rank, int v) {
   uint32_t a;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
-  int v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 // Scores of positions t .. t + 15 (t a multiple of 16) kept where lo_t <= t' < hi_t,
@@ -170,11 +172,14 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   int* gh = p.coarse + (size_t)b * kCoarseBins;
   const int a0 = tb & ~(kSelPer - 1);
   // First round of scores and slots, then the histogram: all in flight together.
+  static_assert(kCoarseBins == 2 * kSelThreads, "two histogram bins per thread");
+  const int h0 = __ldcg(gh + tid), h1 = __ldcg(gh + tid + kSelThreads);
   int v[kSelPer];
   int t = a0 + tid * kSelPer;  // 16 positions inside one 64-position block
   load_scores(row, p.ld, t, tb, te, v);
-  int slot0 = (out_slot && t < te) ? slot_of(p, b, t) : 0;  // slot of t; t + j is slot0 + j
-  for (int i = tid; i < kCoarseBins; i += kSelThreads) s_hist[i] = __ldcg(gh + i);
+  const int bt0 = (out_slot && t < te) ? __ldg(p.bt + (size_t)b * p.max_blocks + (t >> 6)) : 0;
+  s_hist[tid] = h0;
+  s_hist[tid + kSelThreads] = h1;
   if (tid < kCounts) s_counts[tid] = 0;
   __syncthreads();
   if (tid < 32) {  // one warp finds the threshold bin
@@ -184,6 +189,15 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   }
   __syncthreads();
   const int beta = s_misc[0];
+  int slot0 = 0;  // slot of t; t + j is slot0 + j
+  if (out_slot && t < te) {
+    slot0 = bt0;
+    if ((unsigned)slot0 >= (unsigned)p.num_blocks) {
+      set_status(&g_status, kStBadBlock);
+      slot0 = 0;
+    }
+    slot0 = slot0 * kBlock + (t & 63);
+  }
   int lo, width;
   if (beta > 0 && beta < kCoarseBins - 1) {
     lo = (beta - kCoarseOff) << kCoarseShift;
@@ -234,15 +248,18 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
 #pragma unroll
   for (int o = 16; o; o >>= 1) my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
   if (lane == 0 && my_above) atomicAdd(&s_counts[0], my_above);
-  if (C > 1) cluster_sync(); else __syncthreads();  // every rank's counts are final
-  if (r == 0)  // every rank has read the histogram: leave it zero for the next call
-    for (int i = tid; i < kCoarseBins; i += kSelThreads) gh[i] = 0;
-  // 2. every rank's counts
+  __syncthreads();
+  // 2. this rank's counts go to row r of every rank's table; after the cluster
+  //    barrier each CTA reads only its own shared memory, so no CTA touches
+  //    another's after it and none has to wait for the others before leaving.
   if (tid < C * kCounts) {
     const int rr = tid / kCounts, f = tid - rr * kCounts;
-    s_all[rr][f] = C > 1 ? ld_remote(&s_counts[f], rr) : s_counts[f];
+    if (C > 1) st_remote(&s_all[r][f], rr, s_counts[f]);
+    else s_all[0][f] = s_counts[f];
   }
-  __syncthreads();
+  if (C > 1) cluster_sync(); else __syncthreads();  // every rank's counts are in place
+  if (r == 0)  // every rank has read the histogram: leave it zero for the next call
+    for (int i = tid; i < kCoarseBins; i += kSelThreads) gh[i] = 0;
   if (tid < 32) {
     // Warp 0, lanes as fine bins: totals, suffix sums from the top of the window.
     int fine_f = 0;
@@ -302,19 +319,24 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   // 3. ordered write of this part's selection
   if (n_keep <= kSelCap) {
     // From the kept candidates: thread i takes entries [i * per, (i + 1) * per).
+    // One scan of (above tau, at tau) pairs, 16 bits each (n_keep <= 4096):
+    // ties in this CTA before the thread's entries, and of them those kept
+    // (global tie rank below the quota), give its output offset.
     const int per = (n_keep + kSelThreads - 1) / kSelThreads;
     const int e0 = min(n_keep, tid * per), e1 = min(n_keep, e0 + per);
-    int n_eq = 0;
-    for (int e = e0; e < e1; ++e) n_eq += e_sc[e] == tau;
-    int tot;
-    int tr = block_exclusive_scan(n_eq, s_scratch, &tot) + carry_ties;
-    int n_take = 0;
-    for (int e = e0, q = tr; e < e1; ++e) {
-      const int sc = e_sc[e];
-      n_take += sc > tau || (sc == tau && q++ < quota);
+    int n_gt = 0, n_eq = 0;
+    for (int e = e0; e < e1; ++e) {
+      n_gt += e_sc[e] > tau;
+      n_eq += e_sc[e] == tau;
     }
-    int o = block_exclusive_scan(n_take, s_scratch, &tot) + carry_out;
-    carry_out += tot;
+    int tot;
+    const int ex = block_exclusive_scan((n_eq << 16) | n_gt, s_scratch, &tot);
+    const int eq_before = ex >> 16, gt_before = ex & 0xffff;
+    const int tot_eq = tot >> 16, tot_gt = tot & 0xffff;
+    const int tie_room = max(quota - carry_ties, 0);  // ties this CTA may still keep
+    int tr = carry_ties + eq_before;
+    int o = carry_out + gt_before + min(eq_before, tie_room);
+    carry_out += tot_gt + min(tot_eq, tie_room);
     for (int e = e0; e < e1; ++e) {
       const int sc = e_sc[e];
       const bool take = sc > tau || (sc == tau && tr++ < quota);
@@ -366,7 +388,6 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
     for (int j = carry_out + tid; j < p.k; j += kSelThreads) out[j] = -1;
     if (tid == 0) p.n_sel[b] = min(carry_out, p.k);
   }
-  if (C > 1) cluster_sync();  // no CTA leaves while another may still read its counts
 }
 
 // ---------------------------------------------------------------- prefill ---
