@@ -382,8 +382,8 @@ def run_gpu(args, rank, world, local_rank):
         "config": config_block(spec, LAYERS),
         "hbm": {"step_bytes": ab["step"], "achieved_gbs": step_gbs, "peak_gbs": peak,
                 "frac": step_gbs / peak, "peak_kind": peak_kind},
-        "roofline": {"kernel": "dsa_sparse_attn_decode per call in a graph: resolve_slots_kernel + "
-                               "sparse_attn_kernel + attn_combine_kernel",
+        "roofline": {"kernel": "dsa_sparse_attn_decode per call in a graph: sparse_attn_kernel + "
+                               "attn_combine_kernel",
                      "bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                      "traffic": traffic, "algorithmic_bytes": ab["attention"], "ms": agg["attn_ms"],
                      "peak_kind": peak_kind},

@@ -146,7 +146,8 @@ Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
   }
   L.sel_end = off;
   L.attn_begin = off;
-  L.slot = take((size_t)qs.n_q * (size_t)k * 4);
+  if (qs.mode == DSA_MODE_DECODE)  // the fused decode step's selected cache slots
+    L.slot = take((size_t)qs.n_q * (size_t)k * 4);
   L.part_o = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 128 * 4);
   L.part_ml = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 8);
   L.total = off;
@@ -164,7 +165,6 @@ dsa::SelState sel_state(const Layout& L, void* ws, bool with_slot) {
 dsa::AttnWs attn_ws(const Layout& L, void* ws) {
   char* w = static_cast<char*>(ws);
   dsa::AttnWs a;
-  a.slot = reinterpret_cast<int*>(w + L.slot);
   a.part_o = reinterpret_cast<float*>(w + L.part_o);
   a.part_ml = reinterpret_cast<float2*>(w + L.part_ml);
   return a;

@@ -35,7 +35,6 @@ constexpr int kMaxAttnCtas = 320;       // persistent attention grid cap (partia
 constexpr int kCoarseBinsHost = 1024;   // coarse histogram bins (host-side copy of the device constant)
 
 struct AttnWs {
-  int* slot;        // [n_q][k]                    cache slot of every selected position
   float* part_o;    // [kMaxAttnCtas][2][Hq][128]  per-CTA partials of split queries (unnormalised O)
   float2* part_ml;  // [kMaxAttnCtas][2][Hq]       (max in log2 units, sum of weights)
 };
@@ -47,7 +46,8 @@ struct AttnArgs {
   int hq;
   const int32_t* idx;
   const int32_t* n_sel;
-  const int32_t* slot;     // cache slots of idx; null: resolved into ws.slot first
+  const int32_t* slot;     // cache slots of idx (the fused decode step), or null: the
+                           // attention kernel resolves the positions idx itself
   int k, prefix;
   float scale;
   void* out;

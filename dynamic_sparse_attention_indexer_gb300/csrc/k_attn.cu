@@ -54,7 +54,8 @@ struct AttnParams {
   const int32_t* bt;
   const int32_t* ctx;
   const int32_t* nsel;
-  const int32_t* slot;  // cache slot of every selected position, [n_q][k]
+  const int32_t* slot;  // cache slot of every selected position, [n_q][k], or null:
+  const int32_t* idx;   // then the selected positions themselves, [n_q][k]
   int mode, seq, pos0;
   int max_blocks, num_blocks, hkv, hq, group, k, prefix, max_ctx;
   int rows;          // attended rows per tile: 128 / hkv
@@ -150,26 +151,44 @@ __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* 
   return false;
 }
 
-// Cache slots are fetched one tile ahead of their use: fetch_raw issues the
-// load (the block id of a prefix row, the slot of a selected row), resolve
-// turns it into the slot when the copy is issued.
-__device__ __forceinline__ int fetch_raw(const AttnParams& p, const QueryInfo& qf, int r) {
-  return r < qf.n_pre ? __ldg(p.bt + (size_t)qf.seq * p.max_blocks + (r >> 6))
-                      : __ldg(p.slot + (size_t)qf.qi * p.k + (r - qf.n_pre));
+// Cache slots are fetched two tiles ahead of their use, in up to two
+// dependent loads: fetch_first issues the first (the block id of a prefix
+// row; the slot of a selected row, or its position when the call brings
+// positions instead of slots), fetch_second the second (the block id of a
+// selected position), and resolve makes the slot, validated against the pool,
+// when the copy is issued.
+struct RowRef {
+  int a;   // block id (lo >= 0) or cache slot (lo < 0), not yet validated
+  int lo;  // row inside the block, or -1
+};
+__device__ __forceinline__ int fetch_first(const AttnParams& p, const QueryInfo& qf, int r) {
+  if (r < qf.n_pre) return __ldg(p.bt + (size_t)qf.seq * p.max_blocks + (r >> 6));
+  const size_t e = (size_t)qf.qi * p.k + (r - qf.n_pre);
+  return p.slot ? __ldg(p.slot + e) : __ldg(p.idx + e);
 }
-__device__ __forceinline__ int resolve(const AttnParams& p, const QueryInfo& qf, int r, int raw) {
-  if (r >= qf.n_pre) {
-    if ((unsigned)raw >= (unsigned)p.num_blocks * kBlock) {
-      set_status(&g_status, kStBadBlock);
-      raw = 0;
-    }
-    return raw;
-  }
-  if ((unsigned)raw >= (unsigned)p.num_blocks) {
+__device__ __forceinline__ RowRef fetch_second(const AttnParams& p, const QueryInfo& qf, int r, int first) {
+  if (r < qf.n_pre) return RowRef{first, r & 63};  // prefix row r is position r
+  if (p.slot) return RowRef{first, -1};
+  int pos = first;
+  if ((unsigned)pos >= (unsigned)p.max_blocks * kBlock) {
     set_status(&g_status, kStBadBlock);
-    raw = 0;
+    pos = 0;
   }
-  return raw * kBlock + (r & 63);
+  return RowRef{__ldg(p.bt + (size_t)qf.seq * p.max_blocks + (pos >> 6)), pos & 63};
+}
+__device__ __forceinline__ int resolve(const AttnParams& p, RowRef v) {
+  if (v.lo < 0) {
+    if ((unsigned)v.a >= (unsigned)p.num_blocks * kBlock) {
+      set_status(&g_status, kStBadBlock);
+      return 0;
+    }
+    return v.a;
+  }
+  if ((unsigned)v.a >= (unsigned)p.num_blocks) {
+    set_status(&g_status, kStBadBlock);
+    return v.lo;
+  }
+  return v.a * kBlock + v.lo;
 }
 
 __device__ __forceinline__ void write_out(const AttnParams& p, size_t head, int d, float v) {
@@ -228,23 +247,29 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
     const int pt = lane * kProducerWarps + warp;
     const int n_copies = 2 * p.rows;
     auto filled = [&](const Tile& tl) { return min((tl.nvalid + 15) & ~15, p.rows); };
+    auto active = [&](const Tile& tl, int u) {
+      const int c = pt + u * kProducerThreads;
+      return c < n_copies && (c >> 1) < filled(tl);
+    };
+    auto row_of = [&](const Tile& tl, int u) { return tl.r0 + min((pt + u * kProducerThreads) >> 1, tl.nvalid - 1); };
     Cursor cur;
     cursor_init(cur, p);
-    Tile t;
-    bool have = next_tile(cur, p, &t);
-    int raw[2] = {0, 0};
-    auto fetch = [&](const Tile& tl) {
+    Tile t0, t1, t2;  // issued now, next, the one after
+    bool h0 = next_tile(cur, p, &t0);
+    bool h1 = h0 && next_tile(cur, p, &t1);
+    bool h2 = h1 && next_tile(cur, p, &t2);
+    RowRef v0[2];  // rows of t0, both loads issued
+    int f1[2];     // first loads of t1
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = pt + u * kProducerThreads;
-        raw[u] = (c < n_copies && (c >> 1) < filled(tl)) ? fetch_raw(p, tl.qf, tl.r0 + min(c >> 1, tl.nvalid - 1))
-                                                          : 0;
-      }
-    };
-    if (have) fetch(t);
+    for (int u = 0; u < 2; ++u) {
+      v0[u] = RowRef{0, -1};
+      f1[u] = 0;
+      if (h0 && active(t0, u)) v0[u] = fetch_second(p, t0.qf, row_of(t0, u), fetch_first(p, t0.qf, row_of(t0, u)));
+      if (h1 && active(t1, u)) f1[u] = fetch_first(p, t1.qf, row_of(t1, u));
+    }
     const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
     int n = 0, seg = 0;
-    while (have) {
+    while (h0) {
       const int s = n % kStages;
       if (n >= kStages && !mbar_wait(&empty[s], ((n / kStages) - 1) & 1)) {
         set_status(&g_status, kStTimeout);
@@ -252,13 +277,11 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         break;
       }
       if (*s_abort) break;
-      const bool first = t.flags & kFirst;
+      const bool first = t0.flags & kFirst;
       uint32_t bytes = 0;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = pt + u * kProducerThreads;
-        if (c < n_copies && (c >> 1) < filled(t)) bytes += p.piece;
-      }
+      for (int u = 0; u < 2; ++u)
+        if (active(t0, u)) bytes += p.piece;
       if (first && pt == 0) {
         if (seg > 0 && !mbar_wait(q_empty, (seg - 1) & 1)) {
           set_status(&g_status, kStTimeout);
@@ -272,18 +295,28 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int c = pt + u * kProducerThreads;
-        if (c < n_copies && (c >> 1) < filled(t)) {
+        if (active(t0, u)) {
           const int r = c >> 1;
-          const size_t sl = (size_t)resolve(p, t.qf, t.r0 + min(r, t.nvalid - 1), raw[u]);
+          const size_t sl = (size_t)resolve(p, v0[u]);
           const __nv_bfloat16* src = ((c & 1) ? p.vc : p.kc) + sl * p.hkv * kHeadDim;
           bulk_g2s(st + (c & 1) * p.rows * p.pitch + r * p.pitch, src, p.piece, &full[s]);
         }
       }
       if (first && pt == 0)
-        bulk_g2s(s_q, p.q + (size_t)t.qf.qi * p.hq * kHeadDim, q_bytes, &full[s]);
+        bulk_g2s(s_q, p.q + (size_t)t0.qf.qi * p.hq * kHeadDim, q_bytes, &full[s]);
       ++n;
-      have = next_tile(cur, p, &t);
-      if (have) fetch(t);
+      // Advance: second loads of the next tile, first loads of the one after.
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (h1 && active(t1, u)) v0[u] = fetch_second(p, t1.qf, row_of(t1, u), f1[u]);
+        if (h2 && active(t2, u)) f1[u] = fetch_first(p, t2.qf, row_of(t2, u));
+      }
+      const bool more = h2;
+      t0 = t1;
+      h0 = h1;
+      t1 = t2;
+      h1 = h2;
+      h2 = more && next_tile(cur, p, &t2);
     }
     return;
   }
@@ -564,26 +597,6 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnPa
 
 int g_attn_grid[64] = {};
 
-// Selected positions -> cache slots, validated against the pool (stand-alone calls).
-__global__ void resolve_slots_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ nsel,
-                                     const int32_t* __restrict__ bt, int mode, int seq0, int n_q, int k,
-                                     int max_blocks, int num_blocks, int32_t* __restrict__ slot) {
-  pdl_wait();
-  pdl_trigger();
-  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= (long long)n_q * k) return;
-  const int qi = (int)(e / k), j = (int)(e - (long long)qi * k);
-  if (j >= min(max(__ldg(nsel + qi), 0), k)) return;
-  const int seq = mode == 0 ? qi : seq0;
-  const int t = __ldg(idx + e);
-  int blk = 0;
-  if (t >= 0 && t < max_blocks * kBlock)
-    blk = load_block(bt, seq, max_blocks, t >> 6, num_blocks, &g_status);
-  else
-    set_status(&g_status, kStBadBlock);
-  slot[e] = blk * kBlock + (t & 63);
-}
-
 }  // namespace
 
 cudaError_t setup_attn_kernels() {
@@ -605,7 +618,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.bt = a.kv.block_table;
   p.ctx = a.kv.context_lens;
   p.nsel = a.n_sel;
-  p.slot = a.slot ? a.slot : a.ws.slot;
+  p.slot = a.slot;
+  p.idx = a.idx;
   p.mode = a.qs.mode;
   p.seq = a.qs.seq;
   p.pos0 = a.qs.pos0;
@@ -633,13 +647,6 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   int grid = (dev >= 0 && dev < 64 && g_attn_grid[dev] > 0) ? g_attn_grid[dev] : 148;
   if (grid > p.units) grid = p.units;
   cudaError_t e;
-  if (!a.slot) {  // stand-alone call: resolve the selected positions first
-    const long long n = (long long)a.qs.n_q * a.k;
-    e = launch_pdl(resolve_slots_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, 1, a.idx, a.n_sel,
-                   a.kv.block_table, a.qs.mode, a.qs.seq, a.qs.n_q, a.k, a.kv.max_blocks, a.kv.num_blocks,
-                   a.ws.slot);
-    if (e != cudaSuccess) return e;
-  }
   const dim3 block(kProducerThreads + 32 * a.kv.hkv);
   if (p.group <= 8)
     e = launch_pdl(sparse_attn_kernel<1>, dim3(grid), block, kSmemBytes, st, 1, p);

@@ -62,6 +62,30 @@ def test_decode_selection_cluster_sizes(lib, lens):
     _run(synth.small_spec(lens=lens, prefix_len=128, k=1024, hq=8, hkv=2))
 
 
+def _binary_keys(w):
+    """Index keys of 0s and 1s and an all-ones query: scores are counts in
+    [0, 64], so the k-th largest is shared by many positions in every part."""
+    g = torch.Generator().manual_seed(3)
+    w["idx_cache"].copy_(torch.randint(0, 2, tuple(w["idx_cache"].shape), generator=g).to(torch.int8))
+    w["q_idx"].fill_(1)
+
+
+def _zero_query(w):
+    w["q_idx"].zero_()
+
+
+@pytest.mark.parametrize("lens,k,mutate", [
+    ((12000, 16500), 8000, _zero_query),       # all scores equal: the tie quota ends inside rank 1
+    ((30000, 9000, 21000), 1024, _binary_keys),  # ties at the threshold in every part of 4
+    ((60000, 45001), 4000, _binary_keys),        # ... of 8
+])
+def test_decode_ties_across_cluster_parts(lib, lens, k, mutate):
+    """Ties at the k-th largest score spread over the CTAs of a selection
+    cluster: each part keeps its ties only while their rank over the whole
+    sequence is below the quota, so the lowest positions win."""
+    _run(synth.small_spec(lens=lens, prefix_len=128, k=k, hq=8, hkv=2), mutate=mutate)
+
+
 def test_decode_one_query_over_the_whole_grid(lib):
     """A single sequence whose attended rows are cut over every CTA of the
     persistent grid: over a hundred partials per head merged."""
@@ -181,6 +205,27 @@ def test_bad_block_table_sets_status_not_fault(lib):
     dsa.index_scores(kv, dsa.decode_queries(kv), w["q_idx"], 64, scores)
     assert dsa.check_device_status() == 4
     assert dsa.check_device_status() == 0    # read-and-clear
+    torch.cuda.synchronize()
+
+
+def test_bad_selected_position_sets_status_not_fault(lib):
+    """The stand-alone attention call resolves the positions it is given: one
+    outside the block table, or one whose block id lies outside the pool, is
+    reported through the status word and read from block 0 instead."""
+    import dynamic_sparse_attention_indexer_gb300 as dsa
+    spec = synth.small_spec(lens=(700, 900))
+    w = H.on(synth.make_workload(spec, 2, "cpu"), DEV)
+    res = H.run_decode_step(w, split_api=True)
+    kv = H.paged_kv(w)
+    idx = res["idx"].clone()
+    idx[0, 5] = 1 << 24                           # past max_blocks * 64
+    dsa.sparse_attn_decode(kv, w["q"], idx, res["n_sel"], 256, 64, res["out"], res["lse"], res["ws"])
+    assert dsa.check_device_status() == 4
+    idx = res["idx"].clone()
+    w["block_table"][1, int(idx[1, 0]) // 64] = w["k_cache"].shape[0] + 5
+    dsa.sparse_attn_decode(kv, w["q"], idx, res["n_sel"], 256, 64, res["out"], res["lse"], res["ws"])
+    assert dsa.check_device_status() == 4
+    assert dsa.check_device_status() == 0
     torch.cuda.synchronize()
 
 
