@@ -86,6 +86,7 @@ constexpr int kSelRound = kSelThreads * kSelPer;     // 8192 positions per round
 constexpr int kCounts = 1 + kFineBins;               // above, fine bins
 constexpr int kSelCap = 4096;                        // kept candidates per CTA in shared memory
 constexpr int kSelSmem = kSelCap * 3 * 4;
+constexpr int kSelSmemSpread = 120 * 1024;  // over half an SM's shared memory: one CTA per SM
 
 struct SelectParams {
   const int32_t* scores;
@@ -566,12 +567,34 @@ __global__ void __launch_bounds__(32 * kRowWarps) prefill_topk_kernel(const RowT
 
 }  // namespace
 
-bool g_sel16[64] = {};  // clusters of 16 CTAs can be scheduled on this device
+// Per device: clusters of 16 selection CTAs can be scheduled at all, and how
+// many clusters of 1, 2, 4, 8, 16 CTAs fit at once with one CTA per SM.
+bool g_sel16[64] = {};
+int g_spread_cap[64][5] = {};
+
+template <int C>
+int spread_capacity() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, 1);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = kSelSmemSpread;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<C>, &cfg) != cudaSuccess) n = 0;
+  return n;
+}
 
 cudaError_t setup_topk_kernels() {
   cudaError_t e = cudaSuccess;
   auto smem = [&](auto kernel) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmemSpread);
   };
   smem(decode_select_kernel<1>);
   smem(decode_select_kernel<2>);
@@ -581,6 +604,7 @@ cudaError_t setup_topk_kernels() {
   if (e != cudaSuccess) return e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaSuccess;
   // Clusters of 16 are beyond the portable size: use them only where the
   // occupancy query says at least one fits.
   if (cudaFuncSetAttribute(decode_select_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
@@ -597,10 +621,13 @@ cudaError_t setup_topk_kernels() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<16>, &cfg) == cudaSuccess && n > 0 && dev >= 0 &&
-        dev < 64)
-      g_sel16[dev] = true;
+    g_sel16[dev] = cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<16>, &cfg) == cudaSuccess && n > 0;
   }
+  g_spread_cap[dev][0] = spread_capacity<1>();
+  g_spread_cap[dev][1] = spread_capacity<2>();
+  g_spread_cap[dev][2] = spread_capacity<4>();
+  g_spread_cap[dev][3] = spread_capacity<8>();
+  g_spread_cap[dev][4] = g_sel16[dev] ? spread_capacity<16>() : 0;
   cudaGetLastError();  // a refused query leaves no error behind
   return cudaSuccess;
 }
@@ -624,17 +651,23 @@ cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, in
   // CTAs per sequence: about one round of scores each, at most 8 (16 where supported).
   int dev = 0;
   cudaGetDevice(&dev);
-  const int c_max = (dev >= 0 && dev < 64 && g_sel16[dev]) ? 16 : 8;
+  const bool known = dev >= 0 && dev < 64;
+  const int c_max = (known && g_sel16[dev]) ? 16 : 8;
   const long long n_max = (long long)kv.max_ctx - prefix;
   int c = 1;
   while (c < c_max && n_max > (long long)c * kSelRound) c *= 2;
+  // The selection is a chain of dependent steps: a CTA sharing its SM with
+  // another runs it markedly slower (measured).  Where every cluster of the
+  // launch fits with one CTA per SM, ask for enough shared memory to get that.
+  const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4;
+  const int sm = (known && g_spread_cap[dev][ci] >= kv.batch) ? kSelSmemSpread : kSelSmem;
   const dim3 grid(c, kv.batch), block(kSelThreads);
   switch (c) {
-    case 1: return launch_pdl(decode_select_kernel<1>, grid, block, kSelSmem, st, 1, p);
-    case 2: return launch_pdl(decode_select_kernel<2>, grid, block, kSelSmem, st, 2, p);
-    case 4: return launch_pdl(decode_select_kernel<4>, grid, block, kSelSmem, st, 4, p);
-    case 8: return launch_pdl(decode_select_kernel<8>, grid, block, kSelSmem, st, 8, p);
-    default: return launch_pdl(decode_select_kernel<16>, grid, block, kSelSmem, st, 16, p);
+    case 1: return launch_pdl(decode_select_kernel<1>, grid, block, sm, st, 1, p);
+    case 2: return launch_pdl(decode_select_kernel<2>, grid, block, sm, st, 2, p);
+    case 4: return launch_pdl(decode_select_kernel<4>, grid, block, sm, st, 4, p);
+    case 8: return launch_pdl(decode_select_kernel<8>, grid, block, sm, st, 8, p);
+    default: return launch_pdl(decode_select_kernel<16>, grid, block, sm, st, 16, p);
   }
 }
 
