@@ -29,9 +29,10 @@ __device__ int g_status;
 // consumer warps score one position per thread with __dp4a and release the
 // stage, with no CTA-wide barrier per group.  Every warp walks the same group
 // sequence, computed from the block ranges.  With the histogram, each consumer
-// warp counts its scores into its own shared 1024-bin coarse histogram and adds
-// it to the sequence's global histogram when its sequence changes (fire-and-
-// forget atomics; the selection kernel reads the completed histogram).
+// warp counts its scores into its own shared 1024-bin coarse histogram; when
+// the sequence changes (and at the end) the eight are summed and added to the
+// sequence's global histogram (fire-and-forget atomics; the selection kernel
+// reads the completed histogram).
 constexpr int kIdxConsumers = 8;                               // consumer warps
 constexpr int kIdxThreads = 32 * (1 + kIdxConsumers);          // 288
 constexpr int kIdxStages = 8;
@@ -96,16 +97,22 @@ __device__ __forceinline__ bool next_group(GroupCursor& c, const int* seg_start,
   return true;
 }
 
-// Adds a consumer warp's histogram of sequence b to the global one and clears it.
-__device__ __forceinline__ void flush_warp_hist(int* whist, int* gh, int lane) {
-  for (int i = lane; i < kCoarseBins; i += 32) {
-    const int h = whist[i];
-    if (h) {
-      atomicAdd(gh + i, h);
-      whist[i] = 0;
+// Sums the consumer warps' histograms of one sequence into its global one
+// (called by all consumer threads, ct = 0 .. 255); with `clear` the warp
+// histograms are zeroed for the next sequence before anyone counts again.
+__device__ __forceinline__ void flush_cta_hist(int* hist, int* gh, int ct, bool clear) {
+  constexpr int kConsumerThreads = 32 * kIdxConsumers;
+  named_bar_sync(1, kConsumerThreads);  // every warp's counts are in
+  for (int i = ct; i < kCoarseBins; i += kConsumerThreads) {
+    int sum = 0;
+#pragma unroll
+    for (int w = 0; w < kIdxConsumers; ++w) {
+      sum += hist[w * kCoarseBins + i];
+      if (clear) hist[w * kCoarseBins + i] = 0;
     }
+    if (sum) atomicAdd(gh + i, sum);
   }
-  __syncwarp();
+  if (clear) named_bar_sync(1, kConsumerThreads);
 }
 
 template <bool kHist>
@@ -195,8 +202,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
     const int s = n % kIdxStages;
     const int b = g.b, L = len[b];
     const bool want_hist = kHist && L - P > p.k;
-    if (kHist && b != hist_b) {
-      if (hist_b >= 0) flush_warp_hist(whist, p.coarse + (size_t)hist_b * kCoarseBins, lane);
+    if (kHist && b != hist_b) {  // the same group sequence in every consumer warp: uniform
+      if (hist_b >= 0) flush_cta_hist(hist, p.coarse + (size_t)hist_b * kCoarseBins, tid - 32, true);
       hist_b = want_hist ? b : -1;
     }
     if (b != qb) {
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-  if (kHist && hist_b >= 0) flush_warp_hist(whist, p.coarse + (size_t)hist_b * kCoarseBins, lane);
+  if (kHist && hist_b >= 0) flush_cta_hist(hist, p.coarse + (size_t)hist_b * kCoarseBins, tid - 32, false);
 }
 
 // Coarse histogram of existing scores (the stand-alone top-k call): one CTA per
