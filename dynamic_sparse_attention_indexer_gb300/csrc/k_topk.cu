@@ -120,6 +120,27 @@ __device__ __forceinline__ void st_remote(int* p, uint32_t rank, int v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
+// Raw scores of positions t .. t + 15 (t a multiple of 16); chunks wholly outside
+// [lo_t, hi_t) are not read.  mask_scores applies the range later, where the
+// values are used, so that no instruction waits on the loads before that.
+__device__ __forceinline__ void load_raw(const int32_t* row, int ld, int t, int lo_t, int hi_t, int4* x) {
+#pragma unroll
+  for (int q = 0; q < kSelPer / 4; ++q) {
+    const int tq = t + 4 * q;
+    x[q] = make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+    if (tq < ld && tq + 4 > lo_t && tq < hi_t) x[q] = __ldg(reinterpret_cast<const int4*>(row + tq));
+  }
+}
+__device__ __forceinline__ void mask_scores(const int4* x, int t, int lo_t, int hi_t, int* v) {
+#pragma unroll
+  for (int q = 0; q < kSelPer / 4; ++q) {
+    const int tq = t + 4 * q;
+    v[4 * q] = tq >= lo_t && tq < hi_t ? x[q].x : INT_MIN;
+    v[4 * q + 1] = tq + 1 >= lo_t && tq + 1 < hi_t ? x[q].y : INT_MIN;
+    v[4 * q + 2] = tq + 2 >= lo_t && tq + 2 < hi_t ? x[q].z : INT_MIN;
+    v[4 * q + 3] = tq + 3 >= lo_t && tq + 3 < hi_t ? x[q].w : INT_MIN;
+  }
+}
 // Scores of positions t .. t + 15 (t a multiple of 16) kept where lo_t <= t' < hi_t,
 // INT_MIN elsewhere; never reads past the row's ld entries.
 __device__ __forceinline__ void load_scores(const int32_t* row, int ld, int t, int lo_t, int hi_t, int* v) {
@@ -177,7 +198,8 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   const int h0 = __ldcg(gh + tid), h1 = __ldcg(gh + tid + kSelThreads);
   int v[kSelPer];
   int t = a0 + tid * kSelPer;  // 16 positions inside one 64-position block
-  load_scores(row, p.ld, t, tb, te, v);
+  int4 xr[kSelPer / 4];
+  load_raw(row, p.ld, t, tb, te, xr);
   const int bt0 = (out_slot && t < te) ? __ldg(p.bt + (size_t)b * p.max_blocks + (t >> 6)) : 0;
   s_hist[tid] = h0;
   s_hist[tid + kSelThreads] = h1;
@@ -212,6 +234,7 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   const int hi = lo + width;
   // 1. this part's candidates (s >= lo), in position order, into shared memory;
   //    counts per fine bin of the window and above it.
+  mask_scores(xr, t, tb, te, v);
   int n_keep = 0, my_above = 0;
   for (int t0 = a0; t0 < te; t0 += kSelRound) {
     int vn[kSelPer];  // next round, loaded while this one is processed
