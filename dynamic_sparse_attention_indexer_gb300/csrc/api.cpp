@@ -47,6 +47,7 @@ dsa_status ensure_setup() {
   if ((e = dsa::setup_index_kernels()) != cudaSuccess) return cuda_fail("setup (index kernels)", e);
   if ((e = dsa::setup_topk_kernels()) != cudaSuccess) return cuda_fail("setup (top-k kernels)", e);
   if ((e = dsa::setup_attn_kernels()) != cudaSuccess) return cuda_fail("setup (attention kernels)", e);
+  if ((e = dsa::setup_prefix_kernels()) != cudaSuccess) return cuda_fail("setup (prefix kernel)", e);
   done[dev] = true;
   return DSA_OK;
 }
@@ -127,12 +128,13 @@ dsa_status check_scores(const int32_t* scores, int32_t ld, const dsa::KV& kv, co
 // call leaves them zero again.
 struct Layout {
   size_t coarse = 0, slot = 0;
+  size_t pre_ml = 0, pre_o = 0;  // 0 size: none
+  bool pre = false;
   size_t part_o = 0, part_ml = 0;
   size_t sel_end = 0, attn_begin = 0, total = 0;
 };
 
 Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
-  (void)prefix;
   Layout L;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -148,6 +150,11 @@ Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
   L.attn_begin = off;
   if (qs.mode == DSA_MODE_DECODE)  // the fused decode step's selected cache slots
     L.slot = take((size_t)qs.n_q * (size_t)k * 4);
+  if (qs.mode == DSA_MODE_PREFILL && prefix > 0) {  // the prefix part of every query, per tile of queries
+    L.pre = true;
+    L.pre_ml = take((size_t)qs.n_q * (size_t)hq * 8);
+    L.pre_o = take((size_t)qs.n_q * (size_t)hq * 128 * 4);
+  }
   L.part_o = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 128 * 4);
   L.part_ml = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 8);
   L.total = off;
@@ -165,6 +172,8 @@ dsa::SelState sel_state(const Layout& L, void* ws, bool with_slot) {
 dsa::AttnWs attn_ws(const Layout& L, void* ws) {
   char* w = static_cast<char*>(ws);
   dsa::AttnWs a;
+  a.pre_ml = L.pre ? reinterpret_cast<float2*>(w + L.pre_ml) : nullptr;
+  a.pre_o = L.pre ? reinterpret_cast<float*>(w + L.pre_o) : nullptr;
   a.part_o = reinterpret_cast<float*>(w + L.part_o);
   a.part_ml = reinterpret_cast<float2*>(w + L.part_ml);
   return a;
@@ -313,6 +322,7 @@ dsa_status dsa_check_device_status(cudaStream_t stream, int32_t* code) {
   DSA_CUDA("status (index)", dsa::read_clear_status_index(&c, stream));
   DSA_CUDA("status (top-k)", dsa::read_clear_status_topk(&c, stream));
   DSA_CUDA("status (attention)", dsa::read_clear_status_attn(&c, stream));
+  DSA_CUDA("status (prefix attention)", dsa::read_clear_status_prefix(&c, stream));
   DSA_CUDA("status (cache)", dsa::read_clear_status_misc(&c, stream));
   *code = c;
   return DSA_OK;

@@ -35,6 +35,8 @@ constexpr int kMaxAttnCtas = 320;       // persistent attention grid cap (partia
 constexpr int kCoarseBinsHost = 1024;   // coarse histogram bins (host-side copy of the device constant)
 
 struct AttnWs {
+  float2* pre_ml;   // prefill with a prefix: [n_q][Hq] prefix part (max in log2 units, sum), else null
+  float* pre_o;     // [n_q][Hq][128] its unnormalised output
   float* part_o;    // [kMaxAttnCtas][2][Hq][128]  per-CTA partials of split queries (unnormalised O)
   float2* part_ml;  // [kMaxAttnCtas][2][Hq]       (max in log2 units, sum of weights)
 };
@@ -68,6 +70,8 @@ cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx
 cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k,
                                 int32_t* idx, int32_t* n_sel, cudaStream_t st);
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_prefix_attn(const KV& kv, const QS& qs, const void* q, int hq, int prefix, float scale,
+                               float2* pre_ml, float* pre_o, cudaStream_t st);
 cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
                             const int8_t* idx_k, cudaStream_t st);
 cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, const int32_t* n_sel, int k,
@@ -77,12 +81,14 @@ cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, con
 cudaError_t setup_index_kernels();
 cudaError_t setup_topk_kernels();
 cudaError_t setup_attn_kernels();
+cudaError_t setup_prefix_kernels();
 
 // Device status words, one per kernel file: each reads its word into *code
 // (if *code is still 0) and clears it.
 cudaError_t read_clear_status_index(int* code, cudaStream_t st);
 cudaError_t read_clear_status_topk(int* code, cudaStream_t st);
 cudaError_t read_clear_status_attn(int* code, cudaStream_t st);
+cudaError_t read_clear_status_prefix(int* code, cudaStream_t st);
 cudaError_t read_clear_status_misc(int* code, cudaStream_t st);
 
 // Used by the allocation-free top-k entry point (defined in api.cpp).

@@ -69,6 +69,8 @@ struct AttnParams {
   void* out;
   int out_dtype;
   float* lse;
+  const float2* pre_ml;  // prefill: the prefix part of every query, computed per tile of
+  const float* pre_o;    // queries beforehand ([n_q][hq] and [n_q][hq][128]), or null
 };
 
 // 32-bit division when the products fit (the common case), 64-bit otherwise.
@@ -89,12 +91,12 @@ __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi) {
   qf.qi = qi;
   qf.seq = p.mode == 0 ? qi : p.seq;
   const int pos = p.mode == 0 ? min(__ldg(p.ctx + qi), p.max_ctx) - 1 : p.pos0 + qi;
-  qf.n_pre = max(0, min(p.prefix, pos + 1));
+  qf.n_pre = p.pre_ml ? 0 : max(0, min(p.prefix, pos + 1));  // with pre_ml every row is a selected one
   qf.rows = qf.n_pre + min(max(__ldg(p.nsel + qi), 0), p.k);
   return qf;
 }
 
-enum : int { kFirst = 1, kLast = 2, kWhole = 4 };
+enum : int { kFirst = 1, kLast = 2, kWhole = 4, kHead = 8 };  // kHead: the segment starts the query
 
 // The work of all queries is the sequence of their attended-row slots, P + k
 // per query (slots past a query's actual row count are empty).  A CTA takes
@@ -143,7 +145,8 @@ __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* 
     t->r0 = r;
     t->nvalid = nvalid;
     t->flags = (c.fresh ? kFirst : 0) | (last ? kLast : 0) |
-               (last && c.seg_start == qi * RPQ && c.x == q_end ? kWhole : 0);
+               (last && c.seg_start == qi * RPQ && c.x == q_end ? kWhole : 0) |
+               (c.fresh && c.seg_start == qi * RPQ ? kHead : 0);
     t->slot = c.seg_start == c.x_begin ? 0 : 1;
     c.fresh = false;
     return true;
@@ -359,6 +362,27 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         for (int j = 0; j < NT; ++j) o[i][j][0] = o[i][j][1] = o[i][j][2] = o[i][j][3] = 0.f;
 #pragma unroll
       for (int j = 0; j < NT; ++j) m[j][0] = m[j][1] = -INFINITY, l[j][0] = l[j][1] = 0.f;
+      if (p.pre_ml && (t.flags & kHead)) {
+        // The query's prefix part is the starting state of the segment that
+        // begins the query (its sum sits in one row group of lanes).
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int h = j * 8 + hc + e;
+            if (h >= G) continue;
+            const size_t head = (size_t)t.qf.qi * p.hq + (size_t)g * G + h;
+            const float2 ml = __ldg(p.pre_ml + head);
+            m[j][e] = ml.x;
+            l[j][e] = (lane >> 2) == 0 ? ml.y : 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int d = 16 * i + (lane >> 2);
+              o[i][j][e] = __ldg(p.pre_o + head * kHeadDim + d);
+              o[i][j][e + 2] = __ldg(p.pre_o + head * kHeadDim + d + 8);
+            }
+          }
+      }
     }
     const uint8_t* sk = smem + s * kStageBytes + g * (kHeadDim * 2);
     const uint8_t* sv = sk + p.rows * pitch;
@@ -635,7 +659,9 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.piece = a.kv.hkv * kHeadDim * 2;
   p.pitch = p.piece + kRowPad;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.rows_per_q = a.prefix + a.k;
+  p.pre_ml = a.ws.pre_ml;
+  p.pre_o = a.ws.pre_o;
+  p.rows_per_q = p.pre_ml ? a.k : a.prefix + a.k;
   p.units = (int)((long long)a.qs.n_q * p.rows_per_q);
   p.part_o = a.ws.part_o;
   p.part_ml = a.ws.part_ml;
@@ -647,6 +673,10 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   int grid = (dev >= 0 && dev < 64 && g_attn_grid[dev] > 0) ? g_attn_grid[dev] : 148;
   if (grid > p.units) grid = p.units;
   cudaError_t e;
+  if (p.pre_ml) {  // prefill: the prefix part of every query first, per tile of queries
+    e = launch_prefix_attn(a.kv, a.qs, a.q, a.hq, a.prefix, a.scale, a.ws.pre_ml, a.ws.pre_o, st);
+    if (e != cudaSuccess) return e;
+  }
   const dim3 block(kProducerThreads + 32 * a.kv.hkv);
   if (p.group <= 8)
     e = launch_pdl(sparse_attn_kernel<1>, dim3(grid), block, kSmemBytes, st, 1, p);

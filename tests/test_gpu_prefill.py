@@ -51,6 +51,17 @@ def test_prefill_full_int8_range(lib):
     _run(_prefill_spec(T=150, pos0=300, P=64, k=90, idx_lo=-128, idx_hi=127))
 
 
+def test_prefill_prefix_tiles_ragged(lib):
+    """The prefix part is computed per tile of queries: a group of 3 heads (42
+    queries per 128-row tile, two rows unused), a prefix of 130 (three 64-key
+    chunks, the last with 2 keys) and queries before, inside and past it."""
+    _run(_prefill_spec(T=300, pos0=10, P=130, k=80, hq=24, hkv=8))
+
+
+def test_prefill_without_prefix(lib):
+    _run(_prefill_spec(T=100, pos0=0, P=0, k=40))
+
+
 def test_full_prefill_16k(lib):
     spec = synth.CONFIGS[4]
     w = synth.make_workload(spec, 1004, DEV)
