@@ -43,7 +43,8 @@ constexpr int kPieceMax = 8 * kHeadDim * 2;       // K (or V) bytes of one posit
 constexpr int kStageBytes = 2 * kTileRowsMax * (kHeadDim * 2 + kRowPad);  // largest stage (Hkv = 1): 69,632
 constexpr int kMaxHq = 64;
 constexpr int kQBytes = kMaxHq * kHeadDim * 2;    // one query's Q, all heads: 16 KB
-constexpr int kSmemBytes = kStages * kStageBytes + kQBytes + 8 * (2 * kStages + 1) + 16;
+constexpr int kSmemBytes = kStages * kStageBytes + kQBytes + 8 * (2 * kStages + 2) + 16;
+static_assert(kProducerWarps == kStages + 1, "one producer warp per stage, plus the query copier");
 static_assert(2 * 16 * (kPieceMax + kRowPad) <= kStageBytes, "Hkv = 8 stage must fit");
 static_assert(kSmemBytes <= 232448, "attention shared memory above the 227 KB per-CTA limit");
 
@@ -212,14 +213,20 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t v) {
 }
 
 // NT: 8-head column tiles of a KV group (1 for G <= 8, 2 for G <= 16).
-template <int NT>
+// PS: producer layout.  false (decode): every producer thread walks every
+// tile and issues its share of the copies; Q rides on the segment's first
+// tile.  true (prefill, where L2-resident rows make the producer's per-tile
+// chain the limit): one producer warp per ring stage, each with kStages tile
+// times per tile, and Q copied by its own warp through a one-slot ring.
+template <int NT, bool PS>
 __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kernel(const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* s_q = smem + kStages * kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(s_q + kQBytes);
   uint64_t* empty = full + kStages;
   uint64_t* q_empty = empty + kStages;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(q_empty + 1);
+  uint64_t* q_full = q_empty + 1;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(q_full + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.group;
@@ -228,10 +235,11 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
   // Set-up that touches no global memory runs before the wait on the previous kernel.
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], kProducerThreads);
+      mbar_init(&full[s], PS ? 32 : kProducerThreads);
       mbar_init(&empty[s], p.hkv);
     }
     mbar_init(q_empty, p.hkv);
+    if (PS) mbar_init(q_full, 1);
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -241,85 +249,185 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 
   if (warp < kProducerWarps) {
     // ---------------------------------------------------------- producers
-    // Copy c of a tile (K of row c / 2 if c is even, V if odd) is issued by
-    // thread (c % 4) * 32 + (c / 4) % 32, so the copies spread over the warps.
-    // Rows from the valid count up to the next multiple of 16 (the rest of the
-    // last 16-row chunk the consumers read) get the last valid row again, so
-    // that every row the math touches holds finite cache values; their
-    // probabilities are zero.
-    const int pt = lane * kProducerWarps + warp;
-    const int n_copies = 2 * p.rows;
-    auto filled = [&](const Tile& tl) { return min((tl.nvalid + 15) & ~15, p.rows); };
-    auto active = [&](const Tile& tl, int u) {
-      const int c = pt + u * kProducerThreads;
-      return c < n_copies && (c >> 1) < filled(tl);
-    };
-    auto row_of = [&](const Tile& tl, int u) { return tl.r0 + min((pt + u * kProducerThreads) >> 1, tl.nvalid - 1); };
-    Cursor cur;
-    cursor_init(cur, p);
-    Tile t0, t1, t2;  // issued now, next, the one after
-    bool h0 = next_tile(cur, p, &t0);
-    bool h1 = h0 && next_tile(cur, p, &t1);
-    bool h2 = h1 && next_tile(cur, p, &t2);
-    RowRef v0[2];  // rows of t0, both loads issued
-    int f1[2];     // first loads of t1
+    if constexpr (!PS) {
+      // Copy c of a tile (K of row c / 2 if c is even, V if odd) is issued by
+      // thread (c % 4) * 32 + (c / 4) % 32, so the copies spread over the warps.
+      // Rows from the valid count up to the next multiple of 16 (the rest of the
+      // last 16-row chunk the consumers read) get the last valid row again, so
+      // that every row the math touches holds finite cache values; their
+      // probabilities are zero.
+      const int pt = lane * kProducerWarps + warp;
+      const int n_copies = 2 * p.rows;
+      auto filled = [&](const Tile& tl) { return min((tl.nvalid + 15) & ~15, p.rows); };
+      auto active = [&](const Tile& tl, int u) {
+        const int c = pt + u * kProducerThreads;
+        return c < n_copies && (c >> 1) < filled(tl);
+      };
+      auto row_of = [&](const Tile& tl, int u) { return tl.r0 + min((pt + u * kProducerThreads) >> 1, tl.nvalid - 1); };
+      Cursor cur;
+      cursor_init(cur, p);
+      Tile t0, t1, t2;  // issued now, next, the one after
+      bool h0 = next_tile(cur, p, &t0);
+      bool h1 = h0 && next_tile(cur, p, &t1);
+      bool h2 = h1 && next_tile(cur, p, &t2);
+      RowRef v0[2];  // rows of t0, both loads issued
+      int f1[2];     // first loads of t1
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      v0[u] = RowRef{0, -1};
-      f1[u] = 0;
-      if (h0 && active(t0, u)) v0[u] = fetch_second(p, t0.qf, row_of(t0, u), fetch_first(p, t0.qf, row_of(t0, u)));
-      if (h1 && active(t1, u)) f1[u] = fetch_first(p, t1.qf, row_of(t1, u));
-    }
-    const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
-    int n = 0, seg = 0;
-    while (h0) {
-      const int s = n % kStages;
-      if (n >= kStages && !mbar_wait(&empty[s], ((n / kStages) - 1) & 1)) {
-        set_status(&g_status, kStTimeout);
-        *s_abort = 1;
-        break;
+      for (int u = 0; u < 2; ++u) {
+        v0[u] = RowRef{0, -1};
+        f1[u] = 0;
+        if (h0 && active(t0, u)) v0[u] = fetch_second(p, t0.qf, row_of(t0, u), fetch_first(p, t0.qf, row_of(t0, u)));
+        if (h1 && active(t1, u)) f1[u] = fetch_first(p, t1.qf, row_of(t1, u));
       }
-      if (*s_abort) break;
-      const bool first = t0.flags & kFirst;
-      uint32_t bytes = 0;
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-        if (active(t0, u)) bytes += p.piece;
-      if (first && pt == 0) {
-        if (seg > 0 && !mbar_wait(q_empty, (seg - 1) & 1)) {
+      const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
+      int n = 0, seg = 0;
+      while (h0) {
+        const int s = n % kStages;
+        if (n >= kStages && !mbar_wait(&empty[s], ((n / kStages) - 1) & 1)) {
           set_status(&g_status, kStTimeout);
           *s_abort = 1;
+          break;
         }
-        bytes += q_bytes;
-      }
-      seg += first;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      uint8_t* st = smem + s * kStageBytes;
+        if (*s_abort) break;
+        const bool first = t0.flags & kFirst;
+        uint32_t bytes = 0;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = pt + u * kProducerThreads;
-        if (active(t0, u)) {
-          const int r = c >> 1;
-          const size_t sl = (size_t)resolve(p, v0[u]);
-          const __nv_bfloat16* src = ((c & 1) ? p.vc : p.kc) + sl * p.hkv * kHeadDim;
-          bulk_g2s(st + (c & 1) * p.rows * p.pitch + r * p.pitch, src, p.piece, &full[s]);
+        for (int u = 0; u < 2; ++u)
+          if (active(t0, u)) bytes += p.piece;
+        if (first && pt == 0) {
+          if (seg > 0 && !mbar_wait(q_empty, (seg - 1) & 1)) {
+            set_status(&g_status, kStTimeout);
+            *s_abort = 1;
+          }
+          bytes += q_bytes;
+        }
+        seg += first;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        uint8_t* st = smem + s * kStageBytes;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int c = pt + u * kProducerThreads;
+          if (active(t0, u)) {
+            const int r = c >> 1;
+            const size_t sl = (size_t)resolve(p, v0[u]);
+            const __nv_bfloat16* src = ((c & 1) ? p.vc : p.kc) + sl * p.hkv * kHeadDim;
+            bulk_g2s(st + (c & 1) * p.rows * p.pitch + r * p.pitch, src, p.piece, &full[s]);
+          }
+        }
+        if (first && pt == 0)
+          bulk_g2s(s_q, p.q + (size_t)t0.qf.qi * p.hq * kHeadDim, q_bytes, &full[s]);
+        ++n;
+        // Advance: second loads of the next tile, first loads of the one after.
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (h1 && active(t1, u)) v0[u] = fetch_second(p, t1.qf, row_of(t1, u), f1[u]);
+          if (h2 && active(t2, u)) f1[u] = fetch_first(p, t2.qf, row_of(t2, u));
+        }
+        const bool more = h2;
+        t0 = t1;
+        h0 = h1;
+        t1 = t2;
+        h1 = h2;
+        h2 = more && next_tile(cur, p, &t2);
+      }
+    } else {
+      // Producer warp w < kStages issues the tiles n with n % kStages == w, all
+      // into stage w, so it waits only on its own stage's previous use (no
+      // mbarrier phase of another warp's tile can alias) and has kStages tile
+      // times for each of its tiles.  Its lanes take the tile's rows in turn
+      // (row r by lane r % 32) and issue one bulk copy for the row's K and one
+      // for its V.  The cache slots of its next tile are fetched while the
+      // current one is issued, i.e. kStages tiles ahead (the second load of a
+      // position, its block id, then has kStages tile times as well), and those
+      // of the tile after it 2 * kStages tiles ahead.  Rows from the valid count
+      // up to the next multiple of 16 (the rest of the last 16-row chunk the
+      // consumers read) get the last valid row again, so that every row the math
+      // touches holds finite cache values; their probabilities are zero.  Warp
+      // kStages copies each segment's Q, in order, through a one-slot ring of
+      // its own (q_full / q_empty).
+      if (warp < kStages) {
+        const int w = warp;
+        const int R = (p.rows + 31) >> 5;  // rows per lane: 1 .. 4
+        auto filled = [&](const Tile& tl) { return min((tl.nvalid + 15) & ~15, p.rows); };
+        auto active = [&](const Tile& tl, int i) { return i < R && lane + 32 * i < filled(tl); };
+        auto row_of = [&](const Tile& tl, int i) { return tl.r0 + min(lane + 32 * i, tl.nvalid - 1); };
+        Cursor cur;
+        cursor_init(cur, p);
+        int n_walk = 0;
+        auto next_own = [&](Tile* t) {
+          Tile x;
+          while (next_tile(cur, p, &x))
+            if (n_walk++ % kStages == w) {
+              *t = x;
+              return true;
+            }
+          return false;
+        };
+        Tile t0, t1, t2;  // this warp's tile issued now, its next, the one after
+        bool h0 = next_own(&t0);
+        bool h1 = h0 && next_own(&t1);
+        bool h2 = h1 && next_own(&t2);
+        RowRef v0[4];  // rows of t0, both loads issued
+        int f1[4];     // first loads of t1
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v0[i] = RowRef{0, -1};
+          f1[i] = 0;
+          if (h0 && active(t0, i)) v0[i] = fetch_second(p, t0.qf, row_of(t0, i), fetch_first(p, t0.qf, row_of(t0, i)));
+          if (h1 && active(t1, i)) f1[i] = fetch_first(p, t1.qf, row_of(t1, i));
+        }
+        uint8_t* st = smem + w * kStageBytes;
+        for (int j = 0; h0; ++j) {
+          if (j > 0 && !mbar_wait(&empty[w], (j - 1) & 1)) {
+            set_status(&g_status, kStTimeout);
+            *s_abort = 1;
+            break;
+          }
+          if (*s_abort) break;
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (active(t0, i)) bytes += 2 * p.piece;
+          mbar_arrive_expect_tx(&full[w], bytes);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (active(t0, i)) {
+              const int r = lane + 32 * i;
+              const size_t off = (size_t)resolve(p, v0[i]) * p.hkv * kHeadDim;
+              bulk_g2s(st + r * p.pitch, p.kc + off, p.piece, &full[w]);
+              bulk_g2s(st + (p.rows + r) * p.pitch, p.vc + off, p.piece, &full[w]);
+            }
+          // Advance: second loads of the next tile, first loads of the one after.
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (h1 && active(t1, i)) v0[i] = fetch_second(p, t1.qf, row_of(t1, i), f1[i]);
+            if (h2 && active(t2, i)) f1[i] = fetch_first(p, t2.qf, row_of(t2, i));
+          }
+          const bool more = h2;
+          t0 = t1;
+          h0 = h1;
+          t1 = t2;
+          h1 = h2;
+          h2 = more && next_own(&t2);
+        }
+      } else if (lane == 0) {
+        const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
+        Cursor cur;
+        cursor_init(cur, p);
+        Tile t;
+        for (int seg = 0; next_tile(cur, p, &t);) {
+          if (!(t.flags & kFirst)) continue;
+          if (seg > 0 && !mbar_wait(q_empty, (seg - 1) & 1)) {
+            set_status(&g_status, kStTimeout);
+            *s_abort = 1;
+            break;
+          }
+          if (*s_abort) break;
+          mbar_arrive_expect_tx(q_full, q_bytes);
+          bulk_g2s(s_q, p.q + (size_t)t.qf.qi * p.hq * kHeadDim, q_bytes, q_full);
+          ++seg;
         }
       }
-      if (first && pt == 0)
-        bulk_g2s(s_q, p.q + (size_t)t0.qf.qi * p.hq * kHeadDim, q_bytes, &full[s]);
-      ++n;
-      // Advance: second loads of the next tile, first loads of the one after.
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (h1 && active(t1, u)) v0[u] = fetch_second(p, t1.qf, row_of(t1, u), f1[u]);
-        if (h2 && active(t2, u)) f1[u] = fetch_first(p, t2.qf, row_of(t2, u));
-      }
-      const bool more = h2;
-      t0 = t1;
-      h0 = h1;
-      t1 = t2;
-      h1 = h2;
-      h2 = more && next_tile(cur, p, &t2);
     }
     return;
   }
@@ -336,6 +444,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
   Cursor cur;
   cursor_init(cur, p);
   Tile t;
+  int seg = 0;
   for (int n = 0; next_tile(cur, p, &t); ++n) {
     const int s = n % kStages;
     if (!mbar_wait(&full[s], (n / kStages) & 1)) {
@@ -344,6 +453,14 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
       break;
     }
     if (t.flags & kFirst) {
+      if constexpr (PS) {
+        if (!mbar_wait(q_full, seg & 1)) {
+          set_status(&g_status, kStTimeout);
+          *s_abort = 1;
+          break;
+        }
+        ++seg;
+      }
       // Q fragments of this group's heads (heads past G repeat head G - 1; their
       // columns are never written out).
 #pragma unroll
@@ -624,9 +741,14 @@ int g_attn_grid[64] = {};
 }  // namespace
 
 cudaError_t setup_attn_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(sparse_attn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaSuccess;
+  auto smem = [&](auto kernel) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  };
+  smem(sparse_attn_kernel<1, false>);
+  smem(sparse_attn_kernel<2, false>);
+  smem(sparse_attn_kernel<1, true>);
+  smem(sparse_attn_kernel<2, true>);
   int dev = 0, sms = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -678,10 +800,13 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   const dim3 block(kProducerThreads + 32 * a.kv.hkv);
+  const bool ps = a.qs.mode == DSA_MODE_PREFILL;
   if (p.group <= 8)
-    e = launch_pdl(sparse_attn_kernel<1>, dim3(grid), block, kSmemBytes, st, 1, p);
+    e = ps ? launch_pdl(sparse_attn_kernel<1, true>, dim3(grid), block, kSmemBytes, st, 1, p)
+           : launch_pdl(sparse_attn_kernel<1, false>, dim3(grid), block, kSmemBytes, st, 1, p);
   else
-    e = launch_pdl(sparse_attn_kernel<2>, dim3(grid), block, kSmemBytes, st, 1, p);
+    e = ps ? launch_pdl(sparse_attn_kernel<2, true>, dim3(grid), block, kSmemBytes, st, 1, p)
+           : launch_pdl(sparse_attn_kernel<2, false>, dim3(grid), block, kSmemBytes, st, 1, p);
   if (e != cudaSuccess || grid < 2) return e;
   return launch_pdl(attn_combine_kernel, dim3(grid - 1), dim3(kCombThreads), 0, st, 1, p, grid);
 }
