@@ -403,12 +403,63 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args):
+    """The prefill path of the 16K workload (T = 16384 causal queries, 32/4
+    heads, prefix 576, k = 2048): scores, top-k and attention timed per call
+    with CUDA events on the stream they run on (not the decode headline)."""
+    import torch
+    import dynamic_sparse_attention_indexer_gb300 as dsa
+    import harness as H
+    import synth
+    spec = synth.CONFIGS[4]
+    w = synth.make_workload(spec, 1004, "cuda")
+    kv = H.paged_kv(w)
+    T, k, P, hq = spec.num_queries, spec.k, spec.prefix_len, spec.num_q_heads
+    qs = dsa.query_set(dsa.MODE_PREFILL, T, 0, 0)
+    ld = H.round4(T)
+    scores = torch.zeros((T, ld), dtype=torch.int32, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    n_sel = torch.empty(T, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, hq, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, hq), dtype=torch.float32, device="cuda")
+    ws = dsa.make_workspace(dsa.workspace_size(dsa.OP_PREFILL_STEP, kv, qs, k, hq, P), "cuda")
+    calls = {"index": lambda: dsa.index_scores(kv, qs, w["q_idx"], P, scores),
+             "topk": lambda: dsa.topk_select(kv, qs, scores, P, k, idx, n_sel, ws),
+             "attention": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws)}
+    st = torch.cuda.current_stream()
+    for _ in range(max(1, args.warmup)):
+        for f in calls.values():
+            f()
+    torch.cuda.synchronize()
+    ms = {}
+    for name, f in calls.items():
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(args.steps):
+            f()
+        b.record(st)
+        b.synchronize()
+        ms[name] = a.elapsed_time(b) / args.steps
+    assert dsa.check_device_status() == 0
+    total = sum(ms.values())
+    causal_pairs = sum(max(0, t + 1 - P) for t in range(T))  # scored (query, key) pairs
+    print(json.dumps({"metric": "DSA prefill tokens/s, 16K causal chunk, 1xGB300", "value": T / (total * 1e-3),
+                      "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": total, "higher_is_better": True, "dtype": "bf16 / int8 indexer",
+                      "data": "synthetic", "config": {"workload": spec.name, "queries": T, "prefix": P,
+                                                      "q_heads": hq, "kv_heads": spec.num_kv_heads, "top_k": k},
+                      "ms": ms, "indexer_tops": 2 * 64 * causal_pairs / (ms["index"] * 1e-3) / 1e12}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the 16K prefill path instead of the decode headline (one GPU)")
     ap.add_argument("--cpu-sample", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="repeat the CPU baseline's sample until about this much oracle time")
@@ -427,6 +478,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, rank, world)
+        return
+    if args.prefill:
+        if rank == 0:
+            run_prefill(args)
         return
     if world > 1:
         import torch
