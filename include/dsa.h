@@ -138,7 +138,12 @@ dsa_status dsa_kv_write(const dsa_paged_kv* kv, const int32_t* slot_mapping, int
 /* Bytes of workspace an op needs for these sizes (0 when it needs none, or on
  * invalid arguments: see the message).  A buffer sized for DSA_OP_DECODE_STEP
  * serves every decode op, one sized for DSA_OP_PREFILL_STEP every prefill op.
- * index_scores never needs one; pass NULL / 0 there. */
+ * index_scores never needs one; pass NULL / 0 there.  What it holds: per
+ * decode sequence a 4 KB coarse score histogram; for the fused decode step the
+ * selected cache slots (4 B per query and k); the attention's partial states
+ * of queries split over CTAs (about 330 KB per query head); and in prefill
+ * with a prefix, the prefix part of every (query, head): 520 B each (272 MB
+ * for 16K queries x 32 heads). */
 size_t dsa_workspace_size(int32_t op, const dsa_paged_kv* kv, const dsa_query_set* qs,
                           int32_t k, int32_t num_q_heads, int32_t prefix_len);
 /* Zeroes a workspace (async on `stream`).  Required once before first use: the
@@ -186,7 +191,11 @@ dsa_status dsa_sparse_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t
                                   int32_t prefix_len, float softmax_scale, void* out,
                                   int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
                                   cudaStream_t stream);
-/* Prefill form: the queries of `qs` (mode DSA_MODE_PREFILL). */
+/* Prefill form: the queries of `qs` (mode DSA_MODE_PREFILL).  With a prefix
+ * the prefix part of every query is computed first, once per tile of 128
+ * (query, head) rows (§2.4: the prefix is attended in full by every query),
+ * and the selected rows are then added to it; the workspace holds those
+ * partial states (see dsa_workspace_size). */
 dsa_status dsa_sparse_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q,
                                    int32_t num_q_heads, const int32_t* idx, const int32_t* n_sel,
                                    int32_t k, int32_t prefix_len, float softmax_scale, void* out,

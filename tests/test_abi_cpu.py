@@ -157,3 +157,10 @@ def test_workspace_sizes(lib):
     s3 = lib.dsa_workspace_size(3, C.byref(kv3), C.byref(qs3), 2048, 64, 1024)
     assert 8 * 2048 * 4 <= s3 < 64 << 20      # selected slots + attention partials, well under 64 MB
     assert lib.dsa_workspace_size(3, C.byref(kv3), C.byref(qs3), 0, 64, 1024) == 0   # invalid k
+    # prefill with a prefix holds the prefix part of every (query, head): 520 B each
+    kv4 = _kv(num_blocks=256, num_kv_heads=4, max_blocks_per_seq=256, batch=1, max_context_len=16384)
+    qs4 = _qs(1, 16384, 0, 0)
+    with_prefix = lib.dsa_workspace_size(4, C.byref(kv4), C.byref(qs4), 2048, 32, 576)
+    without = lib.dsa_workspace_size(4, C.byref(kv4), C.byref(qs4), 2048, 32, 0)
+    assert with_prefix - without >= 16384 * 32 * 520
+    assert without < 16 << 20                 # no per-query selection state in prefill
