@@ -80,9 +80,10 @@ __device__ __forceinline__ void warp_hist_threshold(const int* h, int nb, int k,
 // scores are loaded while the current one is processed: on this GPU a
 // dependent global access costs on the order of a microsecond.  No global
 // atomics, no fences, no hand-off between CTAs beyond two cluster barriers.
-constexpr int kSelThreads = 512;
-constexpr int kSelPer = 16;                          // consecutive positions per thread per round
-constexpr int kSelRound = kSelThreads * kSelPer;     // 8192 positions per round
+// A round is 8192 positions: 512 threads x 16, or (where the launch has one
+// CTA per SM anyway) 1024 threads x 8, which shortens each thread's serial part.
+constexpr int kSelRound = 8192;                      // positions per round
+constexpr int kSelThreads = 512;                     // threads of the packed launch
 constexpr int kCounts = 1 + kFineBins;               // above, fine bins
 constexpr int kSelCap = 4096;                        // kept candidates per CTA in shared memory
 constexpr int kSelSmem = kSelCap * 3 * 4;
@@ -123,17 +124,19 @@ __device__ __forceinline__ void st_remote(int* p, uint32_t rank, int v) {
 // Raw scores of positions t .. t + 15 (t a multiple of 16); chunks wholly outside
 // [lo_t, hi_t) are not read.  mask_scores applies the range later, where the
 // values are used, so that no instruction waits on the loads before that.
+template <int PER>
 __device__ __forceinline__ void load_raw(const int32_t* row, int ld, int t, int lo_t, int hi_t, int4* x) {
 #pragma unroll
-  for (int q = 0; q < kSelPer / 4; ++q) {
+  for (int q = 0; q < PER / 4; ++q) {
     const int tq = t + 4 * q;
     x[q] = make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
     if (tq < ld && tq + 4 > lo_t && tq < hi_t) x[q] = __ldg(reinterpret_cast<const int4*>(row + tq));
   }
 }
+template <int PER>
 __device__ __forceinline__ void mask_scores(const int4* x, int t, int lo_t, int hi_t, int* v) {
 #pragma unroll
-  for (int q = 0; q < kSelPer / 4; ++q) {
+  for (int q = 0; q < PER / 4; ++q) {
     const int tq = t + 4 * q;
     v[4 * q] = tq >= lo_t && tq < hi_t ? x[q].x : INT_MIN;
     v[4 * q + 1] = tq + 1 >= lo_t && tq + 1 < hi_t ? x[q].y : INT_MIN;
@@ -143,9 +146,10 @@ __device__ __forceinline__ void mask_scores(const int4* x, int t, int lo_t, int 
 }
 // Scores of positions t .. t + 15 (t a multiple of 16) kept where lo_t <= t' < hi_t,
 // INT_MIN elsewhere; never reads past the row's ld entries.
+template <int PER>
 __device__ __forceinline__ void load_scores(const int32_t* row, int ld, int t, int lo_t, int hi_t, int* v) {
 #pragma unroll
-  for (int q = 0; q < kSelPer / 4; ++q) {
+  for (int q = 0; q < PER / 4; ++q) {
     const int tq = t + 4 * q;
     int4 x = make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
     if (tq < ld && tq + 4 > lo_t && tq < hi_t) x = __ldg(reinterpret_cast<const int4*>(row + tq));
@@ -156,8 +160,10 @@ __device__ __forceinline__ void load_scores(const int32_t* row, int ld, int t, i
   }
 }
 
-template <int C>
-__global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const SelectParams p) {
+template <int C, int NTH>
+__global__ void __launch_bounds__(NTH) decode_select_kernel(const SelectParams p) {
+  constexpr int kSelThreads = NTH;               // threads of this launch
+  constexpr int kSelPer = kSelRound / NTH;       // consecutive positions per thread per round
   extern __shared__ __align__(16) int s_ent[];     // [kSelCap] positions | scores | slots
   __shared__ int s_hist[kCoarseBins];
   __shared__ int s_counts[kCounts];                // this rank's: above, fine bins
@@ -194,15 +200,17 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   int* gh = p.coarse + (size_t)b * kCoarseBins;
   const int a0 = tb & ~(kSelPer - 1);
   // First round of scores and slots, then the histogram: all in flight together.
-  static_assert(kCoarseBins == 2 * kSelThreads, "two histogram bins per thread");
-  const int h0 = __ldcg(gh + tid), h1 = __ldcg(gh + tid + kSelThreads);
+  constexpr int kHB = kCoarseBins / kSelThreads;  // histogram bins per thread
+  int hreg[kHB];
+#pragma unroll
+  for (int i = 0; i < kHB; ++i) hreg[i] = __ldcg(gh + tid + i * kSelThreads);
   int v[kSelPer];
-  int t = a0 + tid * kSelPer;  // 16 positions inside one 64-position block
+  int t = a0 + tid * kSelPer;  // kSelPer positions inside one 64-position block
   int4 xr[kSelPer / 4];
-  load_raw(row, p.ld, t, tb, te, xr);
+  load_raw<kSelPer>(row, p.ld, t, tb, te, xr);
   const int bt0 = (out_slot && t < te) ? __ldg(p.bt + (size_t)b * p.max_blocks + (t >> 6)) : 0;
-  s_hist[tid] = h0;
-  s_hist[tid + kSelThreads] = h1;
+#pragma unroll
+  for (int i = 0; i < kHB; ++i) s_hist[tid + i * kSelThreads] = hreg[i];
   if (tid < kCounts) s_counts[tid] = 0;
   __syncthreads();
   if (tid < 32) {  // one warp finds the threshold bin
@@ -234,14 +242,14 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   const int hi = lo + width;
   // 1. this part's candidates (s >= lo), in position order, into shared memory;
   //    counts per fine bin of the window and above it.
-  mask_scores(xr, t, tb, te, v);
+  mask_scores<kSelPer>(xr, t, tb, te, v);
   int n_keep = 0, my_above = 0;
   for (int t0 = a0; t0 < te; t0 += kSelRound) {
     int vn[kSelPer];  // next round, loaded while this one is processed
     const int tn = t + kSelRound;
     int slot_n = 0;
     if (t0 + kSelRound < te) {
-      load_scores(row, p.ld, tn, tb, te, vn);
+      load_scores<kSelPer>(row, p.ld, tn, tb, te, vn);
       slot_n = (out_slot && tn < te) ? slot_of(p, b, tn) : 0;
     }
     uint32_t cmask = 0;
@@ -276,8 +284,8 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   // 2. this rank's counts go to row r of every rank's table; after the cluster
   //    barrier each CTA reads only its own shared memory, so no CTA touches
   //    another's after it and none has to wait for the others before leaving.
-  if (tid < C * kCounts) {
-    const int rr = tid / kCounts, f = tid - rr * kCounts;
+  for (int e = tid; e < C * kCounts; e += kSelThreads) {
+    const int rr = e / kCounts, f = e - rr * kCounts;
     if (C > 1) st_remote(&s_all[r][f], rr, s_counts[f]);
     else s_all[0][f] = s_counts[f];
   }
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
     for (int t0 = a0; t0 < te; t0 += kSelRound) {
       const int tt = t0 + tid * kSelPer;
       int w[kSelPer];
-      load_scores(row, p.ld, tt, tb, te, w);
+      load_scores<kSelPer>(row, p.ld, tt, tb, te, w);
       const int s0 = (out_slot && tt < te) ? slot_of(p, b, tt) : 0;
       uint32_t gt_m = 0, eq_m = 0;
 #pragma unroll
@@ -595,11 +603,13 @@ __global__ void __launch_bounds__(32 * kRowWarps) prefill_topk_kernel(const RowT
 bool g_sel16[64] = {};
 int g_spread_cap[64][5] = {};
 
+constexpr int kSelThreadsSpread = 1024;  // threads of a launch with one CTA per SM
+
 template <int C>
 int spread_capacity() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, 1);
-  cfg.blockDim = dim3(kSelThreads);
+  cfg.blockDim = dim3(kSelThreadsSpread);
   cfg.dynamicSmemBytes = kSelSmemSpread;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -609,7 +619,7 @@ int spread_capacity() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<C>, &cfg) != cudaSuccess) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<C, kSelThreadsSpread>, &cfg) != cudaSuccess) n = 0;
   return n;
 }
 
@@ -619,19 +629,26 @@ cudaError_t setup_topk_kernels() {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmemSpread);
   };
-  smem(decode_select_kernel<1>);
-  smem(decode_select_kernel<2>);
-  smem(decode_select_kernel<4>);
-  smem(decode_select_kernel<8>);
-  smem(decode_select_kernel<16>);
+  smem(decode_select_kernel<1, kSelThreads>);
+  smem(decode_select_kernel<2, kSelThreads>);
+  smem(decode_select_kernel<4, kSelThreads>);
+  smem(decode_select_kernel<8, kSelThreads>);
+  smem(decode_select_kernel<16, kSelThreads>);
+  smem(decode_select_kernel<1, kSelThreadsSpread>);
+  smem(decode_select_kernel<2, kSelThreadsSpread>);
+  smem(decode_select_kernel<4, kSelThreadsSpread>);
+  smem(decode_select_kernel<8, kSelThreadsSpread>);
+  smem(decode_select_kernel<16, kSelThreadsSpread>);
   if (e != cudaSuccess) return e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaSuccess;
   // Clusters of 16 are beyond the portable size: use them only where the
   // occupancy query says at least one fits.
-  if (cudaFuncSetAttribute(decode_select_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-      cudaSuccess) {
+  if (cudaFuncSetAttribute(decode_select_kernel<16, kSelThreads>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(decode_select_kernel<16, kSelThreadsSpread>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           1) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16, 1);
     cfg.blockDim = dim3(kSelThreads);
@@ -644,7 +661,8 @@ cudaError_t setup_topk_kernels() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    g_sel16[dev] = cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<16>, &cfg) == cudaSuccess && n > 0;
+    g_sel16[dev] =
+        cudaOccupancyMaxActiveClusters(&n, decode_select_kernel<16, kSelThreads>, &cfg) == cudaSuccess && n > 0;
   }
   g_spread_cap[dev][0] = spread_capacity<1>();
   g_spread_cap[dev][1] = spread_capacity<2>();
@@ -681,16 +699,29 @@ cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, in
   while (c < c_max && n_max > (long long)c * kSelRound) c *= 2;
   // The selection is a chain of dependent steps: a CTA sharing its SM with
   // another runs it markedly slower (measured).  Where every cluster of the
-  // launch fits with one CTA per SM, ask for enough shared memory to get that.
+  // launch fits with one CTA per SM, ask for enough shared memory to get that,
+  // and give the CTA 1024 threads (8 positions each instead of 16).
   const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4;
-  const int sm = (known && g_spread_cap[dev][ci] >= kv.batch) ? kSelSmemSpread : kSelSmem;
-  const dim3 grid(c, kv.batch), block(kSelThreads);
+  const bool spread = known && g_spread_cap[dev][ci] >= kv.batch;
+  const dim3 grid(c, kv.batch);
+  if (spread) {
+    const dim3 block(kSelThreadsSpread);
+    const int sm = kSelSmemSpread;
+    switch (c) {
+      case 1: return launch_pdl(decode_select_kernel<1, kSelThreadsSpread>, grid, block, sm, st, 1, p);
+      case 2: return launch_pdl(decode_select_kernel<2, kSelThreadsSpread>, grid, block, sm, st, 2, p);
+      case 4: return launch_pdl(decode_select_kernel<4, kSelThreadsSpread>, grid, block, sm, st, 4, p);
+      case 8: return launch_pdl(decode_select_kernel<8, kSelThreadsSpread>, grid, block, sm, st, 8, p);
+      default: return launch_pdl(decode_select_kernel<16, kSelThreadsSpread>, grid, block, sm, st, 16, p);
+    }
+  }
+  const dim3 block(kSelThreads);
   switch (c) {
-    case 1: return launch_pdl(decode_select_kernel<1>, grid, block, sm, st, 1, p);
-    case 2: return launch_pdl(decode_select_kernel<2>, grid, block, sm, st, 2, p);
-    case 4: return launch_pdl(decode_select_kernel<4>, grid, block, sm, st, 4, p);
-    case 8: return launch_pdl(decode_select_kernel<8>, grid, block, sm, st, 8, p);
-    default: return launch_pdl(decode_select_kernel<16>, grid, block, sm, st, 16, p);
+    case 1: return launch_pdl(decode_select_kernel<1, kSelThreads>, grid, block, kSelSmem, st, 1, p);
+    case 2: return launch_pdl(decode_select_kernel<2, kSelThreads>, grid, block, kSelSmem, st, 2, p);
+    case 4: return launch_pdl(decode_select_kernel<4, kSelThreads>, grid, block, kSelSmem, st, 4, p);
+    case 8: return launch_pdl(decode_select_kernel<8, kSelThreads>, grid, block, kSelSmem, st, 8, p);
+    default: return launch_pdl(decode_select_kernel<16, kSelThreads>, grid, block, kSelSmem, st, 16, p);
   }
 }
 
