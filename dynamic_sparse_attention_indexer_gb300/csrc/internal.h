@@ -63,6 +63,8 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
                                 const SelState* sel, int k, cudaStream_t st);
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                const SelState& sel, cudaStream_t st);
+// Whether the decode selection of this batch runs with one CTA per SM.
+bool decode_select_spread(const KV& kv, int prefix);
 cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                  const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st);
 cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix,

@@ -35,15 +35,16 @@ __device__ int g_status;
 // reads the completed histogram).
 constexpr int kIdxConsumers = 8;                               // consumer warps
 constexpr int kIdxThreads = 32 * (1 + kIdxConsumers);          // 288
-constexpr int kIdxStages = 8;
+constexpr int kIdxStages = 8;          // ring stages; 6 where the selection CTAs are to fit beside
+constexpr int kIdxStagesShared = 6;    // a scoring CTA (they are then resident before it ends)
 constexpr int kGroupBlocks = 4;                                // cache blocks per stage
 constexpr int kIdxBlockBytes = kBlock * kIdxDim;               // 4096
 constexpr int kIdxStageBytes = kGroupBlocks * kIdxBlockBytes;  // 16 KB
 constexpr int kMaxRange = 2048;                                // candidate blocks per CTA at most
 constexpr int kScratchInts = 64;
 
-constexpr int idx_smem_bytes() {
-  return kIdxStages * kIdxStageBytes + 16 * kIdxStages /*bars*/ + 4 * (2 * kMaxDecodeBatch + 1) /*seg_start, len*/ +
+constexpr int idx_smem_bytes(int stages = kIdxStages) {
+  return stages * kIdxStageBytes + 16 * stages /*bars*/ + 4 * (2 * kMaxDecodeBatch + 1) /*seg_start, len*/ +
          4 * kMaxRange /*ids*/ + 4 * kIdxConsumers * kCoarseBins /*hist*/ + 4 * kScratchInts + 16;
 }
 
@@ -115,13 +116,13 @@ __device__ __forceinline__ void flush_cta_hist(int* hist, int* gh, int ct, bool 
   if (clear) named_bar_sync(1, kConsumerThreads);
 }
 
-template <bool kHist>
+template <bool kHist, int kStg>
 __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const DecodeIndexParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kIdxStages * kIdxStageBytes);
-  uint64_t* empty = full + kIdxStages;
-  int* seg_start = reinterpret_cast<int*>(empty + kIdxStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStg * kIdxStageBytes);
+  uint64_t* empty = full + kStg;
+  int* seg_start = reinterpret_cast<int*>(empty + kStg);
   int* len = seg_start + kMaxDecodeBatch + 1;
   int* ids = len + kMaxDecodeBatch;
   int* hist = ids + kMaxRange;
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
   if (kHist)
     for (int i = tid; i < kIdxConsumers * kCoarseBins; i += kIdxThreads) hist[i] = 0;
   if (tid == 0) {
-    for (int s = 0; s < kIdxStages; ++s) {
+    for (int s = 0; s < kStg; ++s) {
       mbar_init(&full[s], kGroupBlocks);
       mbar_init(&empty[s], kIdxConsumers);
     }
@@ -172,8 +173,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
     // ---- producer: lane i < 4 copies block i of each group
     if (lane >= kGroupBlocks) return;
     for (int n = 0; next_group(cur, seg_start, jb_base, &g); ++n) {
-      const int s = n % kIdxStages;
-      if (n >= kIdxStages && !mbar_wait(&empty[s], ((n / kIdxStages) - 1) & 1)) {
+      const int s = n % kStg;
+      if (n >= kStg && !mbar_wait(&empty[s], ((n / kStg) - 1) & 1)) {
         set_status(&g_status, kStTimeout);
         return;
       }
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
   int4 qc = make_int4(0, 0, 0, 0);  // chunk lane % 4 of the current sequence's query
   int hist_b = -1;                  // sequence whose counts sit in whist
   for (int n = 0; next_group(cur, seg_start, jb_base, &g); ++n) {
-    const int s = n % kIdxStages;
+    const int s = n % kStg;
     const int b = g.b, L = len[b];
     const bool want_hist = kHist && L - P > p.k;
     if (kHist && b != hist_b) {  // the same group sequence in every consumer warp: uniform
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
       qc = __ldg(reinterpret_cast<const int4*>(p.q_idx + (size_t)b * kIdxDim) + (lane & 3));
       qb = b;
     }
-    if (!mbar_wait(&full[s], (n / kIdxStages) & 1)) {
+    if (!mbar_wait(&full[s], (n / kStg) & 1)) {
       set_status(&g_status, kStTimeout);
       break;
     }
@@ -369,16 +370,19 @@ int g_index_grid[64] = {};  // persistent indexer CTAs per device (SMs x residen
 }
 
 cudaError_t setup_index_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(decode_index_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       idx_smem_bytes());
+  cudaError_t e = cudaFuncSetAttribute(decode_index_kernel<true, kIdxStages>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, idx_smem_bytes());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_index_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_index_kernel<false, kIdxStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              idx_smem_bytes());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_index_kernel<true, kIdxStagesShared>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, idx_smem_bytes(kIdxStagesShared));
   int dev = 0, sms = 0, per_sm = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_index_kernel<true>, kIdxThreads,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_index_kernel<true, kIdxStages>, kIdxThreads,
                                                       idx_smem_bytes());
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_index_grid[dev] = sms * (per_sm > 0 ? per_sm : 1);
   return e;
@@ -412,8 +416,17 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
   p.batch = kv.batch;
   p.k = k;
   const int grid = index_grid(kv, prefix);
-  if (sel) return launch_pdl(decode_index_kernel<true>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1, p);
-  return launch_pdl(decode_index_kernel<false>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1, p);
+  // In the fused step, where the selection packs its CTAs (they do not each
+  // take an SM), a smaller ring lets them be resident beside the scoring CTAs
+  // before those end (measured at 128K, B = 8: step 48.3 -> 47.9 us; where the
+  // selection has one CTA per SM the larger ring streams faster).
+  if (sel && !decode_select_spread(kv, prefix))
+    return launch_pdl(decode_index_kernel<true, kIdxStagesShared>, dim3(grid), dim3(kIdxThreads),
+                      idx_smem_bytes(kIdxStagesShared), st, 1, p);
+  if (sel)
+    return launch_pdl(decode_index_kernel<true, kIdxStages>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1,
+                      p);
+  return launch_pdl(decode_index_kernel<false, kIdxStages>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1, p);
 }
 
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,

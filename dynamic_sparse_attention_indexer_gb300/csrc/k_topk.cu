@@ -673,6 +673,28 @@ cudaError_t setup_topk_kernels() {
   return cudaSuccess;
 }
 
+// CTAs per sequence (about one round of scores each, at most 8, 16 where
+// supported) and whether every cluster fits with one CTA per SM.
+static void select_shape(const KV& kv, int prefix, int* c_out, bool* spread) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool known = dev >= 0 && dev < 64;
+  const int c_max = (known && g_sel16[dev]) ? 16 : 8;
+  const long long n_max = (long long)kv.max_ctx - prefix;
+  int c = 1;
+  while (c < c_max && n_max > (long long)c * kSelRound) c *= 2;
+  const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4;
+  *c_out = c;
+  *spread = known && g_spread_cap[dev][ci] >= kv.batch;
+}
+
+bool decode_select_spread(const KV& kv, int prefix) {
+  int c;
+  bool spread;
+  select_shape(kv, prefix, &c, &spread);
+  return spread;
+}
+
 cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                  const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
   SelectParams p;
@@ -689,20 +711,13 @@ cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, in
   p.idx = idx;
   p.n_sel = n_sel;
   p.slot = sel.slot;
-  // CTAs per sequence: about one round of scores each, at most 8 (16 where supported).
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const bool known = dev >= 0 && dev < 64;
-  const int c_max = (known && g_sel16[dev]) ? 16 : 8;
-  const long long n_max = (long long)kv.max_ctx - prefix;
-  int c = 1;
-  while (c < c_max && n_max > (long long)c * kSelRound) c *= 2;
   // The selection is a chain of dependent steps: a CTA sharing its SM with
   // another runs it markedly slower (measured).  Where every cluster of the
   // launch fits with one CTA per SM, ask for enough shared memory to get that,
   // and give the CTA 1024 threads (8 positions each instead of 16).
-  const int ci = c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4;
-  const bool spread = known && g_spread_cap[dev][ci] >= kv.batch;
+  int c;
+  bool spread;
+  select_shape(kv, prefix, &c, &spread);
   const dim3 grid(c, kv.batch);
   if (spread) {
     const dim3 block(kSelThreadsSpread);
