@@ -100,19 +100,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def code_digest(path):
+    """sha256 of a source file's code: // comments and blank lines removed, so
+    that comment edits do not count as a change of the kernel."""
+    import hashlib
+    import re
+    lines = []
+    for line in open(path).read().splitlines():
+        code = re.sub(r"//.*$", "", line).rstrip()
+        if code.strip():
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def profiled_attention_traffic():
     """DRAM bytes per attention call from the committed ncu summary, or None
-    once the attention source has changed since the counters were taken."""
-    import hashlib
+    once the attention code has changed since the counters were taken."""
     import re
     path = os.path.join(ROOT, "profiles", "decode_128k_kernels_full.md")
     src = os.path.join(ROOT, "dynamic_sparse_attention_indexer_gb300", "csrc", "k_attn.cu")
     try:
         text = open(path).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        digest = code_digest(src)
     except OSError:
         return None
-    m_sha = re.search(r"source_sha256\(k_attn\.cu\): ([0-9a-f]{64})", text)
+    m_sha = re.search(r"code_sha256\(k_attn\.cu\): ([0-9a-f]{64})", text)
     m_bytes = re.search(r"traffic_bytes_per_call: (\d+)", text)
     if not (m_sha and m_bytes) or m_sha.group(1) != digest:
         return None

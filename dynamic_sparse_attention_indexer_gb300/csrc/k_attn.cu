@@ -3,29 +3,35 @@
 //
 // The cache keeps, for every slot (block * 64 + row), the K rows of all KV heads
 // side by side (and the same for V), so one attended position is one contiguous
-// piece of Hkv * 256 bytes of K and one of V.  Work is cut into tiles of
-// 128 / Hkv attended rows of one query (64 KB of K and V whatever Hkv is); a
-// query's tiles cover its causal prefix rows, then its selected rows.  A
-// persistent grid (one CTA per SM) takes one contiguous range of the
-// (query, tile) sequence per CTA, so every CTA streams the same number of bytes
-// and the copy pipeline runs on across query boundaries (§2.3 decode: load only
-// the active KV, asynchronously).
+// piece of Hkv * 256 bytes of K and one of V.  A query has P + k attended-row
+// slots, its causal prefix rows then its selected rows (slots past its actual
+// rows are empty).  A persistent grid (one CTA per SM) takes one contiguous
+// range of the row slots of all queries per CTA (the same number of rows to
+// within one for every CTA) and walks it in tiles of up to 128 / Hkv rows
+// (64 KB of K and V whatever Hkv is) that break at query boundaries, so the
+// copy pipeline runs on across queries (§2.3 decode: load only the active KV,
+// asynchronously).  In prefill the prefix part of every query comes from the
+// prefix pass (k_prefix.cu) as the query's starting state, and only the
+// selected rows are walked here.
 //
 // Warp roles.  Four producer warps gather: every attended position of a tile is
 // two bulk copies (cp.async.bulk, K piece and V piece) into a three-stage ring of
-// shared memory, tracked by mbarriers, two tiles ahead of the math (§2.3
-// prefetch of the next block); the cache slots of a tile are loaded one tile
-// earlier still.  One consumer warp per KV head computes, for each 16-row chunk,
-// S^T = K Q^T and O^T = V^T P^T on the tensor cores (mma.sync m16n8k16 bf16, fp32
-// accumulate; P enters as two bf16 terms, hi + lo, so it keeps ~16 mantissa
-// bits), so the attended rows fill the 16-row M side and the G query heads
-// of the group the 8-wide N side; P^T reaches its operand layout through
-// movmatrix.  The online softmax runs per head column in base 2, reduced over
-// the row groups with warp shuffles, and O is rescaled only when a running max
-// moved.  A query whose tiles all fall in one CTA is written out directly; a
-// query cut by range boundaries leaves one partial (max, sum, unnormalised O)
-// per CTA, and attn_combine_kernel, launched right behind (programmatic
-// dependent launch), merges them.
+// shared memory, tracked by mbarriers, ahead of the math (§2.3 prefetch of the
+// next block); each row's cache slot is fetched two tiles before its copy (a
+// position given by the caller is resolved through the block table by a
+// second, dependent load).  In decode every producer thread walks every tile
+// and issues its share of the copies; in prefill one producer warp per stage
+// takes every third tile (see the PS parameter).  One consumer warp per KV
+// head computes, for each 16-row chunk, S^T = K Q^T and O^T = V^T P^T on the
+// tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate; P enters as two bf16
+// terms, hi + lo, so it keeps ~16 mantissa bits), so the attended rows fill the
+// 16-row M side and the G query heads of the group the 8-wide N side; P^T
+// reaches its operand layout through movmatrix.  The online softmax runs per
+// head column in base 2, reduced over the row groups with warp shuffles, and O
+// is rescaled only when a running max moved.  A query whose rows all fall in
+// one CTA is written out directly; a query cut by range boundaries leaves one
+// partial (max, sum, unnormalised O) per CTA, and attn_combine_kernel,
+// launched right behind (programmatic dependent launch), merges them.
 #include "common.cuh"
 #include "internal.h"
 

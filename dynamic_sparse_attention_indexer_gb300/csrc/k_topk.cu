@@ -76,10 +76,11 @@ __device__ __forceinline__ void warp_hist_threshold(const int* h, int nb, int k,
 //      quota, so the lower positions win).
 // A part with more than kSelCap kept candidates rescans its scores in step 3.
 // Global loads that do not depend on one another (the first round of scores,
-// their cache slots, the histogram) are issued together, and the next round's
+// their block ids, the histogram) are issued together, and the next round's
 // scores are loaded while the current one is processed: on this GPU a
 // dependent global access costs on the order of a microsecond.  No global
-// atomics, no fences, no hand-off between CTAs beyond two cluster barriers.
+// atomics, no fences; the only hand-off between CTAs is the pushed count
+// exchange before one cluster barrier.
 // A round is 8192 positions: 512 threads x 16, or (where the launch has one
 // CTA per SM anyway) 1024 threads x 8, which shortens each thread's serial part.
 constexpr int kSelRound = 8192;                      // positions per round
