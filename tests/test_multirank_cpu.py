@@ -53,3 +53,17 @@ def test_single_process_reduce_is_identity():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.reduce_over_ranks({"ms": 3.0}, "max") == {"ms": 3.0}
+
+
+def test_code_digest_ignores_comments(tmp_path):
+    """The profiled traffic stays valid across comment edits, not code edits."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    a, b, c = tmp_path / "a.cu", tmp_path / "b.cu", tmp_path / "c.cu"
+    a.write_text("// header\nint f(int x) {  // why\n  return x + 1;\n}\n")
+    b.write_text("// another header\n\nint f(int x) {\n  return x + 1;  // note\n}\n")
+    c.write_text("// header\nint f(int x) {\n  return x + 2;\n}\n")
+    assert bench.code_digest(str(a)) == bench.code_digest(str(b))
+    assert bench.code_digest(str(a)) != bench.code_digest(str(c))
