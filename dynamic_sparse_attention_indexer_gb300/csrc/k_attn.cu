@@ -70,7 +70,7 @@ struct AttnParams {
   int pitch;         // shared-memory row pitch: piece + 16
   float scale_log2;
   int units;         // n_q * rows_per_q attended-row slots (< 2^31, checked on the host)
-  int rows_per_q;    // prefix + k
+  int rows_per_q;    // prefix + k (k when the prefix part comes from pre_ml)
   float* part_o;     // [grid][2 slots][hq][128]
   float2* part_ml;   // [grid][2 slots][hq]
   void* out;
