@@ -344,15 +344,27 @@ def run_gpu(args, rank, world, local_rank):
     lse_host = torch.empty(b0["lse"].shape, dtype=torch.float32).pin_memory()
     n_e2e = max(8, min(args.steps, 500))
 
+    # One graph per layer holds the whole call sequence a serving loop makes for
+    # a step: the host-to-device copies of the step's queries (pinned host
+    # memory), the decode step, and the device-to-host copies of its output;
+    # the host waits for the result before the next step.
+    e2e_graphs = []
+    with torch.cuda.stream(stream):
+        for l in range(LAYERS):
+            w, kv, b, ws = layers[l]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                w["q"].copy_(q_host[l], non_blocking=True)
+                w["q_idx"].copy_(qi_host[l], non_blocking=True)
+                step(l)
+                out_host.copy_(b["out"], non_blocking=True)
+                lse_host.copy_(b["lse"], non_blocking=True)
+            e2e_graphs.append(g)
+    torch.cuda.synchronize()
+
     def e2e_step(i):
-        l = i % LAYERS
-        w, kv, b, ws = layers[l]
-        w["q"].copy_(q_host[l], non_blocking=True)
-        w["q_idx"].copy_(qi_host[l], non_blocking=True)
-        graphs[l].replay()
-        out_host.copy_(b["out"], non_blocking=True)
-        lse_host.copy_(b["lse"], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        e2e_graphs[i % LAYERS].replay()
+        stream.synchronize()
 
     with torch.cuda.stream(stream):
         for i in range(8):
