@@ -201,9 +201,14 @@ dsa_status check_tiles(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_t 
   return DSA_OK;
 }
 
+// The attention kernel stages one query's Q (all heads) in a shared-memory
+// slot sized for dsa::kMaxQHeads heads, so more heads are refused here, before
+// anything is launched.
 dsa_status check_heads(int32_t hq, const dsa::KV& kv) {
   if (hq < 1 || hq % kv.hkv != 0)
     return fail(DSA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", hq, kv.hkv);
+  if (hq > dsa::kMaxQHeads)
+    return fail(DSA_ERR_UNSUPPORTED, "num_q_heads %d above %d", hq, dsa::kMaxQHeads);
   if (hq / kv.hkv > 16) return fail(DSA_ERR_UNSUPPORTED, "GQA group %d > 16 query heads per KV head", hq / kv.hkv);
   return DSA_OK;
 }

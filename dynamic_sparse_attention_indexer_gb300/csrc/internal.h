@@ -33,6 +33,7 @@ constexpr int kMaxDecodeBatch = 2048;
 constexpr int kMaxDecodeCtx = 1 << 21;  // longest decode context (positions)
 constexpr int kMaxAttnCtas = 320;       // persistent attention grid cap (partials are sized for it)
 constexpr int kCoarseBinsHost = 1024;   // coarse histogram bins (host-side copy of the device constant)
+constexpr int kMaxQHeads = 64;          // query heads per token the attention kernels hold (Q slot in shared memory)
 
 struct AttnWs {
   float2* pre_ml;   // prefill with a prefix: [n_q][Hq] prefix part (max in log2 units, sum), else null

@@ -47,7 +47,7 @@ constexpr int kTileRowsMax = 128;                 // 128 / Hkv rows per tile
 constexpr int kRowPad = 16;                       // shared-memory row pitch = Hkv * 256 + 16 (conflict-free ldmatrix)
 constexpr int kPieceMax = 8 * kHeadDim * 2;       // K (or V) bytes of one position, Hkv <= 8
 constexpr int kStageBytes = 2 * kTileRowsMax * (kHeadDim * 2 + kRowPad);  // largest stage (Hkv = 1): 69,632
-constexpr int kMaxHq = 64;
+constexpr int kMaxHq = kMaxQHeads;              // the host refuses more heads (check_heads)
 constexpr int kQBytes = kMaxHq * kHeadDim * 2;    // one query's Q, all heads: 16 KB
 constexpr int kSmemBytes = kStages * kStageBytes + kQBytes + 8 * (2 * kStages + 2) + 16;
 static_assert(kProducerWarps == kStages + 1, "one producer warp per stage, plus the query copier");

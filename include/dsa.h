@@ -185,6 +185,9 @@ dsa_status dsa_kv_gather(const dsa_paged_kv* kv, const dsa_query_set* qs, const 
  * (the gather is fused).  Query head h uses KV head h / (num_q_heads / num_kv_heads).
  * q: bf16 [n_q][num_q_heads][128]; out: [n_q][num_q_heads][128] bf16 (RNE) or f32;
  * lse: f32 [n_q][num_q_heads] natural-log softmax denominator (may be NULL).
+ * Heads: num_q_heads <= 64 (one query's Q, all heads, is staged in a 16 KB
+ * shared-memory slot) and num_q_heads / num_kv_heads <= 16; more return
+ * DSA_ERR_UNSUPPORTED before anything is launched.
  * Decode form (query set = decode of the whole batch): */
 dsa_status dsa_sparse_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t num_q_heads,
                                   const int32_t* idx, const int32_t* n_sel, int32_t k,
@@ -205,7 +208,8 @@ dsa_status dsa_sparse_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* 
 /* ---------------------------------------------------- fused decode step --- */
 /* Steps 1-4 for one decode token per sequence, in one call: scores (written to
  * `scores`, [batch][ld]), top-k (idx, n_sel) and attention (out, lse), with the
- * score histogram built while scoring.  Same argument rules as the single steps. */
+ * score histogram built while scoring.  Same argument rules as the single steps
+ * (num_q_heads <= 64, group <= 16). */
 dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* q_idx,
                            int32_t num_q_heads, int32_t prefix_len, int32_t k,
                            float softmax_scale, int32_t* scores, int32_t ld, int32_t* idx,
@@ -223,9 +227,10 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
  * device array of DSA_TOPK_STATIC_SCRATCH_BYTES inside the library, which every
  * GPU that loads the library keeps until the process exits; the call makes no
  * cudaMalloc, cudaFree or other allocating call.
- *   - Scratch needed: about 4.2 KB per sequence (a 1024-bin histogram, a
- *     counter and the selection window), so up to about 1000 sequences fit;
- *     larger batches return DSA_ERR_UNSUPPORTED before anything is launched.
+ *   - Scratch needed: exactly 4096 bytes per sequence (its 1024-bin coarse
+ *     score histogram, nothing else), so the 4 MiB array serves batches of
+ *     up to 1024 sequences; batch 1025 and above return DSA_ERR_UNSUPPORTED
+ *     before anything is launched (checked on the host).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and sets kernel attributes: make that first call
  *     before any stream capture.

@@ -123,6 +123,22 @@ def test_argument_checks(lib):
                                       1 << 30, None) == INVALID
     assert lib.dsa_sparse_attn_decode(*a, 8, 0x80000, 0x90000, 8, 0, float("nan"), 0xB0000, 0, None,
                                       0xA0000, 1 << 30, None) == INVALID
+    # more than 64 query heads: the attention kernels stage one query's Q (all
+    # heads) in a 64-head shared-memory slot, so the host refuses Hq = 128 even
+    # with a valid group (Hkv = 8, G = 16), on every call that reaches them
+    kv8 = _kv(num_kv_heads=8)
+    assert lib.dsa_sparse_attn_decode(C.byref(kv8), 0x60000, 128, 0x80000, 0x90000, 8, 0, 0.1, 0xB0000, 0, None,
+                                      0xA0000, 1 << 30, None) == UNSUPPORTED
+    assert b"64" in lib.dsa_last_error_message()
+    assert lib.dsa_sparse_attn_prefill(C.byref(kv8), C.byref(_qs(1, 10, 0, 0)), 0x60000, 128, 0x80000, 0x90000, 8,
+                                       0, 0.1, 0xB0000, 0, None, 0xA0000, 1 << 30, None) == UNSUPPORTED
+    assert lib.dsa_decode_step(C.byref(kv8), 0x60000, 0x68000, 128, 0, 8, 0.1, 0x70000, 512, 0x80000, 0x90000,
+                               0xB0000, 0, None, 0xA0000, 1 << 30, None) == UNSUPPORTED
+    assert lib.dsa_workspace_size(3, C.byref(kv8), C.byref(qs), 8, 128, 0) == 0
+    # 64 heads with Hkv = 8 pass the head check (the call then reaches the
+    # workspace check, which a tiny workspace fails)
+    assert lib.dsa_sparse_attn_decode(C.byref(kv8), 0x60000, 64, 0x80000, 0x90000, 8, 0, 0.1, 0xB0000, 0, None,
+                                      0xA0000, 16, None) == WORKSPACE
     # prefill attention refuses a decode query set
     assert lib.dsa_sparse_attn_prefill(C.byref(kv), C.byref(qs), 0x60000, 8, 0x80000, 0x90000, 8, 0, 0.1,
                                        0xB0000, 0, None, None, 0, None) == INVALID
@@ -164,3 +180,20 @@ def test_workspace_sizes(lib):
     without = lib.dsa_workspace_size(4, C.byref(kv4), C.byref(qs4), 2048, 32, 0)
     assert with_prefix - without >= 16384 * 32 * 520
     assert without < 16 << 20                 # no per-query selection state in prefill
+
+
+def test_no_alloc_topk_refuses_batches_beyond_the_static_scratch(lib):
+    """The allocation-free decode top-k keeps exactly 4096 bytes of scratch per
+    sequence in its 4 MiB static array: batch 1024 fits, batch 1025 is refused
+    on the host before anything touches the GPU (fake pointers, no GPU here:
+    an accepted call goes on to the CUDA runtime and reports DSA_ERR_CUDA)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: an accepted call would launch on these fake pointers")
+    fn = lib.dsa_topk_select_decode_noalloc
+    for batch, want in ((1024, CUDA), (1025, UNSUPPORTED), (2048, UNSUPPORTED)):
+        kv = _kv(batch=batch, max_context_len=500)
+        st = fn(C.byref(kv), 0x70000, 512, 64, 64, 0x80000, 0x90000, None)
+        assert st == want, (batch, st, lib.dsa_last_error_message())
+        if want == UNSUPPORTED:
+            assert b"static" in lib.dsa_last_error_message()

@@ -22,7 +22,6 @@ import synth
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-UNSUPPORTED = 2
 
 
 def _scores(spec, seed):
@@ -71,18 +70,3 @@ def test_no_alloc_topk_matches_workspace_version(lib):
         assert torch.equal(n_sel, ref[1])
         assert torch.equal(idx, ref[0])
     assert dsa.check_device_status() == 0
-
-
-def test_no_alloc_topk_rejects_sizes_beyond_the_static_scratch(lib):
-    """A batch whose scratch would not fit is refused before any launch."""
-    import dynamic_sparse_attention_indexer_gb300 as dsa
-    spec = synth.small_spec(lens=(700,), k=64)
-    w, kv, scores = _scores(spec, 3)
-    big = dsa.PagedKV(w["k_cache"], w["v_cache"], w["idx_cache"],
-                      w["block_table"].repeat(2048, 1), w["context_lens"].repeat(2048), 700)
-    assert big.batch == 2048                   # 2048 sequences: about 8.4 MB of scratch
-    scores_big = torch.empty((1, 4), dtype=torch.int32, device=DEV)
-    st = lib.dsa_topk_select_decode_noalloc(C.byref(big.struct), scores_big.data_ptr(), 704, 64, 64,
-                                            scores_big.data_ptr(), scores_big.data_ptr(), None)
-    assert st == UNSUPPORTED
-    assert b"static" in lib.dsa_last_error_message()
