@@ -20,7 +20,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa_gb300.so")
 SOURCES = ["api.cpp", "kv_alloc.cpp", "k_index.cu", "k_topk.cu", "k_attn.cu", "k_misc.cu",
            "k_topk_static.cu", "k_prefix.cu"]
-HEADERS = ["common.cuh", "select.cuh", "internal.h"]
+HEADERS = ["common.cuh", "select.cuh", "internal.h", "attn_tile.cuh", "score_walk.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -32,6 +32,7 @@
 // one CTA is written out directly; a query cut by range boundaries leaves one
 // partial (max, sum, unnormalised O) per CTA, and attn_combine_kernel,
 // launched right behind (programmatic dependent launch), merges them.
+#include "attn_tile.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -206,16 +207,6 @@ __device__ __forceinline__ void write_out(const AttnParams& p, size_t head, int 
     reinterpret_cast<__nv_bfloat16*>(p.out)[head * kHeadDim + d] = __float2bfloat16_rn(v);
   else
     reinterpret_cast<float*>(p.out)[head * kHeadDim + d] = v;
-}
-
-// The two bf16 halves of a packed pair, as floats (exact).
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
-
-__device__ __forceinline__ uint32_t transpose8x8(uint32_t v) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(v));
-  return d;
 }
 
 // NT: 8-head column tiles of a KV group (1 for G <= 8, 2 for G <= 16).
@@ -441,12 +432,8 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
   // ------------------------------------------------------------ consumers
   const int g = warp - kProducerWarps;  // KV head
   if (g >= p.hkv) return;
-  const int pitch = p.pitch;
-  const int mi = lane >> 3, rr8 = lane & 7;
   const int hc = 2 * (lane & 3);  // first head column of this lane in an 8-head tile
-  uint32_t qb[NT][8][2];
-  float o[8][NT][4];
-  float m[NT][2], l[NT][2];
+  HeadState<NT> hs;
   Cursor cur;
   cursor_init(cur, p);
   Tile t;
@@ -467,24 +454,10 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         }
         ++seg;
       }
-      // Q fragments of this group's heads (heads past G repeat head G - 1; their
-      // columns are never written out).
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const int h = g * G + min(j * 8 + rr8, G - 1);
-#pragma unroll
-        for (int ks = 0; ks < 8; ks += 2)
-          ldsm_x4(smem_u32(s_q + h * (kHeadDim * 2) + (2 * ks + mi) * 16), qb[j][ks][0], qb[j][ks][1],
-                  qb[j][ks + 1][0], qb[j][ks + 1][1]);
-      }
+      load_q(hs, s_q, g, G, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(q_empty);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < NT; ++j) o[i][j][0] = o[i][j][1] = o[i][j][2] = o[i][j][3] = 0.f;
-#pragma unroll
-      for (int j = 0; j < NT; ++j) m[j][0] = m[j][1] = -INFINITY, l[j][0] = l[j][1] = 0.f;
+      reset_state(hs);
       if (p.pre_ml && (t.flags & kHead)) {
         // The query's prefix part is the starting state of the segment that
         // begins the query (its sum sits in one row group of lanes).
@@ -496,113 +469,24 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
             if (h >= G) continue;
             const size_t head = (size_t)t.qf.qi * p.hq + (size_t)g * G + h;
             const float2 ml = __ldg(p.pre_ml + head);
-            m[j][e] = ml.x;
-            l[j][e] = (lane >> 2) == 0 ? ml.y : 0.f;
+            hs.m[j][e] = ml.x;
+            hs.l[j][e] = (lane >> 2) == 0 ? ml.y : 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int d = 16 * i + (lane >> 2);
-              o[i][j][e] = __ldg(p.pre_o + head * kHeadDim + d);
-              o[i][j][e + 2] = __ldg(p.pre_o + head * kHeadDim + d + 8);
+              hs.o[i][j][e] = __ldg(p.pre_o + head * kHeadDim + d);
+              hs.o[i][j][e + 2] = __ldg(p.pre_o + head * kHeadDim + d + 8);
             }
           }
       }
     }
     const uint8_t* sk = smem + s * kStageBytes + g * (kHeadDim * 2);
-    const uint8_t* sv = sk + p.rows * pitch;
-    for (int c16 = 0; c16 < t.nvalid; c16 += 16) {
-      // S^T = K Q^T: 16 rows x 8 NT heads.
-      float sacc[NT][4];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(smem_u32(sk + (c16 + (mi & 1) * 8 + rr8) * pitch + (2 * ks + (mi >> 1)) * 16), a0, a1, a2, a3);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) mma_bf16_16816(sacc[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
-      }
-      // Online softmax per head column (base 2), reduced over the 8 row groups.
-      const int ra = c16 + (lane >> 2);  // tile rows of elements 0,1 (ra) and 2,3 (ra + 8)
-      const bool va = ra < t.nvalid, vb = ra + 8 < t.nvalid;
-      float alpha[NT][2], ms[NT][2];
-      bool moved = false;
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        sacc[j][0] = va ? sacc[j][0] * p.scale_log2 : -INFINITY;
-        sacc[j][1] = va ? sacc[j][1] * p.scale_log2 : -INFINITY;
-        sacc[j][2] = vb ? sacc[j][2] * p.scale_log2 : -INFINITY;
-        sacc[j][3] = vb ? sacc[j][3] * p.scale_log2 : -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float mx = fmaxf(sacc[j][e], sacc[j][e + 2]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m[j][e], mx);
-          ms[j][e] = mn == -INFINITY ? 0.f : mn;
-          alpha[j][e] = exp2f(m[j][e] - ms[j][e]);
-          moved |= mn != m[j][e];
-          m[j][e] = mn;
-        }
-      }
-      if (__any_sync(0xffffffffu, moved)) {  // rescale only when a running max moved
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            o[i][j][0] *= alpha[j][0];
-            o[i][j][1] *= alpha[j][1];
-            o[i][j][2] *= alpha[j][0];
-            o[i][j][3] *= alpha[j][1];
-          }
-#pragma unroll
-        for (int j = 0; j < NT; ++j) l[j][0] *= alpha[j][0], l[j][1] *= alpha[j][1];
-      }
-      // P in two bf16 terms, P = hi + lo (lo = the rounding residual of hi), so
-      // the P.V product carries about 16 mantissa bits of P instead of 8.
-      uint32_t pb[NT][2], pl[NT][2];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const float p0 = exp2f(sacc[j][0] - ms[j][0]), p1 = exp2f(sacc[j][1] - ms[j][1]);
-        const float p2 = exp2f(sacc[j][2] - ms[j][0]), p3 = exp2f(sacc[j][3] - ms[j][1]);
-        l[j][0] += p0 + p2;
-        l[j][1] += p1 + p3;
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-        const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-        // P^T rows (attended rows) x head columns -> B fragments (rows as K).
-        pb[j][0] = transpose8x8(h01);
-        pb[j][1] = transpose8x8(h23);
-        pl[j][0] = transpose8x8(r01);
-        pl[j][1] = transpose8x8(r23);
-      }
-      // O^T += V^T P^T: d in 8 tiles of 16.
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(smem_u32(sv + (c16 + (mi >> 1) * 8 + rr8) * pitch + (2 * i + (mi & 1)) * 16), a0, a1, a2, a3);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          mma_bf16_16816(o[i][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
-          mma_bf16_16816(o[i][j], a0, a1, a2, a3, pl[j][0], pl[j][1]);
-        }
-      }
-    }
+    attend_rows(hs, sk, sk + p.rows * p.pitch, p.pitch, t.nvalid, p.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
 
     if (t.flags & kLast) {
-      // The segment ends: total weight per head column over the row groups.
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float v = l[j][e];
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          v += __shfl_xor_sync(0xffffffffu, v, 8);
-          v += __shfl_xor_sync(0xffffffffu, v, 16);
-          l[j][e] = v;
-        }
+      total_sums(hs);
       const size_t head0 = (size_t)t.qf.qi * p.hq + (size_t)g * G;
       const size_t sl = (size_t)blockIdx.x * 2 + t.slot;
 #pragma unroll
@@ -612,23 +496,17 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
           const int h = j * 8 + hc + e;
           if (h >= G) continue;
           if (t.flags & kWhole) {
-            const float r = 1.f / l[j][e];
+            const float r = 1.f / hs.l[j][e];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int d = 16 * i + (lane >> 2);
-              write_out(p, head0 + h, d, o[i][j][e] * r);
-              write_out(p, head0 + h, d + 8, o[i][j][e + 2] * r);
+              write_out(p, head0 + h, d, hs.o[i][j][e] * r);
+              write_out(p, head0 + h, d + 8, hs.o[i][j][e + 2] * r);
             }
-            if (lane < 4 && p.lse) p.lse[head0 + h] = (m[j][e] + log2f(l[j][e])) * 0.69314718055994531f;
+            if (lane < 4 && p.lse) p.lse[head0 + h] = (hs.m[j][e] + log2f(hs.l[j][e])) * 0.69314718055994531f;
           } else {
             const size_t ph = sl * p.hq + (size_t)g * G + h;
-            if (lane < 4) p.part_ml[ph] = make_float2(m[j][e], l[j][e]);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int d = 16 * i + (lane >> 2);
-              p.part_o[ph * kHeadDim + d] = o[i][j][e];
-              p.part_o[ph * kHeadDim + d + 8] = o[i][j][e + 2];
-            }
+            store_partial(hs, j, e, lane, p.part_ml + ph, p.part_o + ph * kHeadDim);
           }
         }
     }

@@ -14,6 +14,7 @@
 // tiles skipped.
 #include "common.cuh"
 #include "internal.h"
+#include "score_walk.cuh"
 
 namespace dsa {
 namespace {
@@ -37,7 +38,6 @@ constexpr int kIdxConsumers = 8;                               // consumer warps
 constexpr int kIdxThreads = 32 * (1 + kIdxConsumers);          // 288
 constexpr int kIdxStages = 8;          // ring stages; 6 where the selection CTAs are to fit beside
 constexpr int kIdxStagesShared = 6;    // a scoring CTA (they are then resident before it ends)
-constexpr int kGroupBlocks = 4;                                // cache blocks per stage
 constexpr int kIdxBlockBytes = kBlock * kIdxDim;               // 4096
 constexpr int kIdxStageBytes = kGroupBlocks * kIdxBlockBytes;  // 16 KB
 constexpr int kMaxRange = 2048;                                // candidate blocks per CTA at most
@@ -57,46 +57,6 @@ struct DecodeIndexParams {
   int* coarse;  // [B][kCoarseBins] global histograms, or nullptr
   int ld, max_blocks, num_blocks, prefix, max_ctx, batch, k;
 };
-
-// Candidate blocks of every sequence and their prefix sums: seg_start[b] is the
-// first flattened block of sequence b, seg_start[batch] the total.
-__device__ void candidate_blocks(const int32_t* __restrict__ ctx, int batch, int max_ctx, int prefix,
-                                 int* seg_start, int* len, int* scratch) {
-  int carry = 0;
-  for (int base = 0; base < batch; base += blockDim.x) {
-    const int b = base + threadIdx.x;
-    int nb = 0;
-    if (b < batch) {
-      const int L = min(__ldg(ctx + b), max_ctx);
-      len[b] = L;
-      nb = L > prefix ? (L + kBlock - 1) / kBlock - prefix / kBlock : 0;
-    }
-    int tot;
-    const int ex = block_exclusive_scan(nb, scratch, &tot);
-    if (b < batch) seg_start[b] = carry + ex;
-    carry += tot;
-  }
-  if (threadIdx.x == 0) seg_start[batch] = carry;
-  __syncthreads();
-}
-
-// The group sequence of a CTA range: groups of up to kGroupBlocks consecutive
-// candidate blocks of one sequence.
-struct GroupCursor {
-  int f, f_end, b;
-};
-struct Group {
-  int b, jb, count;  // sequence, block-table index of the first block, blocks
-};
-__device__ __forceinline__ bool next_group(GroupCursor& c, const int* seg_start, int jb_base, Group* g) {
-  if (c.f >= c.f_end) return false;
-  while (seg_start[c.b + 1] <= c.f) ++c.b;  // skip sequences without candidates
-  g->b = c.b;
-  g->jb = c.f - seg_start[c.b] + jb_base;
-  g->count = min(kGroupBlocks, min(c.f_end, seg_start[c.b + 1]) - c.f);
-  c.f += g->count;
-  return true;
-}
 
 // Sums the consumer warps' histograms of one sequence into its global one
 // (called by all consumer threads, ct = 0 .. 255); with `clear` the warp

@@ -19,42 +19,6 @@ namespace {
 
 __device__ int g_status;
 
-// Highest bin b with sum(bins >= b) >= k among nb (256 or 1024) bins in shared
-// memory, and the count above it; one warp.  *bin = -1 when the total is below k.
-__device__ __forceinline__ void warp_hist_threshold(const int* h, int nb, int k, int lane, int* bin, int* above) {
-  const int gs = nb / 32;  // bins per lane group (8 or 32)
-  // Four independent sums over the group's bins, read in a lane-rotated order
-  // (no bank conflicts).
-  int s4[4] = {0, 0, 0, 0};
-  for (int i = 0; i < gs; i += 4)
-#pragma unroll
-    for (int u = 0; u < 4; ++u) s4[u] += h[gs * lane + ((i + u + lane) & (gs - 1))];
-  int suf = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_down_sync(0xffffffffu, suf, o);
-    if (lane + o < 32) suf += y;
-  }
-  const uint32_t reach = __ballot_sync(0xffffffffu, suf >= k);
-  if (!reach) {
-    *bin = -1;
-    *above = 0;
-    return;
-  }
-  const int ls = 31 - __clz(reach);
-  const int above_grp = ls < 31 ? __shfl_sync(0xffffffffu, suf, ls + 1) : 0;
-  int suf2 = lane < gs ? h[gs * ls + lane] : 0;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_down_sync(0xffffffffu, suf2, o);
-    if (lane + o < 32) suf2 += y;
-  }
-  const uint32_t reach2 = __ballot_sync(0xffffffffu, lane < gs && above_grp + suf2 >= k);
-  const int b = 31 - __clz(reach2);
-  *bin = gs * ls + b;
-  *above = above_grp + (b < 31 ? __shfl_sync(0xffffffffu, suf2, b + 1) : 0);
-}
-
 // Decode selection: one thread-block cluster of C CTAs per sequence (C = 1 ..
 // 16, chosen from the longest context so that a CTA reads about one round of
 // 8192 scores).  CTA rank r owns the r-th of C equal parts of the candidates
