@@ -11,8 +11,10 @@ Inputs are synthetic and seeded; they are resident in HBM before timing.
 Consecutive steps rotate over 4 independent KV caches ("layers", 17.6 GB in
 all), so no step finds its data in the 129 MB L2.  Multi-GPU runs (torchrun)
 give every rank its own batch (weak scaling, no collective on the data path).
-The reference arm (--impl reference) times the CPU oracle on a bounded sample
-of the same workload.
+The same line also carries the 16K prefill chunk (scores, top-k, attention,
+timed per call) with the peak rates it is compared against, measured in the
+same run by the microbenchmarks of libdsa_probe.so.  The reference arm
+(--impl reference) times the CPU oracle on a bounded sample of the workload.
 """
 from __future__ import annotations
 
@@ -31,6 +33,7 @@ for _p in (ROOT, os.path.join(ROOT, "tests")):
         sys.path.insert(0, _p)
 
 CONFIG_ID = 3
+PREFILL_ID = 4
 LAYERS = 4
 METRIC = "DSA decode tokens/s & achieved HBM GB/s (% of roofline) at 128K ctx, 1xGB300"
 
@@ -114,21 +117,20 @@ def code_digest(path):
 
 
 def profiled_attention_traffic():
-    """DRAM bytes per attention call from the committed ncu summary, or None
-    once the attention code has changed since the counters were taken."""
-    import re
-    path = os.path.join(ROOT, "profiles", "decode_128k_kernels_full.md")
+    """DRAM bytes per attention call from the committed ncu record
+    (profiles/decode_128k_traffic.json), or None once the attention code has
+    changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "decode_128k_traffic.json")
     src = os.path.join(ROOT, "dynamic_sparse_attention_indexer_gb300", "csrc", "k_attn.cu")
     try:
-        text = open(path).read()
+        with open(path) as f:
+            rec = json.load(f)
         digest = code_digest(src)
-    except OSError:
+    except (OSError, ValueError):
         return None
-    m_sha = re.search(r"code_sha256\(k_attn\.cu\): ([0-9a-f]{64})", text)
-    m_bytes = re.search(r"traffic_bytes_per_call: (\d+)", text)
-    if not (m_sha and m_bytes) or m_sha.group(1) != digest:
+    if rec.get("code_sha256_k_attn") != digest:
         return None
-    return int(m_bytes.group(1))
+    return int(rec["traffic_bytes_per_call"])
 
 
 def reduce_over_ranks(values: dict, op: str):
@@ -181,6 +183,216 @@ def cpu_threads_used():
     # numpy's BLAS is limited to one thread before numpy loads (see main); the
     # int64 scoring and the sort are single threaded in numpy anyway.
     return 1
+
+
+def _export_sequence(w, b, d, tag):
+    """Sequence b's oracle inputs as .npy files in directory d (not timed):
+    query, indexer query, indexer blocks (int8), K and V blocks (bf16 bits)."""
+    import numpy as np
+    import torch
+    L = int(w["context_lens"][b].item())
+    nblk = math.ceil(L / 64)
+    ids = w["block_table"][b, :nblk].long()
+    paths = {}
+    arrays = {"q": w["q"][b].cpu().to(torch.float64).numpy(),
+              "q_idx": w["q_idx"][b].cpu().numpy().astype(np.int64),
+              "idx_cache": w["idx_cache"].index_select(0, ids).cpu().numpy(),
+              "k16": w["k_cache"].index_select(0, ids).view(torch.int16).cpu().numpy().view(np.uint16),
+              "v16": w["v_cache"].index_select(0, ids).view(torch.int16).cpu().numpy().view(np.uint16)}
+    for name, arr in arrays.items():
+        paths[name] = os.path.join(d, f"{tag}_{name}.npy")
+        np.save(paths[name], arr)
+    paths["pos"] = L - 1
+    paths["nblk"] = nblk
+    return paths
+
+
+def _oracle_worker(task):
+    """One host process: loads one sequence's inputs, waits for the common
+    start time, then runs the oracle on that decode token repeatedly for
+    `seconds`.  Returns (tokens, seconds)."""
+    import numpy as np
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import oracle.dsa_oracle as O
+    paths, prefix, k, hkv, start_at, seconds = task
+    q = np.load(paths["q"])
+    q_idx = np.load(paths["q_idx"])
+    idx = np.load(paths["idx_cache"], mmap_mode="r")
+    kc = (np.load(paths["k16"]).astype(np.uint32) << 16).view(np.float32)   # bf16 -> fp32, exact
+    vc = (np.load(paths["v16"]).astype(np.uint32) << 16).view(np.float32)
+    bt = np.arange(paths["nblk"], dtype=np.int64)
+    while time.time() < start_at:
+        time.sleep(0.005)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        O.dsa_query(q, q_idx, kc, vc, idx, bt, paths["pos"], prefix, k, hkv, 1.0 / math.sqrt(128))
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return n, el
+
+
+def cpu_baseline_all_cores(w, spec, seconds, n_seq=4):
+    """The oracle as it stands on every host core at once: one process per
+    core (spawned), each repeating one decode token of the workload (the
+    sequences taken in turn).  Throughput = sum of the per-process rates over
+    the same time window."""
+    import multiprocessing as mp
+    import shutil
+    import tempfile
+    base = "/dev/shm" if os.path.isdir("/dev/shm") else None
+    d = tempfile.mkdtemp(prefix="dsa_oracle_", dir=base)
+    try:
+        seqs = [_export_sequence(w, b, d, f"s{b}") for b in range(min(n_seq, spec.batch))]
+        cores = os.cpu_count() or 1
+        start_at = time.time() + 4.0 + 0.2 * cores  # after every process has loaded its inputs
+        tasks = [(seqs[i % len(seqs)], spec.prefix_len, spec.k, spec.num_kv_heads, start_at, seconds)
+                 for i in range(cores)]
+        with mp.get_context("spawn").Pool(cores) as pool:
+            res = pool.map(_oracle_worker, tasks)
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+    tokens = sum(n for n, _ in res)
+    rate = sum(n / el for n, el in res)
+    return {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes, one per host core, each repeating one decode token of the workload "
+                      f"({len(seqs)} sequences in turn) for {seconds:.0f} s: {tokens} tokens"}
+
+
+class Probes:
+    """Peak-rate microbenchmarks (libdsa_probe.so), timed with CUDA events on
+    the current stream."""
+
+    def __init__(self, dev):
+        import ctypes as C
+        import torch
+        from dynamic_sparse_attention_indexer_gb300 import _build
+        _build.ensure_built()
+        lib = C.CDLL(_build.PROBE_LIB)
+        for fn in ("probe_mma_s8", "probe_mma_bf16"):
+            getattr(lib, fn).restype = C.c_float
+            getattr(lib, fn).argtypes = [C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        lib.probe_gather.restype = C.c_float
+        lib.probe_gather.argtypes = [C.c_void_p, C.c_ulonglong, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                     C.c_void_p]
+        self.lib, self.dev = lib, dev
+        self.sink = torch.zeros(4, dtype=torch.int32, device=dev)
+        self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def _stream(self):
+        import ctypes as C
+        import torch
+        return C.c_void_p(torch.cuda.current_stream(self.dev).cuda_stream)
+
+    def mma_tops(self, kind):
+        """Best of 5: int8 TOPS (kind "s8", m16n8k32) or bf16 TFLOP/s ("bf16", m16n8k16) of mma.sync."""
+        fn, ops = (self.lib.probe_mma_s8, 8192) if kind == "s8" else (self.lib.probe_mma_bf16, 4096)
+        ctas, iters = 4 * self.sms, 20000
+        fn(ctas, 200, self.sink.data_ptr(), self._stream())
+        best = min(fn(ctas, iters, self.sink.data_ptr(), self._stream()) for _ in range(5))
+        return ctas * 8 * iters * 8 * ops / (best * 1e-3) / 1e12
+
+    def gather_gbs(self, piece, region_bytes=32 << 20):
+        """Best of 5: GB/s of random `piece`-byte bulk copies into shared memory
+        from a buffer of region_bytes (L2-resident), four issuing warps and
+        three 64 KB stages per SM."""
+        import torch
+        buf = torch.ones(region_bytes // 4, dtype=torch.int32, device=self.dev)
+        n_pieces = region_bytes // piece
+        iters = 400
+        args = (buf.data_ptr(), n_pieces, piece, 3, self.sms, iters, self.sink.data_ptr(), self._stream())
+        self.lib.probe_gather(*args)
+        best = min(self.lib.probe_gather(*args) for _ in range(5))
+        assert int(self.sink.sum().item()) == 0, "gather probe wait ran out"
+        return self.sms * iters * 65536 / (best * 1e-3) / 1e9
+
+
+def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
+    """The 16K prefill chunk (T = 16384 causal queries against the same 16384
+    positions, 32/4 heads, prefix 576, k = 2048): scores, top-k and attention,
+    each call timed with CUDA events on the stream it runs on, with clocks
+    sampled during the timed calls; the peaks it is compared against, measured
+    now; and the oracle on sampled query rows (one host thread)."""
+    import numpy as np
+    import torch
+    import dynamic_sparse_attention_indexer_gb300 as dsa
+    import harness as H
+    import synth
+    spec = synth.CONFIGS[PREFILL_ID]
+    w = synth.make_workload(spec, 1000 + PREFILL_ID, dev)
+    kv = H.paged_kv(w)
+    T, k, P, hq, hkv = spec.num_queries, spec.k, spec.prefix_len, spec.num_q_heads, spec.num_kv_heads
+    qs = dsa.query_set(dsa.MODE_PREFILL, T, 0, 0)
+    ld = H.round4(T)
+    scores = torch.zeros((T, ld), dtype=torch.int32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(T, dtype=torch.int32, device=dev)
+    out = torch.empty((T, hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, hq), dtype=torch.float32, device=dev)
+    ws = dsa.make_workspace(dsa.workspace_size(dsa.OP_PREFILL_STEP, kv, qs, k, hq, P), dev)
+    calls = {"index": lambda: dsa.index_scores(kv, qs, w["q_idx"], P, scores),
+             "topk": lambda: dsa.topk_select(kv, qs, scores, P, k, idx, n_sel, ws),
+             "attention": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws)}
+    st = torch.cuda.current_stream(dev)
+    for _ in range(max(1, warmup)):
+        for f in calls.values():
+            f()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.3)
+    ms = {}
+    for name, f in calls.items():
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(steps):
+            f()
+        b.record(st)
+        b.synchronize()
+        ms[name] = a.elapsed_time(b) / steps
+    clock_info = clocks.stop()
+    assert dsa.check_device_status(dev) == 0
+    total = sum(ms.values())
+    pos = np.arange(T)
+    causal_pairs = int(np.maximum(0, pos + 1 - P).sum())          # scored (query, key) pairs
+    n_sel_h = n_sel.cpu().numpy().astype(np.int64)
+    gathered = int(n_sel_h.sum()) * hkv * 2 * 128 * 2                # selected K and V rows, every KV head
+    s8 = probes.mma_tops("s8")
+    bf16 = probes.mma_tops("bf16")
+    gather = probes.gather_gbs(hkv * 128 * 2)
+    idx_tops = 2 * 64 * causal_pairs / (ms["index"] * 1e-3) / 1e12
+    attn_gbs = gathered / (ms["attention"] * 1e-3) / 1e9
+    # oracle on sampled rows of the chunk (rows drawn uniformly, seeded)
+    cpu = None
+    if cpu_seconds > 0:
+        import oracle.dsa_oracle as O
+        wn = synth.to_numpy(w)
+        rows = np.random.default_rng(4).integers(0, T, size=4096)
+        n, t0 = 0, time.perf_counter()
+        while n < len(rows) and (n < 4 or time.perf_counter() - t0 < cpu_seconds):
+            O.prefill_query(wn, int(rows[n]))
+            n += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": n / el, "unit": "query rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} query rows of the chunk drawn uniformly at random (seed 4), full oracle per row, "
+                         f"{el:.1f} s"}
+    return {
+        "workload": spec.name, "queries": T, "ms": {**ms, "total": total}, "tokens_per_s": T / (total * 1e-3),
+        "indexer": {"kernel": "prefill_index_kernel (mma.sync m16n8k32 s8)", "bound": "tensor",
+                    "achieved": idx_tops, "peak": s8, "unit": "int8 TOPS", "frac": idx_tops / s8,
+                    "ops": 2 * 64 * causal_pairs,
+                    "peak_kind": "measured in this run: mma.sync m16n8k32 s8 microbenchmark (libdsa_probe.so)"},
+        "attention": {"kernel": "dsa_sparse_attn_prefill per call: prefix_attn_kernel + sparse_attn_kernel + "
+                                "attn_combine_kernel", "bound": "l2",
+                      "achieved": attn_gbs, "peak": gather, "unit": "GB/s", "frac": attn_gbs / gather,
+                      "bytes": gathered,
+                      "peak_kind": f"measured in this run: random {hkv * 256}-byte bulk copies from an L2-resident "
+                                   f"32 MB buffer into shared memory (libdsa_probe.so)"},
+        "mma_bf16_peak_tflops": bf16,
+        "clocks": clock_info,
+        "cpu_baseline": cpu,
+    }
 
 
 # --------------------------------------------------------------- arms ------
@@ -377,24 +589,57 @@ def run_gpu(args, rank, world, local_rank):
     h2d = q_host[0].numel() * 2 + qi_host[0].numel()
     d2h = out_host.numel() * 2 + lse_host.numel() * 4
 
+    # The same sequence without a graph: every step the Python API call
+    # (argument checks and launches through the C ABI), the host-to-device
+    # copies of the step's queries from pinned memory before it and the
+    # device-to-host copies of its output after it, then the host waits.
+    def e2e_api_step(i):
+        w, kv, b, ws = layers[i % LAYERS]
+        w["q"].copy_(q_host[i % LAYERS], non_blocking=True)
+        w["q_idx"].copy_(qi_host[i % LAYERS], non_blocking=True)
+        step(i % LAYERS)
+        out_host.copy_(b["out"], non_blocking=True)
+        lse_host.copy_(b["lse"], non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            e2e_api_step(i)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            e2e_api_step(i)
+        e2e_api_s = time.perf_counter() - t0
+    assert dsa.check_device_status(dev) == 0
+
     # --- aggregate over ranks (max time, summed tokens)
-    agg = reduce_over_ranks({"ms": local_ms, "e2e_s": e2e_s, "attn_ms": attn_ms, "index_ms": index_ms}, "max")
+    agg = reduce_over_ranks({"ms": local_ms, "e2e_s": e2e_s, "e2e_api_s": e2e_api_s, "attn_ms": attn_ms,
+                             "index_ms": index_ms}, "max")
     tokens = reduce_over_ranks({"tok": float(B * args.steps), "e2e_tok": float(B * n_e2e)}, "sum")
 
-    # --- CPU baseline (rank 0, N = 1 only): the oracle on a bounded sample
+    # --- prefill chunk and its peaks (rank 0)
+    prefill = None
+    if rank == 0 and not args.no_prefill:
+        del layers[1:]
+        torch.cuda.empty_cache()
+        prefill = measure_prefill(dev, args.prefill_steps, 3, Probes(dev),
+                                  0.0 if args.no_cpu_baseline or world > 1 else args.cpu_seconds / 2)
+
+    # --- CPU baseline (rank 0, N = 1 only): the oracle on a bounded sample,
+    # on every host core at once, and on one thread
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_all_cores(w0, spec, args.cpu_seconds)
         n_seq = min(args.cpu_sample, B)
         inputs = [oracle_sequence_inputs(w0, b) for b in range(n_seq)]
-        # Repeat the sample until about args.cpu_seconds of CPU work (bounded).
         secs, passes = 0.0, 0
-        while passes < 1 or (secs < args.cpu_seconds and passes < 200):
+        while passes < 1 or (secs < args.cpu_seconds / 2 and passes < 200):
             secs += time_oracle(inputs, spec)
             passes += 1
         n_tok = n_seq * passes
-        cpu = {"value": n_tok / secs, "unit": "tokens/s", "cores": cpu_threads_used(), "kind": "oracle",
-               "sample": f"{n_seq} of the {B} decode tokens of one step (full oracle per token), "
-                         f"{passes} passes: {n_tok} tokens in {secs:.1f} s"}
+        cpu["one_thread"] = {"value": n_tok / secs, "unit": "tokens/s", "cores": cpu_threads_used(),
+                             "sample": f"{n_seq} of the {B} decode tokens of one step (full oracle per token), "
+                                       f"{passes} passes: {n_tok} tokens in {secs:.1f} s"}
 
     if rank != 0:
         return
@@ -420,60 +665,31 @@ def run_gpu(args, rank, world, local_rank):
         "indexer": {"ms": agg["index_ms"], "achieved_gbs": ab["indexer"] / (agg["index_ms"] * 1e-3) / 1e9},
         "clocks": clock_info,
         "e2e": {"value": tokens["e2e_tok"] / agg["e2e_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "how": "graph replay: per step one captured graph of the host-to-device query copies, the "
+                       "decode step and the device-to-host output copies; the host waits for each step"},
+        "e2e_api": {"value": tokens["e2e_tok"] / agg["e2e_api_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "how": "no graph: per step the copies and the Python API call through the C ABI (host "
+                           "argument checks and kernel launches included); the host waits for each step"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
 
 
 def run_prefill(args):
-    """The prefill path of the 16K workload (T = 16384 causal queries, 32/4
-    heads, prefix 576, k = 2048): scores, top-k and attention timed per call
-    with CUDA events on the stream they run on (not the decode headline)."""
+    """Only the 16K prefill chunk (one GPU), printed as its own JSON line: a
+    small command for profiling the prefill kernels."""
     import torch
-    import dynamic_sparse_attention_indexer_gb300 as dsa
-    import harness as H
-    import synth
-    spec = synth.CONFIGS[4]
-    w = synth.make_workload(spec, 1004, "cuda")
-    kv = H.paged_kv(w)
-    T, k, P, hq = spec.num_queries, spec.k, spec.prefix_len, spec.num_q_heads
-    qs = dsa.query_set(dsa.MODE_PREFILL, T, 0, 0)
-    ld = H.round4(T)
-    scores = torch.zeros((T, ld), dtype=torch.int32, device="cuda")
-    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
-    n_sel = torch.empty(T, dtype=torch.int32, device="cuda")
-    out = torch.empty((T, hq, 128), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((T, hq), dtype=torch.float32, device="cuda")
-    ws = dsa.make_workspace(dsa.workspace_size(dsa.OP_PREFILL_STEP, kv, qs, k, hq, P), "cuda")
-    calls = {"index": lambda: dsa.index_scores(kv, qs, w["q_idx"], P, scores),
-             "topk": lambda: dsa.topk_select(kv, qs, scores, P, k, idx, n_sel, ws),
-             "attention": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws)}
-    st = torch.cuda.current_stream()
-    for _ in range(max(1, args.warmup)):
-        for f in calls.values():
-            f()
-    torch.cuda.synchronize()
-    ms = {}
-    for name, f in calls.items():
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(st)
-        for _ in range(args.steps):
-            f()
-        b.record(st)
-        b.synchronize()
-        ms[name] = a.elapsed_time(b) / args.steps
-    assert dsa.check_device_status() == 0
-    total = sum(ms.values())
-    causal_pairs = sum(max(0, t + 1 - P) for t in range(T))  # scored (query, key) pairs
-    print(json.dumps({"metric": "DSA prefill tokens/s, 16K causal chunk, 1xGB300", "value": T / (total * 1e-3),
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    res = measure_prefill(dev, args.steps, args.warmup, Probes(dev), 0.0)
+    print(json.dumps({"metric": "DSA prefill tokens/s, 16K causal chunk, 1xGB300", "value": res["tokens_per_s"],
                       "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-                      "ms_per_step": total, "higher_is_better": True, "dtype": "bf16 / int8 indexer",
-                      "data": "synthetic", "config": {"workload": spec.name, "queries": T, "prefix": P,
-                                                      "q_heads": hq, "kv_heads": spec.num_kv_heads, "top_k": k},
-                      "ms": ms, "indexer_tops": 2 * 64 * causal_pairs / (ms["index"] * 1e-3) / 1e12}),
-          flush=True)
+                      "ms_per_step": res["ms"]["total"], "higher_is_better": True, "dtype": "bf16 / int8 indexer",
+                      "data": "synthetic", "config": {"workload": res["workload"]}, "prefill": res}), flush=True)
 
 
 def main():
@@ -486,8 +702,10 @@ def main():
                     help="time the 16K prefill path instead of the decode headline (one GPU)")
     ap.add_argument("--cpu-sample", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="repeat the CPU baseline's sample until about this much oracle time")
+                    help="oracle time of the all-cores CPU baseline (the one-thread and prefill ones take half)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="leave the prefill chunk out of the headline line")
+    ap.add_argument("--prefill-steps", type=int, default=5, help="timed calls of each prefill step")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="independent caches the steps rotate over (4 keeps every step out of L2; "
                          "1 gives a small case for ncu captures)")

@@ -1,7 +1,9 @@
-"""In-tree build of the C-ABI library ``libdsa_gb300.so`` for sm_103a.
+"""In-tree build of the C-ABI library ``libdsa_gb300.so`` for sm_103a, and of
+``libdsa_probe.so`` (the peak-rate microbenchmarks the measurement reports its
+roofline fractions against; not part of the dsa_* interface).
 
 Each source is compiled by nvcc in parallel into ``_build/``, then linked
-into a shared library beside this file.  A stamp of the sources, flags and
+into the shared libraries beside this file.  A stamp of the sources, flags and
 machine skips the build when nothing changed.
 """
 from __future__ import annotations
@@ -18,6 +20,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa_gb300.so")
+PROBE_LIB = os.path.join(PKG, "libdsa_probe.so")
+PROBE_SOURCES = ["probe_peaks.cu"]
 SOURCES = ["api.cpp", "kv_alloc.cpp", "k_index.cu", "k_topk.cu", "k_attn.cu", "k_misc.cu",
            "k_topk_static.cu", "k_prefix.cu"]
 HEADERS = ["common.cuh", "select.cuh", "internal.h", "attn_tile.cuh", "score_walk.cuh"]
@@ -35,7 +39,7 @@ def _nvcc() -> str:
 
 def _stamp() -> str:
     h = hashlib.sha256()
-    for name in SOURCES + HEADERS:
+    for name in SOURCES + PROBE_SOURCES + HEADERS:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     with open(os.path.join(ROOT, "include", "dsa.h"), "rb") as f:
@@ -45,12 +49,12 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
-def _lib_matches_machine() -> bool:
+def _lib_matches_machine(path: str = LIB) -> bool:
     """The library exists and was linked for this machine (the tree may have
     been copied from a host of another architecture)."""
-    if not os.path.exists(LIB):
+    if not os.path.exists(path):
         return False
-    with open(LIB, "rb") as f:
+    with open(path, "rb") as f:
         head = f.read(20)
     if head[:4] != b"\x7fELF":
         return False
@@ -61,7 +65,7 @@ def _lib_matches_machine() -> bool:
 
 def is_current() -> bool:
     stamp_file = os.path.join(OUT_DIR, "stamp")
-    if not _lib_matches_machine() or not os.path.exists(stamp_file):
+    if not _lib_matches_machine() or not _lib_matches_machine(PROBE_LIB) or not os.path.exists(stamp_file):
         return False
     with open(stamp_file) as f:
         return f.read().strip() == _stamp()
@@ -83,18 +87,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed on {name}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stdout + r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + len(PROBE_SOURCES)) as ex:
+        results = dict(zip(SOURCES + PROBE_SOURCES, ex.map(compile_one, SOURCES + PROBE_SOURCES)))
     if verbose:
-        for _, log in results:
+        for _, log in results.values():
             if log.strip():
                 print(log)
-    tmp = LIB + ".tmp"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    for lib, names in ((LIB, SOURCES), (PROBE_LIB, PROBE_SOURCES)):
+        tmp = lib + ".tmp"
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [results[n][0] for n in names]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     with open(os.path.join(OUT_DIR, "stamp"), "w") as f:
         f.write(_stamp())
     return LIB

@@ -124,6 +124,26 @@ def oracle_decode_sampled(w: dict, b: int, heads_kv, k: int, P: int):
     return {"scores": s, "idx": idx, "n_sel": n_sel, "heads": heads}
 
 
+def oracle_indices_all(w: dict, k: int, P: int, rows=None):
+    """Oracle scores and selection of every decode sequence (or, with `rows`,
+    of those prefill query rows) of a device-resident workload: the indexer
+    cache, block table and indexer queries are read back once."""
+    icache = w["idx_cache"].cpu().numpy()  # int8; the oracle widens the rows it reads
+    bt = w["block_table"].cpu().numpy().astype(np.int64)
+    q_idx = w["q_idx"].cpu().numpy().astype(np.int64)
+    res = {}
+    if rows is None:  # decode: sequence b's newest token
+        lens = w["context_lens"].cpu().numpy()
+        items = [(b, b, int(lens[b]) - 1) for b in range(len(lens))]
+    else:             # prefill: query row i of sequence w["seq"]
+        items = [(int(i), int(w["seq"]), int(w["pos0"]) + int(i)) for i in rows]
+    for key, seq, pos in items:
+        ts, s = O.index_scores(q_idx[key], icache, bt[seq], P, pos)
+        idx, n_sel = O.topk_select(ts, s, k)
+        res[key] = {"scores": s, "idx": idx, "n_sel": n_sel, "pos": pos}
+    return res
+
+
 def run_prefill(w: dict, out_dtype=torch.bfloat16) -> dict:
     """index_scores -> topk_select -> sparse_attn_prefill for the queries of
     sequence w["seq"] at positions pos0 .. pos0 + T - 1."""

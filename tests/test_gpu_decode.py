@@ -231,31 +231,31 @@ def test_bad_selected_position_sets_status_not_fault(lib):
 
 # ------------------------------------------------------- full-size workloads ---
 def _full_size(cfg, sample_seqs, sample_heads):
+    """The full workload in the launch configuration the bench times: scores
+    and indices of EVERY sequence bit-exact against the oracle; attention
+    output and lse against the oracle on sampled (sequence, KV head) pairs."""
     spec = synth.CONFIGS[cfg]
     w = synth.make_workload(spec, 1000 + cfg, DEV)
     res = H.run_decode_step(w)
     P, k = spec.prefix_len, spec.k
     idx = res["idx"].cpu().numpy()
     n_sel = res["n_sel"].cpu().numpy()
+    scores = res["scores"].cpu().numpy()
     out = res["out"].float().cpu().numpy()
     lse = res["lse"].cpu().numpy()
     G = spec.num_q_heads // spec.num_kv_heads
+    ref = H.oracle_indices_all(w, k, P)
+    for b in range(spec.batch):
+        r = ref[b]
+        L = r["pos"] + 1
+        assert np.array_equal(scores[b, P:L], r["scores"]), f"scores seq {b}"
+        assert int(n_sel[b]) == r["n_sel"], f"n_sel seq {b}"
+        assert np.array_equal(idx[b], r["idx"]), f"idx seq {b}"
     for b in sample_seqs:
         r = H.oracle_decode_sampled(w, b, sample_heads, k, P)
-        L = int(w["context_lens"][b].item())
-        assert np.array_equal(res["scores"][b, P:L].cpu().numpy(), r["scores"]), f"scores seq {b}"
-        assert int(n_sel[b]) == r["n_sel"]
-        assert np.array_equal(idx[b], r["idx"]), f"idx seq {b}"
         for g, (o, s) in r["heads"].items():
             H.assert_close(out[b, g * G:(g + 1) * G], o, f"out seq {b} kv head {g}")
             H.assert_close(lse[b, g * G:(g + 1) * G], s, f"lse seq {b} kv head {g}")
-    # properties at every sequence: ascending, in range, prefix never selected
-    for b in range(spec.batch):
-        L = int(w["context_lens"][b].item())
-        sel = idx[b, :n_sel[b]]
-        assert n_sel[b] == min(k, max(0, L - P))
-        assert np.all(np.diff(sel) > 0) and (sel.size == 0 or (sel[0] >= P and sel[-1] < L))
-        assert np.all(idx[b, n_sel[b]:] == -1)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
