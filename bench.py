@@ -273,6 +273,8 @@ class Probes:
         for fn in ("probe_mma_s8", "probe_mma_bf16"):
             getattr(lib, fn).restype = C.c_float
             getattr(lib, fn).argtypes = [C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        lib.probe_tc.restype = C.c_float
+        lib.probe_tc.argtypes = [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         lib.probe_gather.restype = C.c_float
         lib.probe_gather.argtypes = [C.c_void_p, C.c_ulonglong, C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                      C.c_void_p]
@@ -292,6 +294,17 @@ class Probes:
         fn(ctas, 200, self.sink.data_ptr(), self._stream())
         best = min(fn(ctas, iters, self.sink.data_ptr(), self._stream()) for _ in range(5))
         return ctas * 8 * iters * 8 * ops / (best * 1e-3) / 1e12
+
+    def tc_tops(self, f8):
+        """Best of 5: TOPS (e4m3, f8=True) or TFLOP/s (f16) of back-to-back
+        tcgen05.mma 128 x 256 tiles, one CTA per SM."""
+        k = 32 if f8 else 16
+        iters = 20000
+        self.lib.probe_tc(int(f8), self.sms, 200, self.sink.data_ptr(), self._stream())
+        best = min(self.lib.probe_tc(int(f8), self.sms, iters, self.sink.data_ptr(), self._stream())
+                   for _ in range(5))
+        assert int(self.sink.sum().item()) == 0, "tensor-core probe wait ran out"
+        return self.sms * iters * 2 * 128 * 256 * k / (best * 1e-3) / 1e12
 
     def gather_gbs(self, piece, region_bytes=32 << 20):
         """Best of 5: GB/s of random `piece`-byte bulk copies into shared memory
@@ -360,8 +373,15 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
     gathered = int(n_sel_h.sum()) * hkv * 2 * 128 * 2                # selected K and V rows, every KV head
     s8 = probes.mma_tops("s8")
     bf16 = probes.mma_tops("bf16")
+    f8 = probes.tc_tops(True)
+    f16 = probes.tc_tops(False)
     gather = probes.gather_gbs(hkv * 128 * 2)
     idx_tops = 2 * 64 * causal_pairs / (ms["index"] * 1e-3) / 1e12
+    # The indexer stores a 4-byte score per scored pair and reads the indexer
+    # rows of the query and key tiles: it is bound by HBM, not by the tensor cores.
+    idx_bytes = 4 * causal_pairs + T * 64 + (T * 64) * ((T + 127) // 128) // 2
+    peak_hbm, peak_kind = measured_peaks()
+    idx_gbs = idx_bytes / (ms["index"] * 1e-3) / 1e9
     attn_gbs = gathered / (ms["attention"] * 1e-3) / 1e9
     # oracle on sampled rows of the chunk (rows drawn uniformly, seeded)
     cpu = None
@@ -379,17 +399,20 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
                          f"{el:.1f} s"}
     return {
         "workload": spec.name, "queries": T, "ms": {**ms, "total": total}, "tokens_per_s": T / (total * 1e-3),
-        "indexer": {"kernel": "prefill_index_kernel (mma.sync m16n8k32 s8)", "bound": "tensor",
-                    "achieved": idx_tops, "peak": s8, "unit": "int8 TOPS", "frac": idx_tops / s8,
-                    "ops": 2 * 64 * causal_pairs,
-                    "peak_kind": "measured in this run: mma.sync m16n8k32 s8 microbenchmark (libdsa_probe.so)"},
+        "indexer": {"kernel": "prefill_index_kernel (tcgen05.mma kind::f8f6f4, e4m3 operands, exact)",
+                    "bound": "hbm", "achieved": idx_gbs, "peak": peak_hbm, "unit": "GB/s",
+                    "frac": idx_gbs / peak_hbm, "bytes": idx_bytes, "peak_kind": peak_kind,
+                    "tops": idx_tops, "ops": 2 * 64 * causal_pairs,
+                    "tensor_peaks_tops": {"tcgen05_e4m3": f8, "tcgen05_f16": f16, "mma_sync_s8": s8},
+                    "tensor_frac": {"tcgen05_e4m3": idx_tops / f8, "mma_sync_s8": idx_tops / s8},
+                    "peak_note": "tensor peaks measured in this run by libdsa_probe.so microbenchmarks"},
         "attention": {"kernel": "dsa_sparse_attn_prefill per call: prefix_attn_kernel + sparse_attn_kernel + "
                                 "attn_combine_kernel", "bound": "l2",
                       "achieved": attn_gbs, "peak": gather, "unit": "GB/s", "frac": attn_gbs / gather,
                       "bytes": gathered,
                       "peak_kind": f"measured in this run: random {hkv * 256}-byte bulk copies from an L2-resident "
                                    f"32 MB buffer into shared memory (libdsa_probe.so)"},
-        "mma_bf16_peak_tflops": bf16,
+        "mma_sync_bf16_peak_tflops": bf16,
         "clocks": clock_info,
         "cpu_baseline": cpu,
     }

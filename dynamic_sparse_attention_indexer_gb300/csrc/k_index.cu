@@ -9,12 +9,15 @@
 // shared-memory bins added into a per-sequence global histogram), so the
 // selection needs no extra pass over the scores to find its threshold window.
 //
-// Prefill: the causal [T x 64] . [64 x L] int8 product on the tensor cores
-// (mma.sync m16n8k32 s8, exact int32), 128 x 128 output tiles, fully masked
-// tiles skipped.
+// Prefill: the causal [T x 64] . [64 x L] int8 product on the fifth-generation
+// tensor cores (tcgen05.mma, e4m3 or f16 operands, fp32 accumulation in tensor
+// memory, exact), 128 x 256 output tiles, fully masked tiles skipped.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "score_walk.cuh"
+#include "tc.cuh"
 
 namespace dsa {
 namespace {
@@ -234,7 +237,23 @@ __global__ void __launch_bounds__(256) decode_hist_kernel(const DecodeHistParams
 }
 
 // --------------------------------------------------------------- prefill ---
-constexpr int kPT = 128;  // query rows and key columns per tile
+// The causal [T x 64] . [64 x L] product on the fifth-generation tensor cores:
+// one CTA per tile of 128 queries x 256 keys (tiles wholly above the diagonal
+// or inside the prefix are skipped).  The four warps load the tile's int8 rows
+// (the keys through the block table), check whether every value lies in
+// [-16, 16], and convert them into the tensor-core operand layout: e4m3 when
+// they do (exact: e4m3 holds every integer up to 16), f16 otherwise (exact for
+// every int8).  One thread issues the MMAs (tcgen05.mma kind::f8f6f4, 2 x K=32,
+// or kind::f16, 4 x K=16), accumulating in fp32 in tensor memory: every product
+// and partial sum is an integer below 2^24 in magnitude (64 x 128 x 128 = 2^20),
+// so the fp32 result is the exact integer.  The epilogue reads the 128 x 256
+// accumulator back (each thread one query row) and stores the causal,
+// non-prefix part as int32.
+constexpr int kTcM = 128, kTcN = 256, kTcThreads = 128;
+constexpr int kTcSmem = 1024 + 16384 + 32768 + 64;  // alignment slack, A, B (f16 sizes), barrier + TMEM slot
+// One or two CTAs per SM: their accumulators (256 TMEM columns each) fit the
+// 512 columns of an SM, so no CTA waits for tensor memory.
+constexpr int kTcSmemAlloc = 80 * 1024;
 
 struct PrefillIndexParams {
   const int8_t* idx_cache;
@@ -244,83 +263,164 @@ struct PrefillIndexParams {
   int ld, max_blocks, num_blocks, prefix, seq, pos0, n_q;
 };
 
-// 64-byte rows, 16-byte chunks swizzled by (row >> 1) & 3: conflict-free ldmatrix.
-__device__ __forceinline__ int swz64(int row, int chunk) { return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4); }
+__device__ __forceinline__ bool any_above16(int4 v) {
+  const int w[4] = {v.x, v.y, v.z, v.w};
+  bool big = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int x = (int)(int8_t)((unsigned)w[i] >> (8 * b));
+      big |= x > 16 || x < -16;
+    }
+  return big;
+}
+__device__ __forceinline__ int sx8(int w, int b) { return (int)(int8_t)((unsigned)w >> (8 * b)); }
 
-__global__ void __launch_bounds__(256) prefill_index_kernel(const PrefillIndexParams p) {
-  __shared__ __align__(128) int8_t sA[kPT * kIdxDim];
-  __shared__ __align__(128) int8_t sB[kPT * kIdxDim];
+// Row r of an operand: 64 int8 values (4 int4) to e4m3 (64 bytes, 64-byte
+// swizzle) or to f16 (128 bytes, 128-byte swizzle).
+__device__ __forceinline__ void store_row_e4m3(uint8_t* op, int r, const int4 (&v)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = (uint32_t)e4m3x2((float)sx8(w[i], 0), (float)sx8(w[i], 1)) |
+             ((uint32_t)e4m3x2((float)sx8(w[i], 2), (float)sx8(w[i], 3)) << 16);
+    *reinterpret_cast<uint4*>(op + (r >> 3) * 512 + (r & 7) * 64 + ((c ^ ((r & 7) >> 1)) << 4)) =
+        make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+__device__ __forceinline__ void store_row_f16(uint8_t* op, int r, const int4 (&v)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // int4 c holds values 16 c .. 16 c + 15: f16 chunks 2 c and 2 c + 1
+    const int w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 lo = __halves2half2(__int2half_rn(sx8(w[i], 0)), __int2half_rn(sx8(w[i], 1)));
+      const __half2 hi = __halves2half2(__int2half_rn(sx8(w[i], 2)), __int2half_rn(sx8(w[i], 3)));
+      o[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+      o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ch = 2 * c + h;
+      *reinterpret_cast<uint4*>(op + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)) =
+          make_uint4(o[4 * h], o[4 * h + 1], o[4 * h + 2], o[4 * h + 3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads) prefill_index_kernel(const PrefillIndexParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = base;          // A: 128 query rows
+  uint8_t* sb = base + 16384;  // B: 256 key rows
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + 16384 + 32768);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t0 = blockIdx.x * kPT, i0 = blockIdx.y * kPT;
-  const int i_last = min(p.n_q, i0 + kPT) - 1;
+  const int t0 = blockIdx.x * kTcN, i0 = blockIdx.y * kTcM;
+  const int i_last = min(p.n_q, i0 + kTcM) - 1;
   const int t_max = p.pos0 + i_last;  // largest key any query of the tile sees
-  if (t0 > t_max || t0 + kPT - 1 < p.prefix) return;
+  if (t0 > t_max || t0 + kTcN - 1 < p.prefix) return;
 
-  for (int cidx = tid; cidx < kPT * 4; cidx += 256) {
-    const int row = cidx >> 2, ch = cidx & 3;
-    const int i = i0 + row;
-    cp_async16(sA + swz64(row, ch), p.q_idx + (size_t)min(i, p.n_q - 1) * kIdxDim + ch * 16, i < p.n_q ? 16u : 0u);
-    const int t = t0 + row;
-    const bool kv = t <= t_max;
-    const int blk = kv ? load_block(p.bt, p.seq, p.max_blocks, t >> 6, p.num_blocks, &g_status) : 0;
-    cp_async16(sB + swz64(row, ch), p.idx_cache + (size_t)blk * kIdxBlockBytes + (t & 63) * kIdxDim + ch * 16,
-               kv ? 16u : 0u);
+  if (warp == 0) tmem_alloc(tslot, kTcN);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
   }
-  cp_async_commit();
-  cp_async_wait<0>();
+  // Rows: query i0 + tid; keys t0 + tid and t0 + 128 + tid (zero past the
+  // last query / the last key the tile needs).
+  int4 qv[4], kv[2][4];
+  {
+    const int i = i0 + tid;
+    const int4* src = reinterpret_cast<const int4*>(p.q_idx + (size_t)min(i, p.n_q - 1) * kIdxDim);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) qv[c] = i < p.n_q ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + 128 * h + tid;
+      const bool ok = t <= t_max;
+      const int blk = ok ? load_block(p.bt, p.seq, p.max_blocks, t >> 6, p.num_blocks, &g_status) : 0;
+      const int4* ks = reinterpret_cast<const int4*>(p.idx_cache + ((size_t)blk * kBlock + (t & 63)) * kIdxDim);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) kv[h][c] = ok ? __ldg(ks + c) : make_int4(0, 0, 0, 0);
+    }
+  }
+  bool big = false;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) big |= any_above16(qv[c]) | any_above16(kv[0][c]) | any_above16(kv[1][c]);
+  const bool f16 = __syncthreads_or(big) != 0;
+  if (!f16) {
+    store_row_e4m3(sa, tid, qv);
+    store_row_e4m3(sb, tid, kv[0]);
+    store_row_e4m3(sb, tid + 128, kv[1]);
+  } else {
+    store_row_f16(sa, tid, qv);
+    store_row_f16(sb, tid, kv[0]);
+    store_row_f16(sb, tid + 128, kv[1]);
+  }
+  fence_proxy_async();
+  tc_fence_before();
   __syncthreads();
-
-  const int wm = warp & 3, wn = warp >> 2;  // warp tile: 32 rows x 64 cols
-  int acc[2][8][4];
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {
+    if (!f16) {
+      constexpr uint32_t idesc = mma_idesc(kTcM, kTcN, 0);
 #pragma unroll
-  for (int a = 0; a < 2; ++a)
+      for (int k = 0; k < 2; ++k)
+        mma_f8(tmem, smem_desc(smem_u32(sa) + 32 * k, 512, kSwizzle64), smem_desc(smem_u32(sb) + 32 * k, 512, kSwizzle64),
+               idesc, k > 0);
+    } else {
+      constexpr uint32_t idesc = mma_idesc(kTcM, kTcN, 0);
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[a][n][e] = 0;
-
-  const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    uint32_t af[2][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int row = wm * 32 + mt * 16 + (mi & 1) * 8 + rr;
-      ldsm_x4(smem_u32(sA + swz64(row, ks * 2 + (mi >> 1))), af[mt][0], af[mt][1], af[mt][2], af[mt][3]);
+      for (int k = 0; k < 4; ++k)
+        mma_f16(tmem, smem_desc(smem_u32(sa) + 32 * k, 1024, kSwizzle128),
+                smem_desc(smem_u32(sb) + 32 * k, 1024, kSwizzle128), idesc, k > 0);
     }
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      uint32_t b0, b1, b2, b3;
-      const int row = wn * 64 + (2 * np + (mi >> 1)) * 8 + rr;
-      ldsm_x4(smem_u32(sB + swz64(row, ks * 2 + (mi & 1))), b0, b1, b2, b3);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        mma_s8_16832(acc[mt][2 * np], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
-        mma_s8_16832(acc[mt][2 * np + 1], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b2, b3);
-      }
-    }
+    mma_commit(bar);
   }
-
+  if (!mbar_wait(bar, 0)) set_status(&g_status, kStTimeout);
+  tc_fence_after();
+  // Epilogue, 8 chunks of 32 keys: each thread reads its query row's 32
+  // accumulators from tensor memory into the warp's staging area (the operand
+  // memory is free now; row pitch 33 words: conflict-free both ways), then the
+  // warp stores 4 rows of 128 bytes per instruction (8 lanes per row).
+  int* stage = reinterpret_cast<int*>(base) + warp * 32 * 33;
+  const int sub_r = lane >> 3, sub_c = (lane & 7) * 4;
+#pragma unroll 1
+  for (int c = 0; c < kTcN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * c, r);
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
+    for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = __float2int_rn(__uint_as_float(r[j]));
+    __syncwarp();
+    const int t = t0 + 32 * c + sub_c;
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int i = i0 + wm * 32 + mt * 16 + hh * 8 + (lane >> 2);
-      if (i >= p.n_q) continue;
+    for (int m = 0; m < 8; ++m) {
+      const int rw = 4 * m + sub_r;
+      const int i = i0 + 32 * warp + rw;
       const int pos = p.pos0 + i;
-      int* out = p.scores + (size_t)i * p.ld;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int t = t0 + wn * 64 + nt * 8 + (lane & 3) * 2;
-        const int v0 = acc[mt][nt][2 * hh], v1 = acc[mt][nt][2 * hh + 1];
-        if (t >= p.prefix && t + 1 <= pos) {
-          *reinterpret_cast<int2*>(out + t) = make_int2(v0, v1);
+      const int* sv = stage + rw * 33 + sub_c;
+      if (i < p.n_q && t + 3 >= p.prefix && t <= pos) {
+        int* dst = p.scores + (size_t)i * p.ld + t;
+        if (t >= p.prefix && t + 3 <= pos) {
+          *reinterpret_cast<int4*>(dst) = make_int4(sv[0], sv[1], sv[2], sv[3]);
         } else {
-          if (t >= p.prefix && t <= pos) out[t] = v0;
-          if (t + 1 >= p.prefix && t + 1 <= pos) out[t + 1] = v1;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (t + q >= p.prefix && t + q <= pos) dst[q] = sv[q];
         }
       }
     }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTcN);
 }
 
 }  // namespace
@@ -330,7 +430,9 @@ int g_index_grid[64] = {};  // persistent indexer CTAs per device (SMs x residen
 }
 
 cudaError_t setup_index_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(decode_index_kernel<true, kIdxStages>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_index_kernel<true, kIdxStages>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, idx_smem_bytes());
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(decode_index_kernel<false, kIdxStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -418,8 +520,9 @@ cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx
   p.pos0 = qs.pos0;
   p.n_q = qs.n_q;
   const int last_pos = qs.pos0 + qs.n_q - 1;
-  dim3 grid(last_pos / kPT + 1, (qs.n_q + kPT - 1) / kPT);
-  prefill_index_kernel<<<grid, 256, 0, st>>>(p);
+  static_assert(kTcSmem <= kTcSmemAlloc, "prefill indexer shared memory");
+  dim3 grid(last_pos / kTcN + 1, (qs.n_q + kTcM - 1) / kTcM);
+  prefill_index_kernel<<<grid, kTcThreads, kTcSmemAlloc, st>>>(p);
   return cudaGetLastError();
 }
 

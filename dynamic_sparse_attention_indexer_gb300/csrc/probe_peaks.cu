@@ -7,6 +7,10 @@
 //                   uses (tcgen05 has no int8 kind on sm_103a).
 //   probe_mma_bf16  the same for mma.sync m16n8k16 bf16 / f32 accumulate (the
 //                   prefill prefix pass).
+//   probe_tc        fifth-generation tensor-core rate: back-to-back tcgen05.mma
+//                   of 128 x 256 tiles issued by one thread per CTA, kind::f8f6f4
+//                   (e4m3, K = 32) or kind::f16 (f16, K = 16), fp32 accumulation
+//                   in tensor memory (the prefill indexer's instructions).
 //   probe_gather    bulk copies (cp.async.bulk into shared memory) of `piece`
 //                   bytes from random offsets of a buffer: with a buffer that fits
 //                   the L2 this is the rate at which the SMs can gather rows that
@@ -19,6 +23,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace {
 
@@ -98,6 +103,49 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(const uint8_t
   }
 }
 
+// One thread per CTA issues `iters` MMAs of 128 x 256 x K into one 256-column
+// accumulator, then waits for them; the operands are zero (the rate does not
+// depend on the values).
+template <bool F8>
+__global__ void __launch_bounds__(128, 1) tc_kernel(int iters, int* sink) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sa = base;
+  uint8_t* sb = base + 16384;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + 16384 + 32768);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int tid = threadIdx.x;
+  for (int i = tid; i < (16384 + 32768) / 16; i += 128) reinterpret_cast<uint4*>(base)[i] = make_uint4(0, 0, 0, 0);
+  if (tid < 32) dsa::tmem_alloc(tslot, 256);
+  if (tid == 0) {
+    dsa::mbar_init(bar, 1);
+    dsa::mbar_fence_init();
+  }
+  dsa::fence_proxy_async();
+  dsa::tc_fence_before();
+  __syncthreads();
+  dsa::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {
+    constexpr uint32_t idesc = dsa::mma_idesc(128, 256, 0);
+    for (int it = 0; it < iters; ++it) {
+      const uint32_t k = it & 1;
+      if (F8)
+        dsa::mma_f8(tmem, dsa::smem_desc(dsa::smem_u32(sa) + 32 * k, 512, dsa::kSwizzle64),
+                    dsa::smem_desc(dsa::smem_u32(sb) + 32 * k, 512, dsa::kSwizzle64), idesc, it > 0);
+      else
+        dsa::mma_f16(tmem, dsa::smem_desc(dsa::smem_u32(sa) + 32 * k, 1024, dsa::kSwizzle128),
+                     dsa::smem_desc(dsa::smem_u32(sb) + 32 * k, 1024, dsa::kSwizzle128), idesc, it > 0);
+    }
+    dsa::mma_commit(bar);
+  }
+  if (!dsa::mbar_wait(bar, 0)) atomicExch(sink, 3);
+  dsa::tc_fence_before();
+  __syncthreads();
+  dsa::tc_fence_after();
+  if (tid < 32) dsa::tmem_dealloc(tmem, 256);
+}
+
 template <typename F>
 float timed(cudaStream_t st, F launch) {
   cudaEvent_t a, b;
@@ -130,6 +178,16 @@ float probe_mma_s8(int ctas, int iters, int* sink, cudaStream_t st) {
 // (2 * 16 * 8 * 16 = 4096 flops each).
 float probe_mma_bf16(int ctas, int iters, int* sink, cudaStream_t st) {
   return timed(st, [&] { mma_bf16_kernel<<<ctas, 32 * kMmaWarps, 0, st>>>(iters, sink); });
+}
+
+// Elapsed ms of `ctas` CTAs (at most one per SM) x iters tcgen05.mma of
+// 128 x 256 x K: e4m3 (f8 != 0; K = 32, 2 * 128 * 256 * 32 operations each)
+// or f16 (K = 16, 2 * 128 * 256 * 16 flops each).
+float probe_tc(int f8, int ctas, int iters, int* sink, cudaStream_t st) {
+  auto kern = f8 ? tc_kernel<true> : tc_kernel<false>;
+  // 80 KB of shared memory keeps to one or two CTAs per SM (256 TMEM columns each).
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 80 * 1024) != cudaSuccess) return -1.f;
+  return timed(st, [&] { kern<<<ctas, 128, 80 * 1024, st>>>(iters, sink); });
 }
 
 // Elapsed ms of `ctas` CTAs each gathering iters x 64 KB in `piece`-byte bulk
