@@ -53,10 +53,19 @@ def _stream(device=None):
     return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def kv_cache_adjacent(num_blocks: int, num_kv_heads: int, device):
+    """An uninitialised paged K/V cache in the adjacent layout: one bf16 array
+    [num_blocks][64][2][Hkv][128] (the K and V of a slot one contiguous piece);
+    returns the (k_cache, v_cache) views [num_blocks][64][Hkv][128] of it."""
+    kv = torch.empty((num_blocks, BLOCK_SIZE, 2, num_kv_heads, HEAD_DIM), dtype=torch.bfloat16, device=device)
+    return kv[:, :, 0], kv[:, :, 1]
+
+
 class PagedKV:
-    """The paged cache: k_cache/v_cache bf16 [num_blocks][64][Hkv][128],
-    idx_cache int8 [num_blocks][64][64], block_table int32 [B][max_blocks],
-    context_lens int32 [B] (all on one CUDA device)."""
+    """The paged cache: k_cache/v_cache bf16 [num_blocks][64][Hkv][128] (two
+    arrays, or the two views of kv_cache_adjacent), idx_cache int8
+    [num_blocks][64][64], block_table int32 [B][max_blocks], context_lens int32
+    [B] (all on one CUDA device)."""
 
     def __init__(self, k_cache, v_cache, idx_cache, block_table, context_lens, max_context_len=None):
         self.k_cache, self.v_cache, self.idx_cache = k_cache, v_cache, idx_cache
@@ -66,10 +75,16 @@ class PagedKV:
         self.max_context_len = int(max_context_len)
         self.num_kv_heads = int(k_cache.shape[2])
         self.batch = int(block_table.shape[0])
+        # Rows of consecutive slots are kv_row_stride values apart in both arrays.
+        row = int(k_cache.stride(1))
+        for t in (k_cache, v_cache):
+            if t.stride(3) != 1 or t.stride(2) != HEAD_DIM or t.stride(1) != row or t.stride(0) != BLOCK_SIZE * row:
+                raise ValueError("k_cache / v_cache: each slot's row must hold its KV heads contiguously, "
+                                 "slots evenly spaced and the same in both arrays")
         self.struct = _abi.PagedKV(
             _ptr(k_cache), _ptr(v_cache), _ptr(idx_cache), _ptr(block_table), _ptr(context_lens),
             int(k_cache.shape[0]), int(k_cache.shape[1]), self.num_kv_heads, int(k_cache.shape[3]),
-            int(idx_cache.shape[2]), int(block_table.shape[1]), self.batch, self.max_context_len)
+            int(idx_cache.shape[2]), int(block_table.shape[1]), self.batch, self.max_context_len, row)
 
     @property
     def ref(self):

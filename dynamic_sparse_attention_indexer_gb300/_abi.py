@@ -14,7 +14,8 @@ class PagedKV(C.Structure):
     _fields_ = [("k_cache", c_p), ("v_cache", c_p), ("idx_cache", c_p), ("block_table", c_p),
                 ("context_lens", c_p), ("num_blocks", c_i32), ("block_size", c_i32),
                 ("num_kv_heads", c_i32), ("head_dim", c_i32), ("idx_dim", c_i32),
-                ("max_blocks_per_seq", c_i32), ("batch", c_i32), ("max_context_len", c_i32)]
+                ("max_blocks_per_seq", c_i32), ("batch", c_i32), ("max_context_len", c_i32),
+                ("kv_row_stride", c_i32)]
 
 
 class QuerySet(C.Structure):

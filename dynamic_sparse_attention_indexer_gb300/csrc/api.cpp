@@ -73,6 +73,13 @@ dsa_status check_kv(const dsa_paged_kv* kv, dsa::KV* out) {
     return fail(DSA_ERR_INVALID_ARG, "k_cache, v_cache and idx_cache must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(kv->block_table) & 3u) || (reinterpret_cast<uintptr_t>(kv->context_lens) & 3u))
     return fail(DSA_ERR_INVALID_ARG, "block_table and context_lens must be 4-byte aligned");
+  const int32_t row = kv->num_kv_heads * 128;
+  const int32_t stride = kv->kv_row_stride == 0 ? row : kv->kv_row_stride;
+  if (stride < row || stride % 8 != 0)
+    return fail(DSA_ERR_INVALID_ARG, "kv_row_stride %d: must be 0 or a multiple of 8 >= num_kv_heads * 128 (%d)",
+                kv->kv_row_stride, row);
+  if ((int64_t)kv->num_blocks * 64 * stride >= (int64_t(1) << 40))
+    return fail(DSA_ERR_UNSUPPORTED, "num_blocks * 64 * kv_row_stride must stay below 2^40 values");
   out->k_cache = kv->k_cache;
   out->v_cache = kv->v_cache;
   out->idx_cache = kv->idx_cache;
@@ -83,6 +90,9 @@ dsa_status check_kv(const dsa_paged_kv* kv, dsa::KV* out) {
   out->max_blocks = kv->max_blocks_per_seq;
   out->batch = kv->batch;
   out->max_ctx = kv->max_context_len;
+  out->row_stride = stride;
+  out->adjacent = stride == 2 * row &&
+                  static_cast<const char*>(kv->v_cache) == static_cast<const char*>(kv->k_cache) + 2 * (size_t)row;
   return DSA_OK;
 }
 

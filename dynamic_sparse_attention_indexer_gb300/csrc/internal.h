@@ -16,6 +16,8 @@ struct KV {
   const int32_t* block_table;
   const int32_t* context_lens;
   int num_blocks, hkv, max_blocks, batch, max_ctx;
+  int row_stride;  // bf16 values between the K (or V) rows of consecutive slots
+  bool adjacent;   // V row right after the K row of the same slot: one piece of 2 * hkv * 256 bytes
 };
 
 struct QS {

@@ -3,7 +3,8 @@
 //
 // The cache keeps, for every slot (block * 64 + row), the K rows of all KV heads
 // side by side (and the same for V), so one attended position is one contiguous
-// piece of Hkv * 256 bytes of K and one of V.  A query has P + k attended-row
+// piece of Hkv * 256 bytes of K and one of V; where the cache stores a slot's V
+// row right after its K row the two are one piece, fetched with one copy.  A query has P + k attended-row
 // slots, its causal prefix rows then its selected rows (slots past its actual
 // rows are empty).  A persistent grid (one CTA per SM) takes one contiguous
 // range of the row slots of all queries per CTA (the same number of rows to
@@ -53,6 +54,7 @@ constexpr int kQBytes = kMaxHq * kHeadDim * 2;    // one query's Q, all heads: 1
 constexpr int kSmemBytes = kStages * kStageBytes + kQBytes + 8 * (2 * kStages + 2) + 16;
 static_assert(kProducerWarps == kStages + 1, "one producer warp per stage, plus the query copier");
 static_assert(2 * 16 * (kPieceMax + kRowPad) <= kStageBytes, "Hkv = 8 stage must fit");
+static_assert(kTileRowsMax * (2 * kHeadDim * 2 + kRowPad) <= kStageBytes, "adjacent K/V stage (Hkv = 1) must fit");
 static_assert(kSmemBytes <= 232448, "attention shared memory above the 227 KB per-CTA limit");
 
 struct AttnParams {
@@ -68,7 +70,11 @@ struct AttnParams {
   int max_blocks, num_blocks, hkv, hq, group, k, prefix, max_ctx;
   int rows;          // attended rows per tile: 128 / hkv
   int piece;         // bytes of one position's K (or V): hkv * 256
-  int pitch;         // shared-memory row pitch: piece + 16
+  int row_stride;    // bf16 values between the K (or V) rows of consecutive cache slots
+  int per_row;       // copies per attended row: 1 (K and V adjacent in the cache, one piece) or 2
+  int cbytes;        // bytes of one copy: 2 * piece or piece
+  int pitch;         // shared-memory row pitch: cbytes + 16 (adjacent) or piece + 16
+  int v_off;         // shared-memory offset of a row's V from its K: piece (adjacent) or rows * pitch
   float scale_log2;
   int units;         // n_q * rows_per_q attended-row slots (< 2^31, checked on the host)
   int rows_per_q;    // prefix + k (k when the prefix part comes from pre_ml)
@@ -247,20 +253,24 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
   if (warp < kProducerWarps) {
     // ---------------------------------------------------------- producers
     if constexpr (!PS) {
-      // Copy c of a tile (K of row c / 2 if c is even, V if odd) is issued by
-      // thread (c % 4) * 32 + (c / 4) % 32, so the copies spread over the warps.
+      // Copy c of a tile (row c / per_row: its K and V in one piece when they
+      // are adjacent in the cache, else K if c is even and V if odd) is issued
+      // by thread (c % 4) * 32 + (c / 4) % 32, so the copies spread over the warps.
       // Rows from the valid count up to the next multiple of 16 (the rest of the
       // last 16-row chunk the consumers read) get the last valid row again, so
       // that every row the math touches holds finite cache values; their
       // probabilities are zero.
       const int pt = lane * kProducerWarps + warp;
-      const int n_copies = 2 * p.rows;
+      const int shift = p.per_row - 1;  // 0 or 1
+      const int n_copies = p.rows << shift;
       auto filled = [&](const Tile& tl) { return min((tl.nvalid + 15) & ~15, p.rows); };
       auto active = [&](const Tile& tl, int u) {
         const int c = pt + u * kProducerThreads;
-        return c < n_copies && (c >> 1) < filled(tl);
+        return c < n_copies && (c >> shift) < filled(tl);
       };
-      auto row_of = [&](const Tile& tl, int u) { return tl.r0 + min((pt + u * kProducerThreads) >> 1, tl.nvalid - 1); };
+      auto row_of = [&](const Tile& tl, int u) {
+        return tl.r0 + min((pt + u * kProducerThreads) >> shift, tl.nvalid - 1);
+      };
       Cursor cur;
       cursor_init(cur, p);
       Tile t0, t1, t2;  // issued now, next, the one after
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         uint32_t bytes = 0;
 #pragma unroll
         for (int u = 0; u < 2; ++u)
-          if (active(t0, u)) bytes += p.piece;
+          if (active(t0, u)) bytes += p.cbytes;
         if (first && pt == 0) {
           if (seg > 0 && !mbar_wait(q_empty, (seg - 1) & 1)) {
             set_status(&g_status, kStTimeout);
@@ -305,10 +315,10 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         for (int u = 0; u < 2; ++u) {
           const int c = pt + u * kProducerThreads;
           if (active(t0, u)) {
-            const int r = c >> 1;
+            const int r = c >> shift, part = c & shift;  // part 1: the V of a separate layout
             const size_t sl = (size_t)resolve(p, v0[u]);
-            const __nv_bfloat16* src = ((c & 1) ? p.vc : p.kc) + sl * p.hkv * kHeadDim;
-            bulk_g2s(st + (c & 1) * p.rows * p.pitch + r * p.pitch, src, p.piece, &full[s]);
+            const __nv_bfloat16* src = (part ? p.vc : p.kc) + sl * p.row_stride;
+            bulk_g2s(st + r * p.pitch + part * p.v_off, src, p.cbytes, &full[s]);
           }
         }
         if (first && pt == 0)
@@ -390,9 +400,9 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
           for (int i = 0; i < 4; ++i)
             if (active(t0, i)) {
               const int r = lane + 32 * i;
-              const size_t off = (size_t)resolve(p, v0[i]) * p.hkv * kHeadDim;
-              bulk_g2s(st + r * p.pitch, p.kc + off, p.piece, &full[w]);
-              bulk_g2s(st + (p.rows + r) * p.pitch, p.vc + off, p.piece, &full[w]);
+              const size_t off = (size_t)resolve(p, v0[i]) * p.row_stride;
+              bulk_g2s(st + r * p.pitch, p.kc + off, p.cbytes, &full[w]);
+              if (p.per_row == 2) bulk_g2s(st + r * p.pitch + p.v_off, p.vc + off, p.piece, &full[w]);
             }
           // Advance: second loads of the next tile, first loads of the one after.
 #pragma unroll
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
       }
     }
     const uint8_t* sk = smem + s * kStageBytes + g * (kHeadDim * 2);
-    attend_rows(hs, sk, sk + p.rows * p.pitch, p.pitch, t.nvalid, p.scale_log2, lane);
+    attend_rows(hs, sk, sk + p.v_off, p.pitch, t.nvalid, p.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
 
@@ -663,7 +673,11 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.max_ctx = a.kv.max_ctx;
   p.rows = kTileRowsMax / a.kv.hkv;
   p.piece = a.kv.hkv * kHeadDim * 2;
-  p.pitch = p.piece + kRowPad;
+  p.row_stride = a.kv.row_stride;
+  p.per_row = a.kv.adjacent ? 1 : 2;
+  p.cbytes = a.kv.adjacent ? 2 * p.piece : p.piece;
+  p.pitch = p.cbytes + kRowPad;
+  p.v_off = a.kv.adjacent ? p.piece : p.rows * p.pitch;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.pre_ml = a.ws.pre_ml;
   p.pre_o = a.ws.pre_o;

@@ -21,11 +21,12 @@ struct WriteParams {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const int8_t* ik;
-  int ntok, hkv, num_blocks;
+  int ntok, hkv, num_blocks, row_stride;
 };
 
 // One CTA per token: Hkv x 16 chunks of K, the same of V, 4 chunks of the indexer key.
-// A slot's K (and V) row holds all KV heads contiguously, so both copies are straight runs.
+// A slot's K (and V) row holds all KV heads contiguously (row_stride values apart
+// from the next slot's), so both copies are straight runs.
 __global__ void kv_write_kernel(const WriteParams p) {
   const int j = blockIdx.x;
   const int slot = __ldg(p.slots + j);
@@ -40,7 +41,7 @@ __global__ void kv_write_kernel(const WriteParams p) {
       const bool is_v = c >= kv_chunks;
       const int cc = is_v ? c - kv_chunks : c;
       const __nv_bfloat16* src = (is_v ? p.v : p.k) + (size_t)j * p.hkv * kHeadDim + cc * 8;
-      __nv_bfloat16* dst = (is_v ? p.vc : p.kc) + (size_t)slot * p.hkv * kHeadDim + cc * 8;
+      __nv_bfloat16* dst = (is_v ? p.vc : p.kc) + (size_t)slot * p.row_stride + cc * 8;
       *reinterpret_cast<int4*>(dst) = __ldg(reinterpret_cast<const int4*>(src));
     } else {
       const int ch = c - 2 * kv_chunks;
@@ -59,7 +60,7 @@ struct GatherParams {
   const int32_t* nsel;
   __nv_bfloat16* ko;
   __nv_bfloat16* vo;
-  int mode, seq, pos0, max_blocks, num_blocks, hkv, k, prefix, rows_out, max_ctx;
+  int mode, seq, pos0, max_blocks, num_blocks, hkv, k, prefix, rows_out, max_ctx, row_stride;
 };
 
 // CTA: 8 output rows of one (query, KV head); 16 threads per row.
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(128) kv_gather_kernel(const GatherParams p) {
       blk = load_block(p.bt, seq, p.max_blocks, t >> 6, p.num_blocks, &g_status);
     else
       set_status(&g_status, kStBadBlock);
-    const size_t src = (((size_t)blk * kBlock + (t & 63)) * p.hkv + g) * kHeadDim + ch * 8;
+    const size_t src = ((size_t)blk * kBlock + (t & 63)) * p.row_stride + (size_t)g * kHeadDim + ch * 8;
     kval = __ldg(reinterpret_cast<const int4*>(p.kc + src));
     vval = __ldg(reinterpret_cast<const int4*>(p.vc + src));
   }
@@ -103,6 +104,7 @@ cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const 
   p.ntok = ntok;
   p.hkv = kv.hkv;
   p.num_blocks = kv.num_blocks;
+  p.row_stride = kv.row_stride;
   kv_write_kernel<<<ntok, 128, 0, st>>>(p);
   return cudaGetLastError();
 }
@@ -128,6 +130,7 @@ cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, con
   p.prefix = prefix;
   p.rows_out = prefix + k;
   p.max_ctx = kv.max_ctx;
+  p.row_stride = kv.row_stride;
   dim3 grid((p.rows_out + 7) / 8, kv.hkv, qs.n_q);
   kv_gather_kernel<<<grid, 128, 0, st>>>(p);
   return cudaGetLastError();

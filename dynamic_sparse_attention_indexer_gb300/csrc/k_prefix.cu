@@ -37,7 +37,7 @@ struct PrefixParams {
   const __nv_bfloat16* kc;  // [num_blocks][64][hkv][128]
   const __nv_bfloat16* vc;
   const int32_t* bt;
-  int seq, pos0, n_q, hq, hkv, group, prefix, max_blocks, num_blocks;
+  int seq, pos0, n_q, hq, hkv, group, prefix, max_blocks, num_blocks, row_stride;
   float scale_log2;
   float2* pre_ml;  // [n_q][hq] (max in log2 units, sum of weights)
   float* pre_o;    // [n_q][hq][128] unnormalised output
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kPreThreads) prefix_attn_kernel(const PrefixPa
     for (int e = tid; e < kPreKeys * (kHeadDim / 8); e += kPreThreads) {
       const int j = e / (kHeadDim / 8), ch = e % (kHeadDim / 8);
       const bool ok = c * kPreKeys + j < p.prefix;
-      const size_t off = (((size_t)blk * kBlock + j) * p.hkv + g) * kHeadDim + ch * 8;
+      const size_t off = ((size_t)blk * kBlock + j) * p.row_stride + (size_t)g * kHeadDim + ch * 8;
       cp_async16(dk + j * kPrePitch + ch * 16, p.kc + off, ok ? 16u : 0u);
       cp_async16(dv + j * kPrePitch + ch * 16, p.vc + off, ok ? 16u : 0u);
     }
@@ -238,6 +238,7 @@ cudaError_t launch_prefix_attn(const KV& kv, const QS& qs, const void* q, int hq
   p.prefix = prefix;
   p.max_blocks = kv.max_blocks;
   p.num_blocks = kv.num_blocks;
+  p.row_stride = kv.row_stride;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.pre_ml = pre_ml;
   p.pre_o = pre_o;

@@ -30,9 +30,18 @@
  *   - Launch failures return DSA_ERR_CUDA with the CUDA error text.
  *
  * Data layout (row-major, innermost last)
- *   k_cache, v_cache : bf16 [num_blocks][64][num_kv_heads][128]   64 consecutive positions per
- *                      block; a block row holds every KV head of its position, so the K (or V)
- *                      of one position is one contiguous num_kv_heads * 256-byte piece
+ *   k_cache, v_cache : bf16 rows of num_kv_heads * 128 values (every KV head of one position,
+ *                      head h at h * 128), one row per cache slot (slot = block * 64 + row),
+ *                      slot s at k_cache + s * kv_row_stride (v_cache likewise).  Two layouts:
+ *                        separate  kv_row_stride = num_kv_heads * 128 (or 0): k_cache and
+ *                                  v_cache are [num_blocks][64][num_kv_heads][128] each;
+ *                        adjacent  kv_row_stride = 2 * num_kv_heads * 128 and
+ *                                  v_cache = k_cache + num_kv_heads * 128: one array
+ *                                  [num_blocks][64][2][num_kv_heads][128], the K and V of a
+ *                                  slot one contiguous 2 * num_kv_heads * 256-byte piece, which
+ *                                  the attention kernels gather with one copy per position
+ *                                  (fewer, larger copies: the faster layout);
+ *                      any other stride >= num_kv_heads * 128 (multiple of 8) is accepted too
  *   idx_cache        : int8 [num_blocks][64][64]                   indexer key per position
  *   block_table      : int32 [batch][max_blocks_per_seq]           position t of sequence b is
  *                      row t % 64 of block block_table[b][t / 64]
@@ -49,7 +58,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 typedef enum dsa_status {
   DSA_OK = 0,
@@ -72,7 +81,9 @@ enum {
 /* The paged KV cache, described (not owned).  Fixed sizes: block_size 64,
  * head_dim 128, idx_dim 64 (others return DSA_ERR_UNSUPPORTED).
  * max_context_len is a HOST upper bound of context_lens[] (decode) used to size
- * grids; it must be <= max_blocks_per_seq * 64. */
+ * grids; it must be <= max_blocks_per_seq * 64.  kv_row_stride: bf16 values
+ * between the K (or V) rows of consecutive slots (see the data layout above;
+ * 0 = num_kv_heads * 128). */
 typedef struct dsa_paged_kv {
   void* k_cache;
   void* v_cache;
@@ -87,6 +98,7 @@ typedef struct dsa_paged_kv {
   int32_t max_blocks_per_seq;
   int32_t batch;
   int32_t max_context_len;
+  int32_t kv_row_stride;
 } dsa_paged_kv;
 
 /* Which query tokens a call serves.

@@ -16,7 +16,15 @@ ATOL, RTOL = 2e-3, 1e-2
 
 
 def on(w: dict, device) -> dict:
-    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    """The workload on `device`; an adjacent-layout cache moves as its one
+    array and gets its k_cache / v_cache views back."""
+    out = {k: (v.to(device) if isinstance(v, torch.Tensor) and k not in ("k_cache", "v_cache") else v)
+           for k, v in w.items()}
+    if "kv" in w:
+        out["k_cache"], out["v_cache"] = out["kv"][:, :, 0], out["kv"][:, :, 1]
+    else:
+        out["k_cache"], out["v_cache"] = w["k_cache"].to(device), w["v_cache"].to(device)
+    return out
 
 
 def paged_kv(w: dict) -> dsa.PagedKV:

@@ -42,6 +42,7 @@ class Spec:
     num_queries: int = 0           # prefill: T
     pos0: int = 0                  # prefill: position of query 0
     spare_blocks: int = 0          # extra unused blocks in the pool
+    kv_layout: str = "adjacent"    # "adjacent": K and V of a slot in one row; "separate": two arrays
 
 
 # The five workloads of the headline measurement plan.
@@ -102,10 +103,20 @@ def make_workload(spec: Spec, seed: int, device="cpu") -> dict:
         off += n
 
     hkv, hq = spec.num_kv_heads, spec.num_q_heads
-    k_cache = _randn_bf16((pool, BLOCK, hkv, HEAD_DIM), _gen(seed, "k_cache", device), device,
-                          chunk_rows=max(1, (1 << 24) // (hkv * BLOCK * HEAD_DIM)))
-    v_cache = _randn_bf16((pool, BLOCK, hkv, HEAD_DIM), _gen(seed, "v_cache", device), device,
-                          chunk_rows=max(1, (1 << 24) // (hkv * BLOCK * HEAD_DIM)))
+    # The same values in either layout (each array drawn from its own stream).
+    if spec.kv_layout == "adjacent":
+        kv = torch.empty((pool, BLOCK, 2, hkv, HEAD_DIM), dtype=torch.bfloat16, device=device)
+        k_cache, v_cache = kv[:, :, 0], kv[:, :, 1]
+    else:
+        k_cache = torch.empty((pool, BLOCK, hkv, HEAD_DIM), dtype=torch.bfloat16, device=device)
+        v_cache = torch.empty_like(k_cache)
+    rows = max(1, (1 << 24) // (hkv * BLOCK * HEAD_DIM))
+    for name, dst in (("k_cache", k_cache), ("v_cache", v_cache)):
+        g = _gen(seed, name, device)
+        for s0 in range(0, pool, rows):
+            e0 = min(pool, s0 + rows)
+            dst[s0:e0] = torch.randn((e0 - s0, BLOCK, hkv, HEAD_DIM), generator=g, device=device,
+                                     dtype=torch.float32).to(torch.bfloat16)
     if spec.outlier_frac > 0:
         # One independent Bernoulli draw per (block, row, kv head), i.e. per
         # (sequence, position, kv head); K only, before use (x4 is exact in bf16).
@@ -119,7 +130,7 @@ def make_workload(spec: Spec, seed: int, device="cpu") -> dict:
     q = _randn_bf16((nq, hq, HEAD_DIM), _gen(seed, "q", device), device)
     q_idx = torch.randint(spec.idx_lo, spec.idx_hi + 1, (nq, IDX_DIM),
                           generator=_gen(seed, "q_idx", device), device=device, dtype=torch.int8)
-    return {
+    out = {
         "spec": spec, "seed": seed, "mode": spec.mode,
         "k_cache": k_cache, "v_cache": v_cache, "idx_cache": idx_cache,
         "block_table": bt.to(device), "context_lens": torch.tensor(lens, dtype=torch.int32).to(device),
@@ -129,6 +140,9 @@ def make_workload(spec: Spec, seed: int, device="cpu") -> dict:
         "seq": 0, "pos0": spec.pos0, "num_queries": nq,
         "max_context_len": max(lens),
     }
+    if spec.kv_layout == "adjacent":
+        out["kv"] = kv  # the one array behind the k_cache / v_cache views
+    return out
 
 
 def to_numpy(w: dict) -> dict:
@@ -136,6 +150,8 @@ def to_numpy(w: dict) -> dict:
     integers -> int64."""
     out = {}
     for key, val in w.items():
+        if key == "kv":
+            continue  # the k_cache / v_cache views carry its values
         if isinstance(val, torch.Tensor):
             t = val.detach().cpu()
             if t.dtype == torch.bfloat16:

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(raw, n), f"{n} declared in dsa.h but not exported"
         assert n in _abi.SIGNATURES, f"{n} has no ctypes signature"
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     assert lib.dsa_status_string(OOM) == b"DSA_ERR_OOM"
 
 
@@ -84,6 +84,8 @@ def _qs(mode=0, n_q=2, seq=0, pos0=0):
     (dict(v_cache=0x20008), INVALID),         # misaligned
     (dict(max_context_len=8 * 64 + 1), INVALID),
     (dict(batch=0), INVALID),
+    (dict(kv_row_stride=2 * 128 - 8), INVALID),   # below the row of two KV heads
+    (dict(kv_row_stride=2 * 2 * 128 + 4), INVALID),  # rows not 16-byte aligned
 ])
 def test_index_scores_rejects_bad_cache(lib, over, status):
     kv = _kv(**over)
@@ -91,6 +93,18 @@ def test_index_scores_rejects_bad_cache(lib, over, status):
     st = lib.dsa_index_scores(C.byref(kv), C.byref(qs), 0x60000, 0, 0x70000, 512, None, 0, None)
     assert st == status
     assert lib.dsa_last_error_message()
+
+
+def test_kv_row_stride_layouts_accepted(lib):
+    """0 (separate arrays), the separate and the adjacent strides pass the cache
+    checks (the call then reaches the CUDA runtime, absent here)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    for stride, v in ((0, 0x20000), (2 * 128, 0x20000), (2 * 2 * 128, 0x10000 + 2 * 128 * 2)):
+        kv = _kv(kv_row_stride=stride, v_cache=v)
+        qs = _qs(n_q=kv.batch)
+        assert lib.dsa_index_scores(C.byref(kv), C.byref(qs), 0x60000, 0, 0x70000, 512, None, 0, None) == CUDA
 
 
 def test_argument_checks(lib):

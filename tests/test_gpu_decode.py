@@ -22,8 +22,11 @@ def _run(spec, seed=11, out_dtype=torch.bfloat16, split_api=False, mutate=None):
     return res
 
 
-def test_decode_small_fused(lib):
-    _run(synth.small_spec())
+@pytest.mark.parametrize("layout", ["adjacent", "separate"])
+def test_decode_small_fused(lib, layout):
+    """K and V of a slot in one row (one copy per attended position) or in two
+    arrays (two copies)."""
+    _run(synth.small_spec(kv_layout=layout))
 
 
 def test_decode_small_split_calls_match_fused(lib):
@@ -47,8 +50,9 @@ def test_decode_edge_shapes(lib, lens, prefix, k):
 
 
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (32, 2), (8, 8), (16, 1), (64, 8), (8, 1)])
-def test_decode_group_sizes(lib, hq, hkv):
-    _run(synth.small_spec(hq=hq, hkv=hkv, lens=(900, 1800)))
+@pytest.mark.parametrize("layout", ["adjacent", "separate"])
+def test_decode_group_sizes(lib, hq, hkv, layout):
+    _run(synth.small_spec(hq=hq, hkv=hkv, lens=(900, 1800), kv_layout=layout))
 
 
 @pytest.mark.parametrize("lens", [

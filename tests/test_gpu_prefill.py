@@ -51,6 +51,11 @@ def test_prefill_full_int8_range(lib):
     _run(_prefill_spec(T=150, pos0=300, P=64, k=90, idx_lo=-128, idx_hi=127))
 
 
+def test_prefill_separate_kv_arrays(lib):
+    """The same path with K and V in two arrays (two copies per attended row)."""
+    _run(_prefill_spec(T=200, pos0=100, P=64, k=100, hq=16, hkv=4, kv_layout="separate"))
+
+
 def test_prefill_prefix_tiles_ragged(lib):
     """The prefix part is computed per tile of queries: a group of 3 heads (42
     queries per 128-row tile, two rows unused), a prefix of 130 (three 64-key
