@@ -93,8 +93,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = p.prefix, jb_base = P / kBlock;
-  // Shared-memory set-up first: it touches no global memory, so it overlaps
-  // the previous kernel's tail.
+  // Set-up before the wait on the previous kernel of the stream, so that it
+  // overlaps that kernel's tail: shared memory, then the inputs no kernel of
+  // the step writes (context lengths, block table, the indexer cache outside
+  // each sequence's newest position; the caller's contract in dsa.h).  The
+  // scores and histograms are written only after the wait.
   if (kHist)
     for (int i = tid; i < kIdxConsumers * kCoarseBins; i += kIdxThreads) hist[i] = 0;
   if (tid == 0) {
@@ -104,8 +107,6 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
     }
     mbar_fence_init();
   }
-  pdl_wait();
-  pdl_trigger();
   candidate_blocks(p.ctx, p.batch, p.max_ctx, P, seg_start, len, scratch);
   const long long T = seg_start[p.batch];
   const int f_begin = (int)(T * blockIdx.x / gridDim.x), f_end = (int)(T * (blockIdx.x + 1) / gridDim.x);
@@ -133,10 +134,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
   Group g;
 
   if (warp == 0) {
-    // ---- producer: lane i < 4 copies block i of each group
+    // ---- producer: lane i < 4 copies block i of each group.  The first
+    // groups are copied before the wait on the previous kernel, up to the ring
+    // size or the first group holding a sequence's newest position (which the
+    // cache write of this step may be the previous kernel to write).
     if (lane >= kGroupBlocks) return;
+    bool waited = false;
     for (int n = 0; next_group(cur, seg_start, jb_base, &g); ++n) {
       const int s = n % kStg;
+      const int newest_jb = (len[g.b] - 1) >> 6;
+      if (!waited && (n >= kStg || (newest_jb >= g.jb && newest_jb < g.jb + g.count))) {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+      }
       if (n >= kStg && !mbar_wait(&empty[s], ((n / kStg) - 1) & 1)) {
         set_status(&g_status, kStTimeout);
         return;
@@ -152,6 +163,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
     return;
   }
 
+  pdl_wait();
+  pdl_trigger();
   // ---- consumers: warp cw scores rows 32 (cw % 2) .. + 31 of block cw / 2 of each
   // group.  Four lanes share a row, lane l taking the 16-byte chunk l % 4 of the
   // key (so its query chunk is fixed and the warp's shared-memory reads are 512

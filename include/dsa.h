@@ -221,7 +221,16 @@ dsa_status dsa_sparse_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* 
 /* Steps 1-4 for one decode token per sequence, in one call: scores (written to
  * `scores`, [batch][ld]), top-k (idx, n_sel) and attention (out, lse), with the
  * score histogram built while scoring.  Same argument rules as the single steps
- * (num_q_heads <= 64, group <= 16). */
+ * (num_q_heads <= 64, group <= 16).
+ * Overlap with the previous kernel: the kernels are launched with programmatic
+ * dependent launch, and the first one (the scoring, as in dsa_index_scores in
+ * decode mode) reads context_lens, block_table and the indexer cache rows other
+ * than each sequence's newest position before it waits for the previous kernel
+ * of the stream to finish.  These inputs must therefore be complete before that
+ * kernel starts: written by host copies, by kernels launched without early
+ * completion (every kernel not launched with programmatic dependent launch, and
+ * dsa_kv_write), or earlier.  Everything else (the newest token's cache rows,
+ * q, q_idx, the workspace and the outputs) is touched only after the wait. */
 dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* q_idx,
                            int32_t num_q_heads, int32_t prefix_len, int32_t k,
                            float softmax_scale, int32_t* scores, int32_t ld, int32_t* idx,
