@@ -344,9 +344,16 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
     out = torch.empty((T, hq, 128), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, hq), dtype=torch.float32, device=dev)
     ws = dsa.make_workspace(dsa.workspace_size(dsa.OP_PREFILL_STEP, kv, qs, k, hq, P), dev)
+    n_dense = dsa.prefill_dense_queries(kv, qs, k, hq, P)
+    ws_gather = dsa.make_workspace(dsa.prefill_attn_workspace_size(kv, qs, k, hq, P, 0), dev)
+    out_g = torch.empty_like(out)
     calls = {"index": lambda: dsa.index_scores(kv, qs, w["q_idx"], P, scores),
              "topk": lambda: dsa.topk_select(kv, qs, scores, P, k, idx, n_sel, ws),
-             "attention": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws)}
+             "attention": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws),
+             # the same attention with every query gathered (the path the automatic split
+             # keeps for positions past its range), for comparison; not part of the chunk
+             "attention_gather_only": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out_g,
+                                                                      None, ws_gather, n_dense=0)}
     st = torch.cuda.current_stream(dev)
     for _ in range(max(1, warmup)):
         for f in calls.values():
@@ -366,7 +373,7 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
         ms[name] = a.elapsed_time(b) / steps
     clock_info = clocks.stop()
     assert dsa.check_device_status(dev) == 0
-    total = sum(ms.values())
+    total = ms["index"] + ms["topk"] + ms["attention"]
     pos = np.arange(T)
     causal_pairs = int(np.maximum(0, pos + 1 - P).sum())          # scored (query, key) pairs
     n_sel_h = n_sel.cpu().numpy().astype(np.int64)
@@ -382,7 +389,20 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
     idx_bytes = 4 * causal_pairs + T * 64 + (T * 64) * ((T + 127) // 128) // 2
     peak_hbm, peak_kind = measured_peaks()
     idx_gbs = idx_bytes / (ms["index"] * 1e-3) / 1e9
-    attn_gbs = gathered / (ms["attention"] * 1e-3) / 1e9
+    gather_gbs = gathered / (ms["attention_gather_only"] * 1e-3) / 1e9
+    # Tensor work of the dense masked pass as it runs: per KV head and pair of
+    # query tiles (2 x floor(128 / G) queries), every 64-position block up to the
+    # pair's last position, per tile S = Q K^T (128 x 64 x 128) and O += P V with
+    # P as hi + lo (two 128 x 128 x 64 products): 3 x 2 x 128 x 64 x 128 flops.
+    G = hq // hkv
+    qt = 128 // G
+    dense_flops = 0
+    for q0 in range(0, n_dense, 2 * qt):
+        last = min(q0 + 2 * qt, n_dense) - 1
+        dense_flops += ((last // 64) + 1) * 2 * 3 * 2 * 128 * 64 * 128 * hkv
+    dense_tflops = dense_flops / (ms["attention"] * 1e-3) / 1e12 if n_dense == T else None
+    attended = int(n_sel_h.sum()) + int(np.minimum(pos + 1, P).sum())
+    useful_flops = 4 * attended * 128 * hq                           # Q.K and P.V over the attended rows
     # oracle on sampled rows of the chunk (rows drawn uniformly, seeded)
     cpu = None
     if cpu_seconds > 0:
@@ -406,12 +426,20 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
                     "tensor_peaks_tops": {"tcgen05_e4m3": f8, "tcgen05_f16": f16, "mma_sync_s8": s8},
                     "tensor_frac": {"tcgen05_e4m3": idx_tops / f8, "mma_sync_s8": idx_tops / s8},
                     "peak_note": "tensor peaks measured in this run by libdsa_probe.so microbenchmarks"},
-        "attention": {"kernel": "dsa_sparse_attn_prefill per call: prefix_attn_kernel + sparse_attn_kernel + "
-                                "attn_combine_kernel", "bound": "l2",
-                      "achieved": attn_gbs, "peak": gather, "unit": "GB/s", "frac": attn_gbs / gather,
-                      "bytes": gathered,
-                      "peak_kind": f"measured in this run: random {hkv * 256}-byte bulk copies from an L2-resident "
-                                   f"32 MB buffer into shared memory (libdsa_probe.so)"},
+        "attention": {"kernel": "dsa_sparse_attn_prefill per call: dense_mask_kernel + dense_attn_kernel "
+                                "(masked dense pass on tcgen05.mma kind::f16, bf16 operands, fp32 in tensor "
+                                f"memory) for the first {n_dense} of {T} queries (automatic split)",
+                      "bound": "tensor", "achieved": dense_tflops, "peak": f16, "unit": "TFLOP/s",
+                      "frac": dense_tflops / f16 if dense_tflops else None, "flops": dense_flops,
+                      "attended_flops": useful_flops, "dense_queries": n_dense,
+                      "peak_kind": "measured in this run: back-to-back tcgen05.mma kind::f16 128 x 256 tiles "
+                                   "(libdsa_probe.so); bf16 runs at the f16 rate"},
+        "attention_gather_only": {"kernel": "prefix_attn_kernel + sparse_attn_kernel + attn_combine_kernel, every "
+                                            "query's attended rows gathered from L2", "ms": ms["attention_gather_only"],
+                                  "bound": "l2", "achieved": gather_gbs, "peak": gather, "unit": "GB/s",
+                                  "frac": gather_gbs / gather, "bytes": gathered,
+                                  "peak_kind": f"measured in this run: random {hkv * 256}-byte bulk copies from an "
+                                               f"L2-resident 32 MB buffer into shared memory (libdsa_probe.so)"},
         "mma_sync_bf16_peak_tflops": bf16,
         "clocks": clock_info,
         "cpu_baseline": cpu,

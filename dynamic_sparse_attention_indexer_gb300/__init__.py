@@ -151,12 +151,28 @@ def sparse_attn_decode(kv: PagedKV, q, idx, n_sel, k: int, prefix_len: int, out,
 
 
 def sparse_attn_prefill(kv: PagedKV, qs, q, idx, n_sel, k: int, prefix_len: int, out, lse=None, ws=None,
-                        softmax_scale: float | None = None):
+                        softmax_scale: float | None = None, n_dense: int | None = None):
+    """Prefill attention.  n_dense: queries [0, n_dense) by the dense masked
+    pass, the rest gathered; None takes the library's automatic split."""
     scale = 1.0 / math.sqrt(HEAD_DIM) if softmax_scale is None else softmax_scale
     p, n = _ws(ws)
-    _check(lib().dsa_sparse_attn_prefill(kv.ref, C.byref(qs), _ptr(q), int(q.shape[1]), _ptr(idx), _ptr(n_sel), k,
-                                         prefix_len, scale, _ptr(out), _out_dtype(out), _ptr(lse), p, n,
-                                         _stream(q.device)))
+    if n_dense is None:
+        _check(lib().dsa_sparse_attn_prefill(kv.ref, C.byref(qs), _ptr(q), int(q.shape[1]), _ptr(idx), _ptr(n_sel),
+                                             k, prefix_len, scale, _ptr(out), _out_dtype(out), _ptr(lse), p, n,
+                                             _stream(q.device)))
+    else:
+        _check(lib().dsa_sparse_attn_prefill_split(kv.ref, C.byref(qs), _ptr(q), int(q.shape[1]), _ptr(idx),
+                                                   _ptr(n_sel), k, prefix_len, scale, int(n_dense), _ptr(out),
+                                                   _out_dtype(out), _ptr(lse), p, n, _stream(q.device)))
+
+
+def prefill_dense_queries(kv: PagedKV, qs, k: int, num_q_heads: int, prefix_len: int) -> int:
+    """The automatic split: how many leading queries of qs go to the dense pass."""
+    return int(lib().dsa_prefill_dense_queries(kv.ref, C.byref(qs), k, num_q_heads, prefix_len))
+
+
+def prefill_attn_workspace_size(kv: PagedKV, qs, k: int, num_q_heads: int, prefix_len: int, n_dense: int) -> int:
+    return int(lib().dsa_prefill_attn_workspace_size(kv.ref, C.byref(qs), k, num_q_heads, prefix_len, n_dense))
 
 
 def decode_step(kv: PagedKV, q, q_idx, prefix_len: int, k: int, scores, idx, n_sel, out, lse=None, ws=None,

@@ -48,6 +48,7 @@ dsa_status ensure_setup() {
   if ((e = dsa::setup_topk_kernels()) != cudaSuccess) return cuda_fail("setup (top-k kernels)", e);
   if ((e = dsa::setup_attn_kernels()) != cudaSuccess) return cuda_fail("setup (attention kernels)", e);
   if ((e = dsa::setup_prefix_kernels()) != cudaSuccess) return cuda_fail("setup (prefix kernel)", e);
+  if ((e = dsa::setup_dense_kernels()) != cudaSuccess) return cuda_fail("setup (dense prefill kernel)", e);
   done[dev] = true;
   return DSA_OK;
 }
@@ -235,9 +236,46 @@ dsa_status check_heads(int32_t hq, const dsa::KV& kv) {
     if (e_ != cudaSuccess) return cuda_fail(where, e_); \
   } while (0)
 
+// Prefill attention runs its first n_dense queries as a masked dense pass over
+// every causal position (k_dense.cu) and the rest by gathering their attended
+// rows (k_prefix.cu + k_attn.cu).  Per (query, head) row and position the dense
+// pass costs about 1/kDenseRatio of a gathered row on GB300, and a query at
+// position pos attends min(P, pos + 1) + min(k, pos + 1 - P) rows out of
+// pos + 1, so the dense pass is the cheaper one while
+//   pos + 1 <= kDenseRatio * (P + k)   (always when pos < P + k).
+// The split falls on a whole dense tile pair unless every query goes dense.
+constexpr int64_t kDenseRatio = 12;
+
+struct PrefillPlan {
+  int n_dense = 0;       // queries [0, n_dense) dense
+  size_t mask = 0;       // bytes of the dense pass's bitmap (workspace offset 0)
+  dsa::QS rest{};        // the gathered queries
+  Layout L;              // their workspace, at offset `mask`
+  size_t total = 0;
+};
+
+int auto_dense_queries(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_t hq, int32_t prefix) {
+  const int64_t lim = kDenseRatio * ((int64_t)prefix + k) - qs.pos0;
+  if (lim <= 0) return 0;
+  if (lim >= qs.n_q) return qs.n_q;
+  const int pair = 2 * dsa::dense_tile_queries(hq / kv.hkv);
+  return (int)(lim / pair * pair);
+}
+
+PrefillPlan prefill_plan(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_t hq, int32_t prefix, int n_dense) {
+  PrefillPlan pl;
+  pl.n_dense = n_dense;
+  pl.mask = up256(dsa::dense_mask_bytes(qs, n_dense));
+  pl.rest = dsa::QS{qs.mode, qs.n_q - n_dense, qs.seq, qs.pos0 + n_dense};
+  if (pl.rest.n_q > 0) pl.L = layout(kv, pl.rest, k, hq, prefix);
+  pl.total = pl.mask + pl.L.total;
+  return pl;
+}
+
 dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const void* q, int32_t hq,
                      const int32_t* idx, const int32_t* n_sel, int32_t k, int32_t prefix, float scale, void* out,
-                     int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                     int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream,
+                     int32_t n_dense = -1) {
   dsa::KV kv{};
   dsa::QS qs{};
   DSA_TRY(check_kv(kv_, &kv));
@@ -251,6 +289,40 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
   if (out_dtype != DSA_OUT_BF16 && out_dtype != DSA_OUT_F32)
     return fail(DSA_ERR_INVALID_ARG, "out_dtype %d is neither DSA_OUT_BF16 nor DSA_OUT_F32", out_dtype);
   if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (qs.mode == DSA_MODE_PREFILL) {
+    if (n_dense < -1 || n_dense > qs.n_q)
+      return fail(DSA_ERR_INVALID_ARG, "n_dense (%d) must be -1 (automatic) or in [0, n_q]", n_dense);
+    if (n_dense < 0) n_dense = auto_dense_queries(kv, qs, k, hq, prefix);
+    const PrefillPlan pl = prefill_plan(kv, qs, k, hq, prefix, n_dense);
+    DSA_TRY(check_ws(ws, ws_bytes, pl.total));
+    DSA_TRY(ensure_setup());
+    dsa::AttnArgs a;
+    a.kv = kv;
+    a.qs = qs;
+    a.q = q;
+    a.hq = hq;
+    a.idx = idx;
+    a.n_sel = n_sel;
+    a.slot = nullptr;
+    a.k = k;
+    a.prefix = prefix;
+    a.scale = scale;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse = lse;
+    if (pl.n_dense > 0) DSA_CUDA("dense prefill attention launch", dsa::launch_dense_attn(a, pl.n_dense, ws, stream));
+    if (pl.rest.n_q == 0) return DSA_OK;
+    const size_t nd = (size_t)pl.n_dense, row = (size_t)hq * 128;
+    a.qs = pl.rest;
+    a.q = static_cast<const char*>(q) + nd * row * 2;
+    a.idx = idx + nd * (size_t)k;
+    a.n_sel = n_sel + nd;
+    a.out = static_cast<char*>(out) + nd * row * (out_dtype == DSA_OUT_F32 ? 4 : 2);
+    a.lse = lse ? lse + nd * (size_t)hq : nullptr;
+    a.ws = attn_ws(pl.L, static_cast<char*>(ws) + pl.mask);
+    DSA_CUDA("sparse attention launch", dsa::launch_sparse_attn(a, stream));
+    return DSA_OK;
+  }
   const Layout L = layout(kv, qs, k, hq, prefix);
   DSA_TRY(check_ws(ws, ws_bytes, L.total));
   DSA_TRY(ensure_setup());
@@ -339,6 +411,7 @@ dsa_status dsa_check_device_status(cudaStream_t stream, int32_t* code) {
   DSA_CUDA("status (attention)", dsa::read_clear_status_attn(&c, stream));
   DSA_CUDA("status (prefix attention)", dsa::read_clear_status_prefix(&c, stream));
   DSA_CUDA("status (cache)", dsa::read_clear_status_misc(&c, stream));
+  DSA_CUDA("status (dense prefill attention)", dsa::read_clear_status_dense(&c, stream));
   *code = c;
   return DSA_OK;
 }
@@ -351,6 +424,8 @@ size_t dsa_workspace_size(int32_t op, const dsa_paged_kv* kv_, const dsa_query_s
   if (op == DSA_OP_INDEX_SCORES) return 0;
   if (check_k_prefix(k, prefix) != DSA_OK || check_heads(hq, kv) != DSA_OK) return 0;
   const Layout L = layout(kv, qs, k, hq, prefix);
+  if (qs.mode == DSA_MODE_PREFILL && (op == DSA_OP_SPARSE_ATTN || op == DSA_OP_PREFILL_STEP))
+    return prefill_plan(kv, qs, k, hq, prefix, auto_dense_queries(kv, qs, k, hq, prefix)).total;
   switch (op) {
     case DSA_OP_TOPK_SELECT: return L.sel_end;
     case DSA_OP_SPARSE_ATTN:
@@ -454,6 +529,42 @@ dsa_status dsa_sparse_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* 
   if (qs && qs->mode != DSA_MODE_PREFILL)
     return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_prefill needs a DSA_MODE_PREFILL query set");
   return attn_impl(kv, qs, q, hq, idx, n_sel, k, prefix, scale, out, out_dtype, lse, ws, ws_bytes, stream);
+}
+
+dsa_status dsa_sparse_attn_prefill_split(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q,
+                                         int32_t hq, const int32_t* idx, const int32_t* n_sel, int32_t k,
+                                         int32_t prefix, float scale, int32_t n_dense, void* out, int32_t out_dtype,
+                                         float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (qs && qs->mode != DSA_MODE_PREFILL)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_sparse_attn_prefill_split needs a DSA_MODE_PREFILL query set");
+  return attn_impl(kv, qs, q, hq, idx, n_sel, k, prefix, scale, out, out_dtype, lse, ws, ws_bytes, stream, n_dense);
+}
+
+int32_t dsa_prefill_dense_queries(const dsa_paged_kv* kv_, const dsa_query_set* qs_, int32_t k, int32_t hq,
+                                  int32_t prefix) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  if (check_kv(kv_, &kv) != DSA_OK || check_qs(qs_, kv, &qs) != DSA_OK || qs.mode != DSA_MODE_PREFILL) return -1;
+  if (check_k_prefix(k, prefix) != DSA_OK || check_heads(hq, kv) != DSA_OK) return -1;
+  return auto_dense_queries(kv, qs, k, hq, prefix);
+}
+
+size_t dsa_prefill_attn_workspace_size(const dsa_paged_kv* kv_, const dsa_query_set* qs_, int32_t k, int32_t hq,
+                                       int32_t prefix, int32_t n_dense) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  if (check_kv(kv_, &kv) != DSA_OK || check_qs(qs_, kv, &qs) != DSA_OK) return 0;
+  if (qs.mode != DSA_MODE_PREFILL) {
+    fail(DSA_ERR_INVALID_ARG, "dsa_prefill_attn_workspace_size needs a DSA_MODE_PREFILL query set");
+    return 0;
+  }
+  if (check_k_prefix(k, prefix) != DSA_OK || check_heads(hq, kv) != DSA_OK) return 0;
+  if (n_dense < -1 || n_dense > qs.n_q) {
+    fail(DSA_ERR_INVALID_ARG, "n_dense (%d) must be -1 (automatic) or in [0, n_q = %d]", n_dense, qs.n_q);
+    return 0;
+  }
+  if (n_dense < 0) n_dense = auto_dense_queries(kv, qs, k, hq, prefix);
+  return prefill_plan(kv, qs, k, hq, prefix, n_dense).total;
 }
 
 dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t* q_idx, int32_t hq, int32_t prefix,

@@ -77,6 +77,11 @@ cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_prefix_attn(const KV& kv, const QS& qs, const void* q, int hq, int prefix, float scale,
                                float2* pre_ml, float* pre_o, cudaStream_t st);
+// Prefill attention of the first n_dense queries of the set as a masked dense
+// pass on tcgen05 (k_dense.cu); mask_ws holds dense_mask_bytes(qs, n_dense).
+cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st);
+size_t dense_mask_bytes(const QS& qs, int n_dense);
+int dense_tile_queries(int group);
 cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
                             const int8_t* idx_k, cudaStream_t st);
 cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, const int32_t* n_sel, int k,
@@ -87,6 +92,7 @@ cudaError_t setup_index_kernels();
 cudaError_t setup_topk_kernels();
 cudaError_t setup_attn_kernels();
 cudaError_t setup_prefix_kernels();
+cudaError_t setup_dense_kernels();
 
 // Device status words, one per kernel file: each reads its word into *code
 // (if *code is still 0) and clears it.
@@ -95,6 +101,7 @@ cudaError_t read_clear_status_topk(int* code, cudaStream_t st);
 cudaError_t read_clear_status_attn(int* code, cudaStream_t st);
 cudaError_t read_clear_status_prefix(int* code, cudaStream_t st);
 cudaError_t read_clear_status_misc(int* code, cudaStream_t st);
+cudaError_t read_clear_status_dense(int* code, cudaStream_t st);
 
 // Used by the allocation-free top-k entry point (defined in api.cpp).
 dsa_status prepare_decode_topk(const dsa_paged_kv* kv, const int32_t* scores, int32_t ld, int32_t prefix,

@@ -206,16 +206,46 @@ dsa_status dsa_sparse_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t
                                   int32_t prefix_len, float softmax_scale, void* out,
                                   int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
                                   cudaStream_t stream);
-/* Prefill form: the queries of `qs` (mode DSA_MODE_PREFILL).  With a prefix
- * the prefix part of every query is computed first, once per tile of 128
- * (query, head) rows (§2.4: the prefix is attended in full by every query),
- * and the selected rows are then added to it; the workspace holds those
- * partial states (see dsa_workspace_size). */
+/* Prefill form: the queries of `qs` (mode DSA_MODE_PREFILL), in two parts
+ * (§2.3: selection, gather and attention fused per prefill chunk):
+ *   - the first n_dense queries (those at positions below about
+ *     12 * (prefix_len + k), where the attended set is a large share of the causal
+ *     range; see dsa_prefill_dense_queries) as a masked dense pass on the tensor
+ *     cores: every causal position of a tile of queries is read once per tile
+ *     and weighted zero unless it is in the query's attended set.  This part
+ *     reads the K and V rows of every position up to the tile's last one, so
+ *     those rows must hold finite values (any written cache row does); a
+ *     selected position outside [0, pos_i] is left out and sets
+ *     DSA_ERR_BAD_BLOCK_TABLE on the device;
+ *   - the others by gathering their attended rows: with a prefix, the prefix
+ *     part of every query first, once per tile of 128 (query, head) rows (§2.4:
+ *     the prefix is attended in full by every query), then the selected rows
+ *     added to it.
+ * The workspace holds the dense part's attended-position bitmap (8 bytes per
+ * query and 64 positions) and the gathered part's partial states (see
+ * dsa_workspace_size, which sizes the automatic split). */
 dsa_status dsa_sparse_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q,
                                    int32_t num_q_heads, const int32_t* idx, const int32_t* n_sel,
                                    int32_t k, int32_t prefix_len, float softmax_scale, void* out,
                                    int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
                                    cudaStream_t stream);
+/* The same with the split given: queries [0, n_dense) by the dense pass, the
+ * rest by the gather (n_dense = 0: all gathered; n_dense = n_q: all dense;
+ * -1: the automatic split).  The workspace must hold
+ * dsa_prefill_attn_workspace_size(..., n_dense) bytes. */
+dsa_status dsa_sparse_attn_prefill_split(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q,
+                                         int32_t num_q_heads, const int32_t* idx, const int32_t* n_sel,
+                                         int32_t k, int32_t prefix_len, float softmax_scale,
+                                         int32_t n_dense, void* out, int32_t out_dtype, float* lse,
+                                         void* ws, size_t ws_bytes, cudaStream_t stream);
+/* The automatic split of dsa_sparse_attn_prefill: the number of leading queries
+ * of `qs` it runs as the dense pass (-1 on invalid arguments). */
+int32_t dsa_prefill_dense_queries(const dsa_paged_kv* kv, const dsa_query_set* qs, int32_t k,
+                                  int32_t num_q_heads, int32_t prefix_len);
+/* Workspace bytes of dsa_sparse_attn_prefill_split with this n_dense (-1: the
+ * automatic split; 0 on invalid arguments). */
+size_t dsa_prefill_attn_workspace_size(const dsa_paged_kv* kv, const dsa_query_set* qs, int32_t k,
+                                       int32_t num_q_heads, int32_t prefix_len, int32_t n_dense);
 
 /* ---------------------------------------------------- fused decode step --- */
 /* Steps 1-4 for one decode token per sequence, in one call: scores (written to

@@ -152,9 +152,11 @@ def oracle_indices_all(w: dict, k: int, P: int, rows=None):
     return res
 
 
-def run_prefill(w: dict, out_dtype=torch.bfloat16) -> dict:
+def run_prefill(w: dict, out_dtype=torch.bfloat16, n_dense=None) -> dict:
     """index_scores -> topk_select -> sparse_attn_prefill for the queries of
-    sequence w["seq"] at positions pos0 .. pos0 + T - 1."""
+    sequence w["seq"] at positions pos0 .. pos0 + T - 1.  n_dense: queries
+    [0, n_dense) by the dense masked pass, the rest gathered (None: the
+    library's automatic split)."""
     dev = w["q"].device
     kv = paged_kv(w)
     T, k, P, hq = int(w["num_queries"]), int(w["k"]), int(w["prefix_len"]), int(w["num_q_heads"])
@@ -165,10 +167,14 @@ def run_prefill(w: dict, out_dtype=torch.bfloat16) -> dict:
     n_sel = torch.empty(T, dtype=torch.int32, device=dev)
     out = torch.empty((T, hq, 128), dtype=out_dtype, device=dev)
     lse = torch.empty((T, hq), dtype=torch.float32, device=dev)
-    ws = dsa.make_workspace(dsa.workspace_size(dsa.OP_PREFILL_STEP, kv, qs, k, hq, P), dev)
+    if n_dense is None:
+        nbytes = dsa.workspace_size(dsa.OP_PREFILL_STEP, kv, qs, k, hq, P)
+    else:
+        nbytes = dsa.prefill_attn_workspace_size(kv, qs, k, hq, P, n_dense)
+    ws = dsa.make_workspace(nbytes, dev)
     dsa.index_scores(kv, qs, w["q_idx"], P, scores)
     dsa.topk_select(kv, qs, scores, P, k, idx, n_sel, ws)
-    dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws)
+    dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out, lse, ws, n_dense=n_dense)
     status = dsa.check_device_status(dev)
     assert status == 0, f"device status {status}"
     return {"scores": scores, "idx": idx, "n_sel": n_sel, "out": out, "lse": lse}

@@ -153,6 +153,12 @@ def test_argument_checks(lib):
     # workspace check, which a tiny workspace fails)
     assert lib.dsa_sparse_attn_decode(C.byref(kv8), 0x60000, 64, 0x80000, 0x90000, 8, 0, 0.1, 0xB0000, 0, None,
                                       0xA0000, 16, None) == WORKSPACE
+    # the split form: n_dense outside [-1, n_q]
+    qs10 = _qs(1, 10, 0, 0)
+    for n in (-2, 11):
+        assert lib.dsa_sparse_attn_prefill_split(C.byref(kv), C.byref(qs10), 0x60000, 8, 0x80000, 0x90000, 8, 0,
+                                                 0.1, n, 0xB0000, 0, None, 0xA0000, 1 << 30, None) == INVALID
+    assert lib.dsa_prefill_dense_queries(C.byref(kv), C.byref(qs), 8, 8, 0) == -1   # a decode query set
     # prefill attention refuses a decode query set
     assert lib.dsa_sparse_attn_prefill(C.byref(kv), C.byref(qs), 0x60000, 8, 0x80000, 0x90000, 8, 0, 0.1,
                                        0xB0000, 0, None, None, 0, None) == INVALID
@@ -187,13 +193,29 @@ def test_workspace_sizes(lib):
     s3 = lib.dsa_workspace_size(3, C.byref(kv3), C.byref(qs3), 2048, 64, 1024)
     assert 8 * 2048 * 4 <= s3 < 64 << 20      # selected slots + attention partials, well under 64 MB
     assert lib.dsa_workspace_size(3, C.byref(kv3), C.byref(qs3), 0, 64, 1024) == 0   # invalid k
-    # prefill with a prefix holds the prefix part of every (query, head): 520 B each
+    # the 16K prefill chunk: the automatic split sends every query to the dense
+    # pass, whose workspace is the attended-position bitmap (8 B per query and
+    # 64 positions), prefix or not
     kv4 = _kv(num_blocks=256, num_kv_heads=4, max_blocks_per_seq=256, batch=1, max_context_len=16384)
     qs4 = _qs(1, 16384, 0, 0)
-    with_prefix = lib.dsa_workspace_size(4, C.byref(kv4), C.byref(qs4), 2048, 32, 576)
-    without = lib.dsa_workspace_size(4, C.byref(kv4), C.byref(qs4), 2048, 32, 0)
-    assert with_prefix - without >= 16384 * 32 * 520
-    assert without < 16 << 20                 # no per-query selection state in prefill
+    assert lib.dsa_prefill_dense_queries(C.byref(kv4), C.byref(qs4), 2048, 32, 576) == 16384
+    bitmap = 16384 * 256 * 8
+    assert lib.dsa_workspace_size(4, C.byref(kv4), C.byref(qs4), 2048, 32, 576) == bitmap
+    assert lib.dsa_workspace_size(4, C.byref(kv4), C.byref(qs4), 2048, 32, 0) == bitmap
+    wsz = lambda p, n: lib.dsa_prefill_attn_workspace_size(C.byref(kv4), C.byref(qs4), 2048, 32, p, n)
+    assert wsz(576, -1) == bitmap
+    # every query gathered: with a prefix the prefix part of every (query, head), 520 B each
+    assert wsz(576, 0) - wsz(0, 0) >= 16384 * 32 * 520
+    assert wsz(0, 0) < 16 << 20                # no per-query selection state in prefill
+    # a split: the bitmap of the dense queries plus the gathered part's state
+    assert wsz(576, 8192) >= 8192 * 128 * 8 + 8192 * 32 * 520
+    assert wsz(576, 16385) == 0                # more dense queries than the set has
+    # deep into a long sequence the automatic split gathers everything
+    kv5 = _kv(num_blocks=4096, num_kv_heads=4, max_blocks_per_seq=4096, batch=1, max_context_len=262144)
+    assert lib.dsa_prefill_dense_queries(C.byref(kv5), C.byref(_qs(1, 4096, 0, 200000)), 2048, 32, 576) == 0
+    # and near its start takes a whole number of dense tile pairs (2 x 16 queries at group 8)
+    n = lib.dsa_prefill_dense_queries(C.byref(kv5), C.byref(_qs(1, 4096, 0, 30000)), 2048, 32, 576)
+    assert n == (12 * (576 + 2048) - 30000) // 32 * 32
 
 
 def test_no_alloc_topk_refuses_batches_beyond_the_static_scratch(lib):

@@ -19,23 +19,35 @@ def _prefill_spec(T, pos0=0, P=64, k=100, hq=8, hkv=2, batch_lens=None, seq=0, *
                       pos0=pos0, **kw)
 
 
-def _run(spec, seed=5, seq=0, out_dtype=torch.bfloat16):
+# How the attention splits the chunk: the library's automatic split (every
+# query of these small chunks goes to the dense masked pass), every query
+# gathered, and a split inside a dense tile pair (both parts in one call).
+SPLITS = ["auto", "gather", "split"]
+
+
+def _n_dense(split, T):
+    return {"auto": None, "gather": 0, "split": T // 2 + 1}[split]
+
+
+def _run(spec, seed=5, seq=0, out_dtype=torch.bfloat16, split="auto"):
     w_cpu = synth.make_workload(spec, seed, "cpu")
     w_cpu["seq"] = seq
     w = H.on(w_cpu, DEV)
-    res = H.run_prefill(w, out_dtype=out_dtype)
+    res = H.run_prefill(w, out_dtype=out_dtype, n_dense=_n_dense(split, spec.num_queries))
     H.check_prefill_against_oracle(synth.to_numpy(w_cpu), res)
     return res
 
 
-def test_prefill_small_from_position_zero(lib):
+@pytest.mark.parametrize("split", SPLITS)
+def test_prefill_small_from_position_zero(lib, split):
     """Queries inside the prefix, at its edge, and with fewer / more than k candidates."""
-    _run(_prefill_spec(T=400, pos0=0, P=64, k=100))
+    _run(_prefill_spec(T=400, pos0=0, P=64, k=100), split=split)
 
 
-def test_prefill_continuation_chunk(lib):
+@pytest.mark.parametrize("split", SPLITS)
+def test_prefill_continuation_chunk(lib, split):
     """A chunk of queries that starts deep into the sequence (pos0 > 0)."""
-    _run(_prefill_spec(T=200, pos0=1000, P=100, k=256, hq=16, hkv=2))
+    _run(_prefill_spec(T=200, pos0=1000, P=100, k=256, hq=16, hkv=2), split=split)
 
 
 def test_prefill_second_sequence_of_the_table(lib):
@@ -43,28 +55,89 @@ def test_prefill_second_sequence_of_the_table(lib):
     _run(spec, seq=1)
 
 
-def test_prefill_group_16_and_fp32(lib):
-    _run(_prefill_spec(T=130, pos0=200, P=32, k=50, hq=32, hkv=2), out_dtype=torch.float32)
+@pytest.mark.parametrize("split", SPLITS)
+def test_prefill_group_16_and_fp32(lib, split):
+    _run(_prefill_spec(T=130, pos0=200, P=32, k=50, hq=32, hkv=2), out_dtype=torch.float32, split=split)
 
 
 def test_prefill_full_int8_range(lib):
     _run(_prefill_spec(T=150, pos0=300, P=64, k=90, idx_lo=-128, idx_hi=127))
 
 
-def test_prefill_separate_kv_arrays(lib):
+@pytest.mark.parametrize("split", SPLITS)
+def test_prefill_separate_kv_arrays(lib, split):
     """The same path with K and V in two arrays (two copies per attended row)."""
-    _run(_prefill_spec(T=200, pos0=100, P=64, k=100, hq=16, hkv=4, kv_layout="separate"))
+    _run(_prefill_spec(T=200, pos0=100, P=64, k=100, hq=16, hkv=4, kv_layout="separate"), split=split)
 
 
-def test_prefill_prefix_tiles_ragged(lib):
-    """The prefix part is computed per tile of queries: a group of 3 heads (42
-    queries per 128-row tile, two rows unused), a prefix of 130 (three 64-key
-    chunks, the last with 2 keys) and queries before, inside and past it."""
-    _run(_prefill_spec(T=300, pos0=10, P=130, k=80, hq=24, hkv=8))
+@pytest.mark.parametrize("split", SPLITS)
+def test_prefill_prefix_tiles_ragged(lib, split):
+    """Tiles of a group of 3 heads (42 queries per 128-row tile, two rows
+    unused), a prefix of 130 (three 64-key chunks, the last with 2 keys) and
+    queries before, inside and past it."""
+    _run(_prefill_spec(T=300, pos0=10, P=130, k=80, hq=24, hkv=8), split=split)
 
 
-def test_prefill_without_prefix(lib):
-    _run(_prefill_spec(T=100, pos0=0, P=0, k=40))
+@pytest.mark.parametrize("split", SPLITS)
+def test_prefill_without_prefix(lib, split):
+    _run(_prefill_spec(T=100, pos0=0, P=0, k=40), split=split)
+
+
+def test_prefill_group_1(lib):
+    """One query head per KV head: 128 queries per dense tile."""
+    _run(_prefill_spec(T=300, pos0=40, P=20, k=60, hq=4, hkv=4))
+
+
+def test_prefill_automatic_split_at_the_crossover(lib):
+    """A chunk whose later queries lie past the dense pass's range: the
+    automatic split runs a whole number of dense tile pairs and gathers the rest."""
+    spec = _prefill_spec(T=400, pos0=300, P=16, k=24)
+    w_cpu = synth.make_workload(spec, 5, "cpu")
+    w_cpu["seq"] = 0
+    w = H.on(w_cpu, DEV)
+    kv = H.paged_kv(w)
+    qs = H.dsa.query_set(H.dsa.MODE_PREFILL, spec.num_queries, 0, spec.pos0)
+    n = H.dsa.prefill_dense_queries(kv, qs, spec.k, spec.num_q_heads, spec.prefix_len)
+    pair = 2 * (128 // (spec.num_q_heads // spec.num_kv_heads))
+    lim = 12 * (spec.prefix_len + spec.k) - spec.pos0
+    assert 0 < n < spec.num_queries and n % pair == 0 and n <= lim < n + pair
+    res = H.run_prefill(w)
+    H.check_prefill_against_oracle(synth.to_numpy(w_cpu), res)
+
+
+def test_prefill_dense_ignores_unwritten_slots(lib):
+    """Slots of the last block past the chunk's last position hold NaN (never
+    written): the dense pass reads them with its 64-position blocks but gives
+    them zero weight, so every output stays finite and matches the oracle."""
+    spec = _prefill_spec(T=100, pos0=37, P=16, k=40)
+    w_cpu = synth.make_workload(spec, 5, "cpu")
+    w_cpu["seq"] = 0
+    last = spec.pos0 + spec.num_queries - 1
+    blk = int(w_cpu["block_table"][0, last // 64])
+    w_cpu["kv"][blk, last % 64 + 1:] = float("nan")  # [block][row][K/V][head][128]
+    w = H.on(w_cpu, DEV)
+    res = H.run_prefill(w, n_dense=spec.num_queries)
+    assert torch.isfinite(res["out"].float()).all() and torch.isfinite(res["lse"]).all()
+    H.check_prefill_against_oracle(synth.to_numpy(w_cpu), res)
+
+
+def test_prefill_dense_bad_selected_position_sets_status(lib):
+    """A selected position past the query's own one is left out by the dense
+    pass and reported through the status word, without a fault."""
+    spec = _prefill_spec(T=64, pos0=100, P=16, k=40)
+    w = H.on(synth.make_workload(spec, 5, "cpu") | {"seq": 0}, DEV)
+    res = H.run_prefill(w, n_dense=spec.num_queries)
+    kv = H.paged_kv(w)
+    qs = H.dsa.query_set(H.dsa.MODE_PREFILL, spec.num_queries, 0, spec.pos0)
+    idx = res["idx"].clone()
+    idx[3, 0] = spec.pos0 + 3 + 5
+    ws = H.dsa.make_workspace(H.dsa.prefill_attn_workspace_size(kv, qs, spec.k, spec.num_q_heads,
+                                                                  spec.prefix_len, spec.num_queries), DEV)
+    out = torch.empty_like(res["out"])
+    H.dsa.sparse_attn_prefill(kv, qs, w["q"], idx, res["n_sel"], spec.k, spec.prefix_len, out, None, ws,
+                              n_dense=spec.num_queries)
+    assert H.dsa.check_device_status() == 4
+    assert H.dsa.check_device_status() == 0
 
 
 def test_full_prefill_16k(lib):
