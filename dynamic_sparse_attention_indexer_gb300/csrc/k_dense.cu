@@ -18,26 +18,31 @@
 // bitmap, word [c][i] holding positions 64c .. 64c + 63 of dense query i.
 //
 // dense_attn_kernel, one CTA per (KV head, two tiles of QT = floor(128 / G)
-// queries), heaviest (latest) tiles first, 320 threads:
-//   warp 8       producer: TMA loads of the two Q tiles (once), then per chunk
-//                of 64 positions the K block of the KV head (two 8 KB boxes,
-//                128-byte swizzle) with the tiles' mask words into a 3-stage
-//                ring, and its V block into a 2-stage ring (K is released as
-//                soon as S is computed, V only after P V);
-//   warp 9       one thread issues the MMAs: S_t(j) = Q_t K(j)^T into one of two
-//                64-column TMEM buffers per tile, then
-//                O_t += P_t(j - 1) V(j - 1) with P as two bf16 terms, hi and the
-//                residual lo (V as an MN-major operand), each group committed to
-//                an mbarrier;
+// queries), heaviest (latest) tiles first, 352 threads:
+//   warp 8       K producer: TMA loads of the two Q tiles (once), then per
+//                chunk of 64 positions the K block of the KV head (two 8 KB
+//                boxes, 128-byte swizzle) with the tiles' mask words into a
+//                4-stage ring, released as soon as S is computed;
+//   warp 10      V producer: the chunk's V block into a 3-stage ring, released
+//                after P V.  Separate issuers keep the K loads several chunks
+//                ahead of their use;
+//   warp 9       one thread issues the MMAs: S_t(j) = Q_t K(j)^T (A and B from
+//                shared memory) and O_t += P_t(j) V(j) with P in tensor memory
+//                as two bf16 terms, hi and the residual lo (V an MN-major
+//                operand in shared memory), each group committed to an mbarrier;
 //   warps 0-7    softmax, one thread per (query, head) row (TMEM lane), warps
 //                0-3 tile 0 and 4-7 tile 1: masked online softmax in base 2 with a
 //                lazy rescale of O (only when the running max grows by more than
 //                2^8), P = hi + lo (about 16 significant bits, as in the gathered
 //                path: a single bf16 P costs 2^-9 |v| per dominant weight, more
 //                than the attention's tolerance when few keys carry the softmax)
-//                written into the swizzled K-major operand layout, and at the
-//                end O / l and the log-sum-exp.
-// Tensor memory: S buffers at columns 0-255 ([tile][buffer] x 64), O at 256-511.
+//                stored into tensor memory, and at the end O / l and the
+//                log-sum-exp.
+// Tensor memory, per tile t at column 256 t: S (64 fp32 columns), P_hi and P_lo
+// (32 columns each, two bf16 per column), O (128 fp32 columns).  Keeping P in
+// tensor memory keeps shared-memory traffic to the K, V and Q operand reads:
+// with P stored to and read back from shared memory, that traffic (about 320 KB
+// per 64 positions of a tile pair) held the tensor pipe to a third of its rate.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -55,22 +60,22 @@ namespace {
 
 __device__ int g_status;
 
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
-constexpr int kThreads = 320;
+constexpr int kKStages = 4;
+constexpr int kVStages = 3;
+constexpr int kThreads = 352;
 constexpr uint32_t kQHalf = 16384;   // 128 rows x 128 bytes: one 64-wide half of the head dim
 constexpr uint32_t kKVHalf = 8192;   // 64 positions x 128 bytes
 constexpr uint32_t kKVStage = 2 * kKVHalf;
-constexpr uint32_t kPBytes = 16384;  // 128 rows x 64 bf16
 constexpr uint32_t kMaskStage = 2048;  // up to 2 x 128 mask words
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = 4 * kQHalf;
 constexpr uint32_t kOffV = kOffK + kKStages * kKVStage;
-constexpr uint32_t kOffP = kOffV + kVStages * kKVStage;  // [tile][hi, lo]
-constexpr uint32_t kOffMask = kOffP + 4 * kPBytes;
+constexpr uint32_t kOffMask = kOffV + kVStages * kKVStage;
 constexpr uint32_t kOffBar = kOffMask + kKStages * kMaskStage;
-constexpr uint32_t kNumBars = 1 + 3 * kKStages + 2 * kVStages + 4 + 4 + 2 + 2 + 2;
+constexpr uint32_t kNumBars = 1 + 3 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2;
 constexpr uint32_t kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM address slot + alignment slack
+// tensor-memory columns of tile t: base + 256 t + ...
+constexpr uint32_t kColS = 0, kColPHi = 64, kColPLo = 96, kColO = 128;
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 constexpr float kRescaleLog2 = 8.f;  // O is rescaled only when the max grows by more than this (base-2 units)
 
@@ -89,9 +94,61 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Waits on an mbarrier phase with every lane of the warp; the result is warp-uniform.
+// Two fp32 lanes in one 64-bit register, and the packed fp32x2 arithmetic of
+// sm_100-class GPUs (one instruction for both lanes).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Waits for phase `parity` of `bar` for at most ~2 s, the thread suspended in
+// the hardware between checks (try_wait with a suspend-time hint of 100 us: it
+// returns as soon as the phase completes).  A polling wait here took issue
+// slots from the thread that issues the MMAs on the same SM sub-partition and
+// halved the tensor-core rate.
+__device__ __forceinline__ bool mbar_sleep_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
+        : "memory");
+    if (ok) return true;
+    if (global_ns() - t0 > 2000000000ull) return false;
+  }
+}
+
+// The same with every lane of the warp; the result is warp-uniform.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+  return __all_sync(0xffffffffu, mbar_sleep_wait(bar, parity));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -106,9 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* m_free = k_empty + kKStages;  // mask words read, one arrival per softmax warp
   uint64_t* v_full = m_free + kKStages;
   uint64_t* v_empty = v_full + kVStages;
-  uint64_t* s_full = v_empty + kVStages;  // [tile][buffer]
-  uint64_t* s_free = s_full + 4;          // [tile][buffer], one arrival per softmax warp
-  uint64_t* p_full = s_free + 4;          // [tile], one arrival per softmax warp
+  uint64_t* s_full = v_empty + kVStages;  // [tile]
+  uint64_t* s_free = s_full + 2;          // [tile], one arrival per softmax warp
+  uint64_t* p_full = s_free + 2;          // [tile], one arrival per softmax warp
   uint64_t* p_free = p_full + 2;          // [tile]
   uint64_t* drain = p_free + 2;
   uint64_t* tail = drain + 1;             // V rows past the tiles' last position zeroed
@@ -130,11 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-    }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&s_free[t], 4);
       mbar_init(&p_full[t], 4);
       mbar_init(&p_free[t], 1);
     }
@@ -151,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
+    // ---------------------------------------------------------- K producer
     const int rows = p.group * p.qt;
     const int mwords = min(2 * p.qt, p.nq_pad - q0);  // even: q0 and nq_pad are even
     if (lane == 0) {
@@ -164,11 +219,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(base + kOffQ + (t * 2 + x) * kQHalf, &qmap, 0, x, g * p.group, q0 + t * p.qt, q_full);
     }
     int blk_next = 0;
-    int k_issued = 0, v_issued = 0;
+    int k_issued = 0;
     for (int j = 0; j < nc; ++j) {
       if ((j & 31) == 0) blk_next = j + lane < nc ? load_block(p.bt, 0, 0, j + lane, p.num_blocks, &g_status) : 0;
       const int blk = __shfl_sync(0xffffffffu, blk_next, j & 31);
-      const int sk = j % kKStages, sv = j % kVStages;
+      const int sk = j % kKStages;
       if (j >= kKStages && !(warp_wait(&k_empty[sk], ((j / kKStages) + 1) & 1) &&
                              warp_wait(&m_free[sk], ((j / kKStages) + 1) & 1)))
         break;
@@ -180,6 +235,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                  &k_full[sk]);
       }
       k_issued = j + 1;
+    }
+    if (k_issued < nc && lane == 0) set_status(&g_status, kStTimeout);
+    // every copy this warp started has landed before the CTA ends
+    bool landed = true;
+    for (int j = max(k_issued - kKStages, 0); j < k_issued; ++j)
+      if (!warp_wait(&k_full[j % kKStages], (j / kKStages) & 1)) landed = false;
+    if (!landed && lane == 0) set_status(&g_status, kStTimeout);
+  } else if (warp == 10) {
+    // ---------------------------------------------------------- V producer
+    int blk_next = 0;
+    int v_issued = 0;
+    for (int j = 0; j < nc; ++j) {
+      if ((j & 31) == 0) blk_next = j + lane < nc ? load_block(p.bt, 0, 0, j + lane, p.num_blocks, &g_status) : 0;
+      const int blk = __shfl_sync(0xffffffffu, blk_next, j & 31);
+      const int sv = j % kVStages;
       if (j >= kVStages && !warp_wait(&v_empty[sv], ((j / kVStages) + 1) & 1)) break;
       if (lane == 0) {
         uint8_t* st = base + kOffV + sv * kKVStage;
@@ -189,10 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       v_issued = j + 1;
     }
     if (v_issued < nc && lane == 0) set_status(&g_status, kStTimeout);
-    // every copy this warp started has landed before the CTA ends
     bool landed = true;
-    for (int j = max(k_issued - kKStages, 0); j < k_issued; ++j)
-      if (!warp_wait(&k_full[j % kKStages], (j / kKStages) & 1)) landed = false;
     for (int j = max(v_issued - kVStages, 0); j < v_issued; ++j)
       if (!warp_wait(&v_full[j % kVStages], (j / kVStages) & 1)) landed = false;
     if (!landed && lane == 0) set_status(&g_status, kStTimeout);
@@ -214,44 +281,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = mma_idesc(128, 64, kFmtBF16);
       constexpr uint32_t idesc_o = mma_idesc(128, 128, kFmtBF16, 0, 1);
-      bool ok = mbar_wait(q_full, 0);
+      bool ok = mbar_sleep_wait(q_full, 0);
       tc_fence_after();
-      const uint32_t qb = smem_u32(base + kOffQ);
+      // descriptors computed once; a byte offset o added to the start address adds o >> 4
+      const uint64_t dq = smem_desc(smem_u32(base + kOffQ), 1024, kSwizzle128);
+      const uint64_t dk = smem_desc(smem_u32(base + kOffK), 1024, kSwizzle128);
+      const uint64_t dv = smem_desc_mn(smem_u32(base + kOffV), kKVHalf, 1024);
       for (int j = 0; ok && j <= nc; ++j) {
-        if (j < nc) {  // S_t(j) = Q_t K(j)^T
-          const int s = j % kKStages, b = j & 1;
-          ok = mbar_wait(&k_full[s], (j / kKStages) & 1);
+        if (j < nc) {  // S_t(j) = Q_t K(j)^T, once softmax_t has read S_t(j - 1)
+          const int s = j % kKStages;
+          ok = mbar_sleep_wait(&k_full[s], (j / kKStages) & 1);
           tc_fence_after();
-          const uint32_t kb = smem_u32(base + kOffK + s * kKVStage);
-          for (int t = 0; ok && t < 2; ++t) {
-            ok = mbar_wait(&s_free[t * 2 + b], ((j >> 1) & 1) ^ 1);
+          const uint64_t kb = dk + (uint64_t)(s * (kKVStage >> 4));
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!(ok = ok && mbar_sleep_wait(&s_free[t], (j & 1) ^ 1))) break;
             tc_fence_after();
-            const uint32_t qt_base = qb + t * 2 * kQHalf;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f16(tmem + (t * 2 + b) * 64,
-                      smem_desc(qt_base + (kk >> 2) * kQHalf + (kk & 3) * 32, 1024, kSwizzle128),
-                      smem_desc(kb + (kk >> 2) * kKVHalf + (kk & 3) * 32, 1024, kSwizzle128), idesc_s, kk > 0);
-            mma_commit(&s_full[t * 2 + b]);
+              mma_f16(tmem + t * 256 + kColS, dq + (uint64_t)((t * 2 * kQHalf + (kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                      kb + (uint64_t)(((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+            mma_commit(&s_full[t]);
           }
           mma_commit(&k_empty[s]);
         }
         if (j > 0 && ok) {  // O_t += (P_hi + P_lo)_t(j - 1) V(j - 1)
           const int jp = j - 1, s = jp % kVStages;
-          ok = mbar_wait(&v_full[s], (jp / kVStages) & 1);
-          if (ok && jp == nc - 1 && last_rows < kBlock) ok = mbar_wait(tail, 0);
+          ok = mbar_sleep_wait(&v_full[s], (jp / kVStages) & 1);
+          if (ok && jp == nc - 1 && last_rows < kBlock) ok = mbar_sleep_wait(tail, 0);
           tc_fence_after();
-          const uint32_t vb = smem_u32(base + kOffV + s * kKVStage);
-          for (int t = 0; ok && t < 2; ++t) {
-            ok = mbar_wait(&p_full[t], jp & 1);
+          const uint64_t vb = dv + (uint64_t)(s * (kKVStage >> 4));
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!(ok = ok && mbar_sleep_wait(&p_full[t], jp & 1))) break;
             tc_fence_after();
-            const uint32_t pb = smem_u32(base + kOffP + t * 2 * kPBytes);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_f16(tmem + 256 + t * 128, smem_desc(pb + h * kPBytes + kk * 32, 1024, kSwizzle128),
-                        smem_desc_mn(vb + kk * 2048, kKVHalf, 1024), idesc_o, jp > 0 || h > 0 || kk > 0);
+                mma_f16_ts(tmem + t * 256 + kColO, tmem + t * 256 + (h ? kColPLo : kColPHi) + kk * 8,
+                           vb + (uint64_t)((kk * 2048) >> 4), idesc_o, jp > 0 || h > 0 || kk > 0);
             mma_commit(&p_free[t]);
           }
           mma_commit(&v_empty[s]);
@@ -259,10 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) set_status(&g_status, kStTimeout);
       mma_commit(drain);  // every MMA issued above is complete before the CTA ends
-      if (!mbar_wait(drain, 0)) set_status(&g_status, kStTimeout);
+      if (!mbar_sleep_wait(drain, 0)) set_status(&g_status, kStTimeout);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ---------------------------------------------------------------- softmax
     const int t = warp >> 2;
     const int r = ((warp & 3) << 5) | lane;  // row = TMEM lane
@@ -271,23 +340,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = qi < p.qt && qd < p.n_dense;
     const int mword = t * p.qt + qi;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    uint8_t* prow = base + kOffP + t * 2 * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    const bool pos_scale = p.scale_log2 > 0.f;
     for (int j = 0; j < nc; ++j) {
-      const int b = j & 1, s = j % kKStages;
-      if (!(ok = warp_wait(&s_full[t * 2 + b], (j >> 1) & 1))) break;
+      const int s = j % kKStages;
+      if (!(ok = warp_wait(&s_full[t], j & 1))) break;
       tc_fence_after();
       uint32_t sv[64];
       {
         uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
         uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tmem_ld32(lane_addr + (t * 2 + b) * 64, lo);
-        tmem_ld32(lane_addr + (t * 2 + b) * 64 + 32, hi);
+        tmem_ld32(lane_addr + t * 256 + kColS, lo);
+        tmem_ld32(lane_addr + t * 256 + kColS + 32, hi);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[t * 2 + b]);
+      if (lane == 0) mbar_arrive(&s_free[t]);
       // the chunk's mask words came with its K block (phase j / kKStages of k_full[s]); the producer
       // refills the stage only after every softmax warp has read them (m_free)
       if (!(ok = warp_wait(&k_full[s], (j / kKStages) & 1))) break;
@@ -296,13 +365,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&m_free[s]);
       const uint32_t wlo = (uint32_t)w, whi = (uint32_t)(w >> 32);
+      // x = the raw score where the position is attended, -inf elsewhere; with a
+      // positive scale the scaled max is the scale times the raw max
       float x[64];
-      float mx = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const uint32_t bit = i < 32 ? (wlo >> i) & 1u : (whi >> (i - 32)) & 1u;
-        x[i] = bit ? __uint_as_float(sv[i]) * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[i]);
+        x[i] = bit ? __uint_as_float(sv[i]) : -INFINITY;
+      }
+      float mx;
+      if (pos_scale) {
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; i += 8) {
+          a0 = max3(a0, x[i], x[i + 1]);
+          a1 = max3(a1, x[i + 2], x[i + 3]);
+          a2 = max3(a2, x[i + 4], x[i + 5]);
+          a3 = max3(a3, x[i + 6], x[i + 7]);
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * p.scale_log2;
+      } else {  // scale <= 0: scale first (a masked -inf stays -inf)
+        mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          x[i] = x[i] == -INFINITY ? -INFINITY : x[i] * p.scale_log2;
+          mx = fmaxf(mx, x[i]);
+        }
       }
       float factor = 1.f;
       bool rescale = false;
@@ -315,16 +403,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = mx;
       }
       const float m_use = m == -INFINITY ? 0.f : m;
-      float sum = 0.f;
+      // p = 2^(scale x - m) two at a time; P = hi + lo with hi the truncated top
+      // 16 bits of p (exact bf16) and lo = p - hi rounded to bf16 (~16 bits in all)
+      const uint64_t c2 = pos_scale ? f2_pack(p.scale_log2, p.scale_log2) : f2_pack(1.f, 1.f);
+      const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      uint64_t sum2 = f2_pack(0.f, 0.f);
       uint32_t pk[32], pl[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float a = ex2(x[2 * i] - m_use), c = ex2(x[2 * i + 1] - m_use);
-        sum += a + c;
-        pk[i] = pack_bf16x2(a, c);
-        pl[i] = pack_bf16x2(a - __uint_as_float(pk[i] << 16), c - __uint_as_float(pk[i] & 0xffff0000u));
+        float a, c;
+        f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), c2, nm2), a, c);
+        a = ex2(a);
+        c = ex2(c);
+        const uint64_t pp = f2_pack(a, c);
+        sum2 = f2_add(sum2, pp);
+        const uint32_t ab = __float_as_uint(a), cb = __float_as_uint(c);
+        pk[i] = __byte_perm(ab, cb, 0x7632);
+        float la, lc;
+        f2_unpack(f2_sub(pp, f2_pack(__uint_as_float(ab & 0xffff0000u), __uint_as_float(cb & 0xffff0000u))), la, lc);
+        pl[i] = pack_bf16x2(la, lc);
       }
-      l += sum;
+      {
+        float s0, s1;
+        f2_unpack(sum2, s0, s1);
+        l += s0 + s1;
+      }
       // P(j) overwrites P(j - 1) and O may be rescaled only once O += P(j - 1) V(j - 1) is done
       if (j > 0 && !(ok = warp_wait(&p_free[t], (j - 1) & 1))) break;
       tc_fence_after();
@@ -332,20 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + 256 + t * 128 + c * 32, o);
+          tmem_ld32(lane_addr + t * 256 + kColO + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          tmem_st32(lane_addr + 256 + t * 128 + c * 32, o);
+          tmem_st32(lane_addr + t * 256 + kColO + c * 32, o);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(prow + kPBytes + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pl[4 * c], pl[4 * c + 1], pl[4 * c + 2], pl[4 * c + 3]);
-      }
-      fence_proxy_async();
+      tmem_st32(lane_addr + t * 256 + kColPHi, pk);
+      tmem_st32(lane_addr + t * 256 + kColPLo, pl);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
@@ -359,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + 256 + t * 128 + c * 32, o);
+        tmem_ld32(lane_addr + t * 256 + kColO + c * 32, o);
         if (!valid) continue;
         if (p.out_dtype == DSA_OUT_F32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * kHeadDim + c * 32);
