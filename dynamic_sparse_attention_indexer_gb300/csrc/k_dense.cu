@@ -18,31 +18,35 @@
 // bitmap, word [c][i] holding positions 64c .. 64c + 63 of dense query i.
 //
 // dense_attn_kernel, one CTA per (KV head, two tiles of QT = floor(128 / G)
-// queries), heaviest (latest) tiles first, 352 threads:
-//   warp 8       K producer: TMA loads of the two Q tiles (once), then per
-//                chunk of 64 positions the K block of the KV head (two 8 KB
-//                boxes, 128-byte swizzle) with the tiles' mask words into a
-//                4-stage ring, released as soon as S is computed;
-//   warp 10      V producer: the chunk's V block into a 3-stage ring, released
-//                after P V.  Separate issuers keep the K loads several chunks
-//                ahead of their use;
-//   warp 9       one thread issues the MMAs: S_t(j) = Q_t K(j)^T (A and B from
-//                shared memory) and O_t += P_t(j) V(j) with P in tensor memory
-//                as two bf16 terms, hi and the residual lo (V an MN-major
-//                operand in shared memory), each group committed to an mbarrier;
+// queries), heaviest (latest) tiles first, 320 threads, in steps of 128
+// positions (two cache blocks):
+//   warp 8       producer: TMA loads of the two Q tiles (once), then per step
+//                the two K blocks of the KV head (8 KB boxes, 128-byte swizzle)
+//                with the tiles' mask words, and the two V blocks, into 2-stage
+//                rings (K stage i + 1 and V stage i free up together: the
+//                products of step i - 1 and the S of step i are issued back to
+//                back);
+//   warp 9       one thread issues the MMAs, per tile t: O_t += P_t(i) V(i) (P
+//                in tensor memory as two bf16 terms, hi and the residual lo; V
+//                an MN-major operand) and then S_t(i + 1) = Q_t K(i + 1)^T
+//                (M = 128, N = 128, K = 16 per instruction, the shape at which
+//                one issuing thread keeps the tensor core at its full rate: an
+//                issue costs ~63 cycles, an N = 64 product only 34), each group
+//                committed to an mbarrier.  The tiles alternate, so one tile's
+//                softmax overlaps the other tile's products;
 //   warps 0-7    softmax, one thread per (query, head) row (TMEM lane), warps
 //                0-3 tile 0 and 4-7 tile 1: masked online softmax in base 2 with a
 //                lazy rescale of O (only when the running max grows by more than
-//                2^8), P = hi + lo (about 16 significant bits, as in the gathered
-//                path: a single bf16 P costs 2^-9 |v| per dominant weight, more
-//                than the attention's tolerance when few keys carry the softmax)
-//                stored into tensor memory, and at the end O / l and the
-//                log-sum-exp.
-// Tensor memory, per tile t at column 256 t: S (64 fp32 columns), P_hi and P_lo
-// (32 columns each, two bf16 per column), O (128 fp32 columns).  Keeping P in
-// tensor memory keeps shared-memory traffic to the K, V and Q operand reads:
-// with P stored to and read back from shared memory, that traffic (about 320 KB
-// per 64 positions of a tile pair) held the tensor pipe to a third of its rate.
+//                2^8) and P = hi + lo (about 16 significant bits, as in the
+//                gathered path: a single bf16 P costs 2^-9 |v| per dominant
+//                weight, more than the attention's tolerance when few keys carry
+//                the softmax), written over S in tensor memory, and at the end
+//                O / l and the log-sum-exp.
+// Tensor memory per tile t at column 256 t: S (128 fp32 columns), overwritten
+// by P in place, 32 positions at a time: positions 32c .. 32c + 31 as P_hi in
+// columns 32c .. 32c + 15 and P_lo in 32c + 16 .. 32c + 31 (two bf16 per
+// column); O in columns 128 .. 255.  S(i + 1) overwrites P(i): the tcgen05.mma
+// operations of one thread run in issue order, so P V reads P first.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -60,23 +64,22 @@ namespace {
 
 __device__ int g_status;
 
-constexpr int kKStages = 4;
-constexpr int kVStages = 3;
-constexpr int kThreads = 352;
+constexpr int kStages = 2;       // K and V ring stages, one 128-position step each
+constexpr int kThreads = 320;
 constexpr uint32_t kQHalf = 16384;   // 128 rows x 128 bytes: one 64-wide half of the head dim
-constexpr uint32_t kKVHalf = 8192;   // 64 positions x 128 bytes
+constexpr uint32_t kKVBlockHalf = 8192;            // 64 positions x 128 bytes
+constexpr uint32_t kKVHalf = 2 * kKVBlockHalf;     // 128 positions x 128 bytes
 constexpr uint32_t kKVStage = 2 * kKVHalf;
-constexpr uint32_t kMaskStage = 2048;  // up to 2 x 128 mask words
+constexpr uint32_t kMaskChunk = 2048;  // up to 2 x 128 mask words of one block
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = 4 * kQHalf;
-constexpr uint32_t kOffV = kOffK + kKStages * kKVStage;
-constexpr uint32_t kOffMask = kOffV + kVStages * kKVStage;
-constexpr uint32_t kOffBar = kOffMask + kKStages * kMaskStage;
-constexpr uint32_t kNumBars = 1 + 3 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2;
+constexpr uint32_t kOffV = kOffK + kStages * kKVStage;
+constexpr uint32_t kOffMask = kOffV + kStages * kKVStage;
+constexpr uint32_t kOffBar = kOffMask + kStages * 2 * kMaskChunk;
+constexpr uint32_t kNumBars = 1 + 5 * kStages + 2 + 2 + 2;
 constexpr uint32_t kSmem = kOffBar + kNumBars * 8 + 16 + 1024;  // + TMEM address slot + alignment slack
-// tensor-memory columns of tile t: base + 256 t + ...
-constexpr uint32_t kColS = 0, kColPHi = 64, kColPLo = 96, kColO = 128;
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
+constexpr uint32_t kColO = 128;  // tensor-memory column of O within a tile's 256
 constexpr float kRescaleLog2 = 8.f;  // O is rescaled only when the max grows by more than this (base-2 units)
 
 struct DenseParams {
@@ -130,18 +133,22 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // returns as soon as the phase completes).  A polling wait here took issue
 // slots from the thread that issues the MMAs on the same SM sub-partition and
 // halved the tensor-core rate.
+__device__ __forceinline__ bool mbar_try_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_sleep_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_sleep(bar, parity)) return true;  // the usual case: no timer read
   const uint64_t t0 = global_ns();
   while (true) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
-        : "memory");
-    if (ok) return true;
+    if (mbar_try_sleep(bar, parity)) return true;
     if (global_ns() - t0 > 2000000000ull) return false;
   }
 }
@@ -151,6 +158,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_sleep_wait(bar, parity));
 }
 
+// POS_SCALE: softmax_scale > 0 (the usual case: the max of the scaled scores is
+// the scale times the raw max); otherwise every score is scaled first.
+template <bool POS_SCALE>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_attn_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DenseParams p) {
@@ -158,40 +168,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kOffBar);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;  // K block and mask words of a chunk landed
-  uint64_t* k_empty = k_full + kKStages;
-  uint64_t* m_free = k_empty + kKStages;  // mask words read, one arrival per softmax warp
-  uint64_t* v_full = m_free + kKStages;
-  uint64_t* v_empty = v_full + kVStages;
-  uint64_t* s_full = v_empty + kVStages;  // [tile]
-  uint64_t* s_free = s_full + 2;          // [tile], one arrival per softmax warp
-  uint64_t* p_full = s_free + 2;          // [tile], one arrival per softmax warp
-  uint64_t* p_free = p_full + 2;          // [tile]
-  uint64_t* drain = p_free + 2;
-  uint64_t* tail = drain + 1;             // V rows past the tiles' last position zeroed
+  uint64_t* k_full = bars + 1;  // K blocks and mask words of a step landed
+  uint64_t* k_empty = k_full + kStages;
+  uint64_t* m_free = k_empty + kStages;  // mask words read, one arrival per softmax warp
+  uint64_t* v_full = m_free + kStages;
+  uint64_t* v_empty = v_full + kStages;
+  uint64_t* s_full = v_empty + kStages;  // [tile]: S(i) computed (and every earlier product done)
+  uint64_t* p_full = s_full + 2;         // [tile]: P(i) written, one arrival per softmax warp
+  uint64_t* drain = p_full + 2;
+  uint64_t* tail = drain + 1;            // V rows past the tiles' last position zeroed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(tail + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % p.hkv;
   const int q0 = (p.n_super - 1 - blockIdx.x / p.hkv) * 2 * p.qt;  // heaviest tiles first
   const int q_last = min(q0 + 2 * p.qt, p.n_dense) - 1;
-  const int nc = (p.pos0 + q_last) / kBlock + 1;  // chunks of 64 positions the tiles see
-  const int last_rows = p.pos0 + q_last - (nc - 1) * kBlock + 1;  // positions of the last chunk in range
+  const int pos_last = p.pos0 + q_last;
+  const int nc = pos_last / kBlock + 1;  // blocks of 64 positions the tiles see
+  const int ns = (nc + 1) / 2;           // steps of two blocks
+  const int last_rows = pos_last - (ns - 1) * 2 * kBlock + 1;  // positions of the last step in range (1..128)
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kKStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&m_free[s], 8);
-    }
-    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&s_free[t], 4);
       mbar_init(&p_full[t], 4);
-      mbar_init(&p_free[t], 1);
     }
     mbar_init(drain, 1);
     mbar_init(tail, 1);
@@ -206,69 +212,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
 
   if (warp == 8) {
-    // ---------------------------------------------------------- K producer
-    const int rows = p.group * p.qt;
+    // ------------------------------------------------------------- producer
     const int mwords = min(2 * p.qt, p.nq_pad - q0);  // even: q0 and nq_pad are even
     if (lane == 0) {
       tma_prefetch_map(&qmap);
       tma_prefetch_map(&kmap);
       tma_prefetch_map(&vmap);
-      mbar_arrive_expect_tx(q_full, 4u * (uint32_t)rows * 128u);
+      mbar_arrive_expect_tx(q_full, 4u * (uint32_t)(p.group * p.qt) * 128u);
       for (int t = 0; t < 2; ++t)
         for (int x = 0; x < 2; ++x)
           tma_load_4d(base + kOffQ + (t * 2 + x) * kQHalf, &qmap, 0, x, g * p.group, q0 + t * p.qt, q_full);
     }
     int blk_next = 0;
-    int k_issued = 0;
-    for (int j = 0; j < nc; ++j) {
-      if ((j & 31) == 0) blk_next = j + lane < nc ? load_block(p.bt, 0, 0, j + lane, p.num_blocks, &g_status) : 0;
-      const int blk = __shfl_sync(0xffffffffu, blk_next, j & 31);
-      const int sk = j % kKStages;
-      if (j >= kKStages && !(warp_wait(&k_empty[sk], ((j / kKStages) + 1) & 1) &&
-                             warp_wait(&m_free[sk], ((j / kKStages) + 1) & 1)))
-        break;
+    int k_issued = 0, v_issued = 0;
+    for (int i = 0; i < ns; ++i) {
+      const int c0 = 2 * i, nb = c0 + 1 < nc ? 2 : 1;  // blocks in this step
+      if ((c0 & 31) == 0) blk_next = c0 + lane < nc ? load_block(p.bt, 0, 0, c0 + lane, p.num_blocks, &g_status) : 0;
+      const int b0 = __shfl_sync(0xffffffffu, blk_next, c0 & 31);
+      const int b1 = __shfl_sync(0xffffffffu, blk_next, (c0 + 1) & 31);
+      const int s = i % kStages;
+      const uint32_t par = ((i / kStages) + 1) & 1;
+      if (i >= kStages && !(warp_wait(&k_empty[s], par) && warp_wait(&m_free[s], par))) break;
       if (lane == 0) {
-        uint8_t* st = base + kOffK + sk * kKVStage;
-        mbar_arrive_expect_tx(&k_full[sk], kKVStage + (uint32_t)mwords * 8u);
-        for (int x = 0; x < 2; ++x) tma_load_4d(st + x * kKVHalf, &kmap, 0, x, g, blk * kBlock, &k_full[sk]);
-        bulk_g2s(base + kOffMask + sk * kMaskStage, p.mask + (size_t)j * p.nq_pad + q0, (uint32_t)mwords * 8u,
-                 &k_full[sk]);
+        uint8_t* st = base + kOffK + s * kKVStage;
+        mbar_arrive_expect_tx(&k_full[s], (uint32_t)nb * (2 * kKVBlockHalf + (uint32_t)mwords * 8u));
+        for (int a = 0; a < nb; ++a) {
+          for (int x = 0; x < 2; ++x)
+            tma_load_4d(st + x * kKVHalf + a * kKVBlockHalf, &kmap, 0, x, g, (a ? b1 : b0) * kBlock, &k_full[s]);
+          bulk_g2s(base + kOffMask + (s * 2 + a) * kMaskChunk, p.mask + (size_t)(c0 + a) * p.nq_pad + q0,
+                   (uint32_t)mwords * 8u, &k_full[s]);
+        }
       }
-      k_issued = j + 1;
+      k_issued = i + 1;
+      if (i >= kStages && !warp_wait(&v_empty[s], par)) break;
+      if (lane == 0) {
+        uint8_t* st = base + kOffV + s * kKVStage;
+        mbar_arrive_expect_tx(&v_full[s], (uint32_t)nb * 2 * kKVBlockHalf);
+        for (int a = 0; a < nb; ++a)
+          for (int x = 0; x < 2; ++x)
+            tma_load_4d(st + x * kKVHalf + a * kKVBlockHalf, &vmap, 0, x, g, (a ? b1 : b0) * kBlock, &v_full[s]);
+      }
+      v_issued = i + 1;
     }
-    if (k_issued < nc && lane == 0) set_status(&g_status, kStTimeout);
+    if (v_issued < ns && lane == 0) set_status(&g_status, kStTimeout);
     // every copy this warp started has landed before the CTA ends
     bool landed = true;
-    for (int j = max(k_issued - kKStages, 0); j < k_issued; ++j)
-      if (!warp_wait(&k_full[j % kKStages], (j / kKStages) & 1)) landed = false;
+    for (int i = max(k_issued - kStages, 0); i < k_issued; ++i)
+      if (!warp_wait(&k_full[i % kStages], (i / kStages) & 1)) landed = false;
+    for (int i = max(v_issued - kStages, 0); i < v_issued; ++i)
+      if (!warp_wait(&v_full[i % kStages], (i / kStages) & 1)) landed = false;
     if (!landed && lane == 0) set_status(&g_status, kStTimeout);
-  } else if (warp == 10) {
-    // ---------------------------------------------------------- V producer
-    int blk_next = 0;
-    int v_issued = 0;
-    for (int j = 0; j < nc; ++j) {
-      if ((j & 31) == 0) blk_next = j + lane < nc ? load_block(p.bt, 0, 0, j + lane, p.num_blocks, &g_status) : 0;
-      const int blk = __shfl_sync(0xffffffffu, blk_next, j & 31);
-      const int sv = j % kVStages;
-      if (j >= kVStages && !warp_wait(&v_empty[sv], ((j / kVStages) + 1) & 1)) break;
-      if (lane == 0) {
-        uint8_t* st = base + kOffV + sv * kKVStage;
-        mbar_arrive_expect_tx(&v_full[sv], kKVStage);
-        for (int x = 0; x < 2; ++x) tma_load_4d(st + x * kKVHalf, &vmap, 0, x, g, blk * kBlock, &v_full[sv]);
-      }
-      v_issued = j + 1;
-    }
-    if (v_issued < nc && lane == 0) set_status(&g_status, kStTimeout);
-    bool landed = true;
-    for (int j = max(v_issued - kVStages, 0); j < v_issued; ++j)
-      if (!warp_wait(&v_full[j % kVStages], (j / kVStages) & 1)) landed = false;
-    if (!landed && lane == 0) set_status(&g_status, kStTimeout);
-    // Positions of the last block past the tiles' last position may hold anything
-    // (unwritten slots); P is zero there, and their V rows are zeroed so that no
-    // non-finite value meets a zero weight in the product.
-    if (landed && v_issued == nc && last_rows < kBlock) {
-      uint8_t* vt = base + kOffV + ((nc - 1) % kVStages) * kKVStage;
-      const int n16 = (kBlock - last_rows) * 8;  // 16-byte pieces per half
+    // Positions of the last step past the tiles' last position (a block not
+    // loaded, or unwritten slots of the last block) may hold anything; P is zero
+    // there, and their V rows are zeroed so that no non-finite value meets a
+    // zero weight in the product.
+    if (landed && v_issued == ns && last_rows < 2 * kBlock) {
+      uint8_t* vt = base + kOffV + ((ns - 1) % kStages) * kKVStage;
+      const int n16 = (2 * kBlock - last_rows) * 8;  // 16-byte pieces per half
       for (int e = lane; e < 2 * n16; e += 32)
         *reinterpret_cast<uint4*>(vt + (e / n16) * kKVHalf + last_rows * 128 + (e % n16) * 16) =
             make_uint4(0, 0, 0, 0);
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // -------------------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc_s = mma_idesc(128, 64, kFmtBF16);
+      constexpr uint32_t idesc_s = mma_idesc(128, 128, kFmtBF16);
       constexpr uint32_t idesc_o = mma_idesc(128, 128, kFmtBF16, 0, 1);
       bool ok = mbar_sleep_wait(q_full, 0);
       tc_fence_after();
@@ -287,44 +287,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq = smem_desc(smem_u32(base + kOffQ), 1024, kSwizzle128);
       const uint64_t dk = smem_desc(smem_u32(base + kOffK), 1024, kSwizzle128);
       const uint64_t dv = smem_desc_mn(smem_u32(base + kOffV), kKVHalf, 1024);
-      for (int j = 0; ok && j <= nc; ++j) {
-        if (j < nc) {  // S_t(j) = Q_t K(j)^T, once softmax_t has read S_t(j - 1)
-          const int s = j % kKStages;
-          ok = mbar_sleep_wait(&k_full[s], (j / kKStages) & 1);
-          tc_fence_after();
-          const uint64_t kb = dk + (uint64_t)(s * (kKVStage >> 4));
+      auto issue_qk = [&](int t, int i) {  // S_t(i) = Q_t K(i)^T
+        const uint64_t kb = dk + (uint64_t)((i % kStages) * (kKVStage >> 4));
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!(ok = ok && mbar_sleep_wait(&s_free[t], (j & 1) ^ 1))) break;
-            tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16(tmem + t * 256, dq + (uint64_t)((t * 2 * kQHalf + (kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                  kb + (uint64_t)(((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
+        mma_commit(&s_full[t]);
+      };
+      if (ok) ok = mbar_sleep_wait(&k_full[0], 0);
+      tc_fence_after();
+      if (ok) {
+        issue_qk(0, 0);
+        issue_qk(1, 0);
+        mma_commit(&k_empty[0]);
+      }
+      for (int i = 0; ok && i < ns; ++i) {
+        const int sv = i % kStages;
+        ok = mbar_sleep_wait(&v_full[sv], (i / kStages) & 1);
+        if (ok && i == ns - 1 && last_rows < 2 * kBlock) ok = mbar_sleep_wait(tail, 0);
+        if (ok && i + 1 < ns) ok = mbar_sleep_wait(&k_full[(i + 1) % kStages], ((i + 1) / kStages) & 1);
+        tc_fence_after();
+        const uint64_t vb = dv + (uint64_t)(sv * (kKVStage >> 4));
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!(ok = ok && mbar_sleep_wait(&p_full[t], i & 1))) break;
+          tc_fence_after();
+          // O_t += (P_hi + P_lo)_t(i) V(i): 8 steps of 16 positions, P columns of
+          // positions 16kk .. 16kk + 15 at 32 (kk / 2) + 8 (kk % 2) (+ 16 for lo)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_f16(tmem + t * 256 + kColS, dq + (uint64_t)((t * 2 * kQHalf + (kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
-                      kb + (uint64_t)(((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idesc_s, kk > 0);
-            mma_commit(&s_full[t]);
-          }
-          mma_commit(&k_empty[s]);
+              mma_f16_ts(tmem + t * 256 + kColO, tmem + t * 256 + 32 * (kk >> 1) + 8 * (kk & 1) + 16 * h,
+                         vb + (uint64_t)((kk * 2048) >> 4), idesc_o, i > 0 || h > 0 || kk > 0);
+          if (i + 1 < ns) issue_qk(t, i + 1);  // overwrites P_t(i) after the products above have read it
+          else mma_commit(&s_full[t]);         // the last products done: the epilogue's signal
         }
-        if (j > 0 && ok) {  // O_t += (P_hi + P_lo)_t(j - 1) V(j - 1)
-          const int jp = j - 1, s = jp % kVStages;
-          ok = mbar_sleep_wait(&v_full[s], (jp / kVStages) & 1);
-          if (ok && jp == nc - 1 && last_rows < kBlock) ok = mbar_sleep_wait(tail, 0);
-          tc_fence_after();
-          const uint64_t vb = dv + (uint64_t)(s * (kKVStage >> 4));
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!(ok = ok && mbar_sleep_wait(&p_full[t], jp & 1))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ts(tmem + t * 256 + kColO, tmem + t * 256 + (h ? kColPLo : kColPHi) + kk * 8,
-                           vb + (uint64_t)((kk * 2048) >> 4), idesc_o, jp > 0 || h > 0 || kk > 0);
-            mma_commit(&p_free[t]);
-          }
-          mma_commit(&v_empty[s]);
-        }
+        mma_commit(&v_empty[sv]);
+        if (i + 1 < ns) mma_commit(&k_empty[(i + 1) % kStages]);
       }
       if (!ok) set_status(&g_status, kStTimeout);
       mma_commit(drain);  // every MMA issued above is complete before the CTA ends
@@ -339,116 +340,149 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qd = q0 + t * p.qt + qi;  // dense query index
     const bool valid = qi < p.qt && qd < p.n_dense;
     const int mword = t * p.qt + qi;
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + t * 256;
+    constexpr bool pos_scale = POS_SCALE;
+    const uint64_t c2 = pos_scale ? f2_pack(p.scale_log2, p.scale_log2) : f2_pack(1.f, 1.f);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    const bool pos_scale = p.scale_log2 > 0.f;
-    for (int j = 0; j < nc; ++j) {
-      const int s = j % kKStages;
-      if (!(ok = warp_wait(&s_full[t], j & 1))) break;
+    for (int i = 0; i < ns; ++i) {
+      const int s = i % kStages;
+      if (!(ok = warp_wait(&s_full[t], i & 1))) break;
       tc_fence_after();
-      uint32_t sv[64];
-      {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tmem_ld32(lane_addr + t * 256 + kColS, lo);
-        tmem_ld32(lane_addr + t * 256 + kColS + 32, hi);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[t]);
-      // the chunk's mask words came with its K block (phase j / kKStages of k_full[s]); the producer
+      // the step's mask words came with its K blocks (phase i / kStages of k_full[s]); the producer
       // refills the stage only after every softmax warp has read them (m_free)
-      if (!(ok = warp_wait(&k_full[s], (j / kKStages) & 1))) break;
-      uint64_t w = 0;
-      if (valid) w = reinterpret_cast<const uint64_t*>(base + kOffMask + s * kMaskStage)[mword];
+      if (!(ok = warp_wait(&k_full[s], (i / kStages) & 1))) break;
+      uint64_t w[2] = {0ull, 0ull};
+      if (valid) {
+        w[0] = reinterpret_cast<const uint64_t*>(base + kOffMask + (s * 2) * kMaskChunk)[mword];
+        if (2 * i + 1 < nc) w[1] = reinterpret_cast<const uint64_t*>(base + kOffMask + (s * 2 + 1) * kMaskChunk)[mword];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&m_free[s]);
-      const uint32_t wlo = (uint32_t)w, whi = (uint32_t)(w >> 32);
-      // x = the raw score where the position is attended, -inf elsewhere; with a
-      // positive scale the scaled max is the scale times the raw max
-      float x[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const uint32_t bit = i < 32 ? (wlo >> i) & 1u : (whi >> (i - 32)) & 1u;
-        x[i] = bit ? __uint_as_float(sv[i]) : -INFINITY;
-      }
-      float mx;
-      if (pos_scale) {
-        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 64; i += 8) {
-          a0 = max3(a0, x[i], x[i + 1]);
-          a1 = max3(a1, x[i + 2], x[i + 3]);
-          a2 = max3(a2, x[i + 4], x[i + 5]);
-          a3 = max3(a3, x[i + 6], x[i + 7]);
-        }
-        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * p.scale_log2;
-      } else {  // scale <= 0: scale first (a masked -inf stays -inf)
-        mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = x[i] == -INFINITY ? -INFINITY : x[i] * p.scale_log2;
-          mx = fmaxf(mx, x[i]);
-        }
-      }
-      float factor = 1.f;
-      bool rescale = false;
-      if (mx > m + kRescaleLog2) {  // also the first finite max (m = -inf)
-        if (m != -INFINITY) {
-          factor = ex2(m - mx);
-          l *= factor;
-          rescale = true;
-        }
-        m = mx;
-      }
-      const float m_use = m == -INFINITY ? 0.f : m;
-      // p = 2^(scale x - m) two at a time; P = hi + lo with hi the truncated top
-      // 16 bits of p (exact bf16) and lo = p - hi rounded to bf16 (~16 bits in all)
-      const uint64_t c2 = pos_scale ? f2_pack(p.scale_log2, p.scale_log2) : f2_pack(1.f, 1.f);
-      const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      // The step's 128 positions in two halves of 64.  Each half's S is read from
+      // tensor memory once (P is written over it): tensor-memory reads from the
+      // threads compete with the products for its bandwidth, so a separate max
+      // pass over S cost more than it saved, and holding all 128 scores in
+      // registers spilled.  When the second half raises the running max past the
+      // lazy threshold, the first half's P is rescaled together with O.
       uint64_t sum2 = f2_pack(0.f, 0.f);
-      uint32_t pk[32], pl[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float a, c;
-        f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), c2, nm2), a, c);
-        a = ex2(a);
-        c = ex2(c);
-        const uint64_t pp = f2_pack(a, c);
-        sum2 = f2_add(sum2, pp);
-        const uint32_t ab = __float_as_uint(a), cb = __float_as_uint(c);
-        pk[i] = __byte_perm(ab, cb, 0x7632);
-        float la, lc;
-        f2_unpack(f2_sub(pp, f2_pack(__uint_as_float(ab & 0xffff0000u), __uint_as_float(cb & 0xffff0000u))), la, lc);
-        pl[i] = pack_bf16x2(la, lc);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sv[2][32];
+        tmem_ld32_nowait(lane_addr + 64 * hh, sv[0]);
+        tmem_ld32_nowait(lane_addr + 64 * hh + 32, sv[1]);
+        tmem_wait_ld();
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t wb = q ? (uint32_t)(w[hh] >> 32) : (uint32_t)w[hh];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = (wb >> e) & 1u ? __uint_as_float(sv[q][e]) : -INFINITY;
+            if (!pos_scale) x = x == -INFINITY ? -INFINITY : x * p.scale_log2;
+            sv[q][e] = __float_as_uint(x);
+          }
+          float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            a0 = max3(a0, __uint_as_float(sv[q][e]), __uint_as_float(sv[q][e + 1]));
+            a1 = max3(a1, __uint_as_float(sv[q][e + 2]), __uint_as_float(sv[q][e + 3]));
+          }
+          mx = max3(mx, a0, a1);
+        }
+        if (pos_scale) mx *= p.scale_log2;  // -inf stays -inf
+        float factor = 1.f;
+        bool rescale = false;
+        if (mx > m + kRescaleLog2) {  // also the first finite max (m = -inf)
+          if (m != -INFINITY) {
+            factor = ex2(m - mx);
+            l *= factor;
+            rescale = true;
+          }
+          m = mx;
+        }
+        // O (the products of the previous steps are complete: s_full of this step
+        // came after them) and, in the second half, this step's first-half P.  The
+        // tensor-memory loads and stores are warp-wide, so the warp rescales if any
+        // row needs it, the other rows by 1.
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (hh == 1) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t hl[32];  // [0, 16): hi, [16, 32): lo of positions 32c .. 32c + 31, two per column
+              tmem_ld32(lane_addr + 32 * c, hl);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float a = (__uint_as_float(hl[e] << 16) + __uint_as_float(hl[16 + e] << 16)) * factor;
+                const float b =
+                    (__uint_as_float(hl[e] & 0xffff0000u) + __uint_as_float(hl[16 + e] & 0xffff0000u)) * factor;
+                const uint32_t ab = __float_as_uint(a), bb = __float_as_uint(b);
+                hl[e] = __byte_perm(ab, bb, 0x7632);
+                hl[16 + e] =
+                    pack_bf16x2(a - __uint_as_float(ab & 0xffff0000u), b - __uint_as_float(bb & 0xffff0000u));
+              }
+              tmem_st32(lane_addr + 32 * c, hl);
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + kColO + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+            tmem_st32(lane_addr + kColO + c * 32, o);
+          }
+        }
+        const float m_use = m == -INFINITY ? 0.f : m;
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
+        // p = 2^(scale s - m); P = hi + lo with hi the truncated top 16 bits of p
+        // (exact bf16) and lo = p - hi rounded to bf16 (~16 bits in all)
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {  // positions 64 hh + 16 c8 .. + 15
+          const int q = c8 >> 1, o = 16 * (c8 & 1);
+          uint32_t ph[8], pl[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float a, b;
+            f2_unpack(
+                f2_fma(f2_pack(__uint_as_float(sv[q][o + 2 * e]), __uint_as_float(sv[q][o + 2 * e + 1])), c2, nm2), a,
+                b);
+            a = ex2(a);
+            b = ex2(b);
+            const uint64_t pp = f2_pack(a, b);
+            sum2 = f2_add(sum2, pp);
+            const uint32_t ab = __float_as_uint(a), bb = __float_as_uint(b);
+            ph[e] = __byte_perm(ab, bb, 0x7632);
+            float la, lb;
+            f2_unpack(f2_sub(pp, f2_pack(__uint_as_float(ab & 0xffff0000u), __uint_as_float(bb & 0xffff0000u))), la,
+                      lb);
+            pl[e] = pack_bf16x2(la, lb);
+          }
+          // positions 32c + o .. + 15 (c = 2 hh + q): hi in columns 32c + o / 2 .. + 7, lo 16 columns further
+          const int c = 2 * hh + q;
+          tmem_st8_nowait(lane_addr + 32 * c + o / 2, ph);
+          tmem_st8_nowait(lane_addr + 32 * c + 16 + o / 2, pl);
+        }
+        if (hh == 0) {  // the first half's weights into l before a possible rescale in the second
+          float s0, s1;
+          f2_unpack(sum2, s0, s1);
+          l += s0 + s1;
+          sum2 = f2_pack(0.f, 0.f);
+          tmem_wait_st();  // its P is in tensor memory before the second half may rescale it
+        }
       }
       {
         float s0, s1;
         f2_unpack(sum2, s0, s1);
         l += s0 + s1;
       }
-      // P(j) overwrites P(j - 1) and O may be rescaled only once O += P(j - 1) V(j - 1) is done
-      if (j > 0 && !(ok = warp_wait(&p_free[t], (j - 1) & 1))) break;
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + t * 256 + kColO + c * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          tmem_st32(lane_addr + t * 256 + kColO + c * 32, o);
-        }
-      }
-      tmem_st32(lane_addr + t * 256 + kColPHi, pk);
-      tmem_st32(lane_addr + t * 256 + kColPLo, pl);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    // ---- epilogue: O / l, log-sum-exp
-    if (ok && (ok = warp_wait(&p_free[t], (nc - 1) & 1))) {
+    // ---- epilogue: O / l, log-sum-exp, once the last products are done
+    if (ok && (ok = warp_wait(&s_full[t], ns & 1))) {
       tc_fence_after();
       const int head = g * p.group + (r - qi * p.group);
       const size_t row = (size_t)qd * p.hq + head;
@@ -456,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + t * 256 + kColO + c * 32, o);
+        tmem_ld32(lane_addr + kColO + c * 32, o);
         if (!valid) continue;
         if (p.out_dtype == DSA_OUT_F32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * kHeadDim + c * 32);
@@ -567,7 +601,10 @@ size_t dense_mask_bytes(const QS& qs, int n_dense) {
 }
 
 cudaError_t setup_dense_kernels() {
-  return cudaFuncSetAttribute(dense_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  cudaError_t e = cudaFuncSetAttribute(dense_attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dense_attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  return e;
 }
 
 cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st) {
@@ -604,8 +641,8 @@ cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cud
   p.n_super = (n_dense + 2 * qt - 1) / (2 * qt);
   p.out_dtype = a.out_dtype;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  return launch_pdl(dense_attn_kernel, dim3(p.n_super * a.kv.hkv), dim3(kThreads), kSmem, st, 1, qmap, kmap, vmap,
-                    p);
+  return launch_pdl(p.scale_log2 > 0.f ? dense_attn_kernel<true> : dense_attn_kernel<false>,
+                    dim3(p.n_super * a.kv.hkv), dim3(kThreads), kSmem, st, 1, qmap, kmap, vmap, p);
 }
 
 cudaError_t read_clear_status_dense(int* code, cudaStream_t st) {
