@@ -209,7 +209,7 @@ dsa_status dsa_sparse_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t
 /* Prefill form: the queries of `qs` (mode DSA_MODE_PREFILL), in two parts
  * (§2.3: selection, gather and attention fused per prefill chunk):
  *   - the first n_dense queries (those at positions below about
- *     12 * (prefix_len + k), where the attended set is a large share of the causal
+ *     10 * (prefix_len + k), where the attended set is a large share of the causal
  *     range; see dsa_prefill_dense_queries) as a masked dense pass on the tensor
  *     cores: every causal position of a tile of queries is read once per tile
  *     and weighted zero unless it is in the query's attended set.  This part

@@ -214,8 +214,8 @@ def test_workspace_sizes(lib):
     kv5 = _kv(num_blocks=4096, num_kv_heads=4, max_blocks_per_seq=4096, batch=1, max_context_len=262144)
     assert lib.dsa_prefill_dense_queries(C.byref(kv5), C.byref(_qs(1, 4096, 0, 200000)), 2048, 32, 576) == 0
     # and near its start takes a whole number of dense tile pairs (2 x 16 queries at group 8)
-    n = lib.dsa_prefill_dense_queries(C.byref(kv5), C.byref(_qs(1, 4096, 0, 30000)), 2048, 32, 576)
-    assert n == (12 * (576 + 2048) - 30000) // 32 * 32
+    n = lib.dsa_prefill_dense_queries(C.byref(kv5), C.byref(_qs(1, 4096, 0, 24000)), 2048, 32, 576)
+    assert n == (10 * (576 + 2048) - 24000) // 32 * 32
 
 
 def test_no_alloc_topk_refuses_batches_beyond_the_static_scratch(lib):

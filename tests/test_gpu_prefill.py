@@ -99,7 +99,7 @@ def test_prefill_automatic_split_at_the_crossover(lib):
     qs = H.dsa.query_set(H.dsa.MODE_PREFILL, spec.num_queries, 0, spec.pos0)
     n = H.dsa.prefill_dense_queries(kv, qs, spec.k, spec.num_q_heads, spec.prefix_len)
     pair = 2 * (128 // (spec.num_q_heads // spec.num_kv_heads))
-    lim = 12 * (spec.prefix_len + spec.k) - spec.pos0
+    lim = 10 * (spec.prefix_len + spec.k) - spec.pos0
     assert 0 < n < spec.num_queries and n % pair == 0 and n <= lim < n + pair
     res = H.run_prefill(w)
     H.check_prefill_against_oracle(synth.to_numpy(w_cpu), res)
