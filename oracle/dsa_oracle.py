@@ -209,6 +209,28 @@ def prefill_query(w: dict, i: int, scale: float | None = None) -> dict:
 
 
 # --------------------------------------------------------------------------
+# Local sliding-window attention, the hybrid attention's local sibling
+# ("Qwen3.5在摩尔线程MTT S5000上的原生推理优化实践", section 2.3)
+# --------------------------------------------------------------------------
+def window_positions(pos: int, window: int) -> np.ndarray:
+    """Reading taken (the page names the sub-module, "局部滑动窗口注意力", and
+    gives no definition): a causal window of ``window`` positions ending at the
+    query's own, [max(0, pos - window + 1), pos]; no prefix, no selection."""
+    return np.arange(max(0, pos - window + 1), pos + 1, dtype=np.int64)
+
+
+def window_query(w: dict, pos: int, q_heads: np.ndarray, seq: int, window: int,
+                 scale: float | None = None) -> dict:
+    """Window attention of one query token at ``pos`` of sequence ``seq``."""
+    d = w["k_cache"].shape[-1]
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    positions = window_positions(pos, window)
+    out, lse = sparse_gqa_attention(q_heads, w["k_cache"], w["v_cache"], w["block_table"][seq],
+                                    positions, int(w["num_kv_heads"]), scale)
+    return {"attended": positions, "out": out, "lse": lse}
+
+
+# --------------------------------------------------------------------------
 # Cache write and block allocation (section 2.4, KDA)
 # --------------------------------------------------------------------------
 def kv_write(k_cache, v_cache, idx_cache, slot_mapping, k_new, v_new, idx_new):

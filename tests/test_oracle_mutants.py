@@ -37,6 +37,10 @@ MUTANTS = {
     "k_minus_one": ("chosen = ts[order[:k]]", "chosen = ts[order[:k - 1]]"),
     "slot_block_row_swapped": ("blk, row = divmod(int(slot), BLOCK)",
                                "row, blk = divmod(int(slot), BLOCK)"),
+    "window_one_longer": ("return np.arange(max(0, pos - window + 1), pos + 1, dtype=np.int64)",
+                          "return np.arange(max(0, pos - window), pos + 1, dtype=np.int64)"),
+    "window_excludes_self": ("return np.arange(max(0, pos - window + 1), pos + 1, dtype=np.int64)",
+                             "return np.arange(max(0, pos - window + 1), pos, dtype=np.int64)"),
     "value_rows_from_key_cache": ("vr = fetch_rows(v_cache, bt_row, positions, head=g)",
                                   "vr = fetch_rows(k_cache, bt_row, positions, head=g)"),
 }

@@ -322,6 +322,59 @@ def test_dense_limit_prefill_equals_causal_sdpa():
     assert check_dense_prefill_equals_sdpa()
 
 
+def check_window_equals_banded_sdpa(mod=O):
+    """Local sliding-window attention: every query attends [pos - W + 1, pos],
+    which is PyTorch's SDPA with a banded boolean mask; with W >= T it is the
+    causal SDPA."""
+    spec = synth.Spec("p", "prefill", 1, (150,), 0, 4, 2, 8, num_queries=150, pos0=0)
+    w = synth.to_numpy(synth.make_workload(spec, 9, "cpu"))
+    T = 150
+    i_idx = np.arange(T)[:, None]
+    j_idx = np.arange(T)[None, :]
+    for W in (37, 64, 150, 500):
+        band = torch.from_numpy((j_idx <= i_idx) & (j_idx > i_idx - W))
+        for g in range(2):
+            kr = mod.fetch_rows(w["k_cache"], w["block_table"][0], np.arange(T), head=g)
+            vr = mod.fetch_rows(w["v_cache"], w["block_table"][0], np.arange(T), head=g)
+            q = np.transpose(w["q"][:, 2 * g:2 * g + 2, :], (1, 0, 2))   # [2, T, d]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q)[None], torch.from_numpy(np.repeat(kr[None], 2, 0))[None],
+                torch.from_numpy(np.repeat(vr[None], 2, 0))[None], attn_mask=band,
+                scale=1 / math.sqrt(128))[0].numpy()
+            for i in (0, 1, 36, 37, 38, 63, 64, 65, 149):
+                r = mod.window_query(w, i, w["q"][i], 0, W)
+                if len(r["attended"]) != min(W, i + 1):
+                    return False
+                if not np.allclose(r["out"][2 * g:2 * g + 2], ref[:, i], rtol=0, atol=1e-12):
+                    return False
+    return True
+
+
+def test_window_equals_banded_sdpa():
+    assert check_window_equals_banded_sdpa()
+
+
+def check_window_of_one(mod=O):
+    """W = 1: every head's output is the query's own V row and its log-sum-exp
+    is its own scaled score."""
+    w = _small_workload(lens=(300,), batch=1, prefix_len=0, hq=4, hkv=2, k=8)
+    for pos in (0, 63, 64, 299):
+        r = mod.window_query(w, pos, w["q"][0], 0, 1)
+        for h in range(4):
+            g = h // 2
+            v = mod.fetch_rows(w["v_cache"], w["block_table"][0], np.array([pos]), head=g)[0]
+            kk = mod.fetch_rows(w["k_cache"], w["block_table"][0], np.array([pos]), head=g)[0]
+            if not np.allclose(r["out"][h], v, rtol=0, atol=1e-12):
+                return False
+            if not np.isclose(r["lse"][h], float(w["q"][0][h] @ kk) / math.sqrt(128), rtol=0, atol=1e-10):
+                return False
+    return True
+
+
+def test_window_of_one():
+    assert check_window_of_one()
+
+
 def check_block_table_permutation(mod=O):
     """Re-laying the cache under another block permutation changes nothing."""
     w = _small_workload(lens=(777,), batch=1, prefix_len=64, hq=8, hkv=2, k=100)
