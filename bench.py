@@ -116,6 +116,21 @@ def code_digest(path):
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
+WINDOW = 4096  # positions of the sliding-window sibling the bench times
+
+
+def window_decode_line(spec, lens, ms, peak, peak_kind):
+    """Decode window attention (each sequence's newest token over its last
+    WINDOW positions) against the bytes it must move: the K and V rows of the
+    window for every KV head, Q and the bf16 output."""
+    rows = sum(min(WINDOW, int(L)) for L in lens)
+    nbytes = rows * spec.num_kv_heads * 512 + 2 * len(lens) * spec.num_q_heads * 128 * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "dsa_window_attn_decode per call in a graph: window_idx_kernel + sparse_attn_kernel + "
+                      "attn_combine_kernel", "window": WINDOW, "ms": ms, "bound": "hbm", "achieved": gbs,
+            "peak": peak, "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes, "peak_kind": peak_kind}
+
+
 def profiled_attention_traffic():
     """DRAM bytes per attention call from the committed ncu record
     (profiles/decode_128k_traffic.json), or None once the attention code has
@@ -353,7 +368,9 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
              # the same attention with every query gathered (the path the automatic split
              # keeps for positions past its range), for comparison; not part of the chunk
              "attention_gather_only": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out_g,
-                                                                      None, ws_gather, n_dense=0)}
+                                                                      None, ws_gather, n_dense=0),
+             # the local sliding-window sibling on the same chunk, not part of it
+             "window": lambda: dsa.window_attn_prefill(kv, qs, w["q"], WINDOW, out_g)}
     st = torch.cuda.current_stream(dev)
     for _ in range(max(1, warmup)):
         for f in calls.values():
@@ -403,6 +420,14 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
     dense_tflops = dense_flops / (ms["attention"] * 1e-3) / 1e12 if n_dense == T else None
     attended = int(n_sel_h.sum()) + int(np.minimum(pos + 1, P).sum())
     useful_flops = 4 * attended * 128 * hq                           # Q.K and P.V over the attended rows
+    # the window form: each tile pair from the block of its first window position
+    win_flops = 0
+    for q0 in range(0, T, 2 * qt):
+        last = min(q0 + 2 * qt, T) - 1
+        c_begin = max(0, q0 - WINDOW + 1) // 64
+        blocks = last // 64 + 1 - c_begin
+        win_flops += ((blocks + 1) // 2) * 2 * 3 * 2 * 128 * 128 * 128 * hkv  # steps x tiles x products
+    win_tflops = win_flops / (ms["window"] * 1e-3) / 1e12
     # oracle on sampled rows of the chunk (rows drawn uniformly, seeded)
     cpu = None
     if cpu_seconds > 0:
@@ -440,6 +465,9 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
                                   "frac": gather_gbs / gather, "bytes": gathered,
                                   "peak_kind": f"measured in this run: random {hkv * 256}-byte bulk copies from an "
                                                f"L2-resident 32 MB buffer into shared memory (libdsa_probe.so)"},
+        "window": {"kernel": "dsa_window_attn_prefill per call: dense_attn_kernel with the window as its mask",
+                   "window": WINDOW, "ms": ms["window"], "bound": "tensor", "achieved": win_tflops, "peak": f16,
+                   "unit": "TFLOP/s", "frac": win_tflops / f16, "flops": win_flops},
         "mma_sync_bf16_peak_tflops": bf16,
         "clocks": clock_info,
         "cpu_baseline": cpu,
@@ -596,6 +624,19 @@ def run_gpu(args, rank, world, local_rank):
     reps = max(8, min(args.steps // LAYERS, 250))
     attn_ms = per_launch_ms(graph_of(attn_call), reps)
     index_ms = per_launch_ms(graph_of(index_call), reps)
+
+    # the local sliding-window sibling over the same caches: each sequence's
+    # newest token over its last WINDOW positions
+    hq_d = spec.num_q_heads
+    win_ws = [dsa.make_workspace(dsa.window_workspace_size(layers[l][1], hq_d, WINDOW), dev) for l in range(LAYERS)]
+    win_out = torch.empty_like(layers[0][2]["out"])
+
+    def win_call(l):
+        w, kv, b, ws = layers[l]
+        dsa.window_attn_decode(kv, w["q"], WINDOW, win_out, None, win_ws[l])
+
+    win_ms = per_launch_ms(graph_of(win_call), reps)
+    del win_ws
     step(0)
     torch.cuda.synchronize()
 
@@ -665,7 +706,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # --- aggregate over ranks (max time, summed tokens)
     agg = reduce_over_ranks({"ms": local_ms, "e2e_s": e2e_s, "e2e_api_s": e2e_api_s, "attn_ms": attn_ms,
-                             "index_ms": index_ms}, "max")
+                             "index_ms": index_ms, "win_ms": win_ms}, "max")
     tokens = reduce_over_ranks({"tok": float(B * args.steps), "e2e_tok": float(B * n_e2e)}, "sum")
 
     # --- prefill chunk and its peaks (rank 0)
@@ -714,6 +755,7 @@ def run_gpu(args, rank, world, local_rank):
                      "traffic": traffic, "algorithmic_bytes": ab["attention"], "ms": agg["attn_ms"],
                      "peak_kind": peak_kind},
         "indexer": {"ms": agg["index_ms"], "achieved_gbs": ab["indexer"] / (agg["index_ms"] * 1e-3) / 1e9},
+        "window_decode": window_decode_line(spec, lens, agg["win_ms"], peak, peak_kind),
         "clocks": clock_info,
         "e2e": {"value": tokens["e2e_tok"] / agg["e2e_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

@@ -175,6 +175,26 @@ def prefill_attn_workspace_size(kv: PagedKV, qs, k: int, num_q_heads: int, prefi
     return int(lib().dsa_prefill_attn_workspace_size(kv.ref, C.byref(qs), k, num_q_heads, prefix_len, n_dense))
 
 
+def window_workspace_size(kv: PagedKV, num_q_heads: int, window: int) -> int:
+    return int(lib().dsa_window_workspace_size(kv.ref, num_q_heads, window))
+
+
+def window_attn_decode(kv: PagedKV, q, window: int, out, lse=None, ws=None, softmax_scale: float | None = None):
+    """Local sliding-window attention of each sequence's newest token over its
+    last `window` positions."""
+    scale = 1.0 / math.sqrt(HEAD_DIM) if softmax_scale is None else softmax_scale
+    p, n = _ws(ws)
+    _check(lib().dsa_window_attn_decode(kv.ref, _ptr(q), int(q.shape[1]), int(window), scale, _ptr(out),
+                                        _out_dtype(out), _ptr(lse), p, n, _stream(q.device)))
+
+
+def window_attn_prefill(kv: PagedKV, qs, q, window: int, out, lse=None, softmax_scale: float | None = None):
+    """Local sliding-window attention of the prefill queries of qs."""
+    scale = 1.0 / math.sqrt(HEAD_DIM) if softmax_scale is None else softmax_scale
+    _check(lib().dsa_window_attn_prefill(kv.ref, C.byref(qs), _ptr(q), int(q.shape[1]), int(window), scale,
+                                         _ptr(out), _out_dtype(out), _ptr(lse), _stream(q.device)))
+
+
 def decode_step(kv: PagedKV, q, q_idx, prefix_len: int, k: int, scores, idx, n_sel, out, lse=None, ws=None,
                 softmax_scale: float | None = None):
     scale = 1.0 / math.sqrt(HEAD_DIM) if softmax_scale is None else softmax_scale

@@ -255,7 +255,12 @@ struct PrefillPlan {
   size_t total = 0;
 };
 
+// The dense pass addresses cache slots through a tensor map, whose dimensions
+// stop at 2^32 elements: larger pools take the gathered path only.
+bool dense_pool_ok(const dsa::KV& kv) { return (int64_t)kv.num_blocks * 64 <= (int64_t(1) << 32); }
+
 int auto_dense_queries(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_t hq, int32_t prefix) {
+  if (!dense_pool_ok(kv)) return 0;
   const int64_t lim = kDenseRatio * ((int64_t)prefix + k) - qs.pos0;
   if (lim <= 0) return 0;
   if (lim >= qs.n_q) return qs.n_q;
@@ -294,6 +299,8 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
     if (n_dense < -1 || n_dense > qs.n_q)
       return fail(DSA_ERR_INVALID_ARG, "n_dense (%d) must be -1 (automatic) or in [0, n_q]", n_dense);
     if (n_dense < 0) n_dense = auto_dense_queries(kv, qs, k, hq, prefix);
+    if (n_dense > 0 && !dense_pool_ok(kv))
+      return fail(DSA_ERR_UNSUPPORTED, "the dense prefill pass needs num_blocks * 64 <= 2^32");
     const PrefillPlan pl = prefill_plan(kv, qs, k, hq, prefix, n_dense);
     DSA_TRY(check_ws(ws, ws_bytes, pl.total));
     DSA_TRY(ensure_setup());
@@ -343,6 +350,35 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
   a.lse = lse;
   a.ws = attn_ws(L, ws);
   DSA_CUDA("sparse attention launch", dsa::launch_sparse_attn(a, stream));
+  return DSA_OK;
+}
+
+// Local sliding-window attention (the hybrid attention's local sibling): decode
+// workspace = index lists [B][window] + counts [B] + the attention partials.
+struct WindowLayout {
+  size_t idx = 0, n_sel = 0, attn = 0, total = 0;
+  Layout L;
+};
+
+WindowLayout window_layout(const dsa::KV& kv, int32_t hq, int32_t window) {
+  WindowLayout W;
+  const dsa::QS qs{DSA_MODE_DECODE, kv.batch, 0, 0};
+  W.idx = 0;
+  W.n_sel = up256((size_t)kv.batch * (size_t)window * 4);
+  W.attn = W.n_sel + up256((size_t)kv.batch * 4);
+  W.L = layout(kv, qs, window, hq, 0);
+  W.total = W.attn + W.L.total;
+  return W;
+}
+
+dsa_status check_window_call(int32_t window, const void* q, const void* out, int32_t out_dtype, float scale) {
+  if (window < 1) return fail(DSA_ERR_INVALID_ARG, "window (%d) must be >= 1", window);
+  if (window > (1 << 24)) return fail(DSA_ERR_UNSUPPORTED, "window above 2^24");
+  if (!q || !aligned16(q) || !out || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  if (out_dtype != DSA_OUT_BF16 && out_dtype != DSA_OUT_F32)
+    return fail(DSA_ERR_INVALID_ARG, "out_dtype %d is neither DSA_OUT_BF16 nor DSA_OUT_F32", out_dtype);
+  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
   return DSA_OK;
 }
 
@@ -566,6 +602,84 @@ size_t dsa_prefill_attn_workspace_size(const dsa_paged_kv* kv_, const dsa_query_
   }
   if (n_dense < 0) n_dense = auto_dense_queries(kv, qs, k, hq, prefix);
   return prefill_plan(kv, qs, k, hq, prefix, n_dense).total;
+}
+
+size_t dsa_window_workspace_size(const dsa_paged_kv* kv_, int32_t hq, int32_t window) {
+  dsa::KV kv{};
+  if (check_kv(kv_, &kv) != DSA_OK || check_heads(hq, kv) != DSA_OK) return 0;
+  if (window < 1 || window > (1 << 24)) {
+    fail(DSA_ERR_INVALID_ARG, "window (%d) must be in [1, 2^24]", window);
+    return 0;
+  }
+  return window_layout(kv, hq, window).total;
+}
+
+dsa_status dsa_window_attn_decode(const dsa_paged_kv* kv_, const void* q, int32_t hq, int32_t window, float scale,
+                                  void* out, int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  dsa::KV kv{};
+  DSA_TRY(check_kv(kv_, &kv));
+  const dsa_query_set qs_ = {DSA_MODE_DECODE, kv.batch, 0, 0};
+  dsa::QS qs{};
+  DSA_TRY(check_qs(&qs_, kv, &qs));
+  DSA_TRY(check_heads(hq, kv));
+  DSA_TRY(check_window_call(window, q, out, out_dtype, scale));
+  DSA_TRY(check_tiles(kv, qs, window, 0));
+  const WindowLayout W = window_layout(kv, hq, window);
+  DSA_TRY(check_ws(ws, ws_bytes, W.total));
+  DSA_TRY(ensure_setup());
+  char* w = static_cast<char*>(ws);
+  int32_t* idx = reinterpret_cast<int32_t*>(w + W.idx);
+  int32_t* n_sel = reinterpret_cast<int32_t*>(w + W.n_sel);
+  DSA_CUDA("window index launch", dsa::launch_window_idx(kv, window, idx, n_sel, stream));
+  dsa::AttnArgs a;
+  a.kv = kv;
+  a.qs = qs;
+  a.q = q;
+  a.hq = hq;
+  a.idx = idx;
+  a.n_sel = n_sel;
+  a.slot = nullptr;
+  a.k = window;
+  a.prefix = 0;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.ws = attn_ws(W.L, w + W.attn);
+  DSA_CUDA("window attention launch", dsa::launch_sparse_attn(a, stream));
+  return DSA_OK;
+}
+
+dsa_status dsa_window_attn_prefill(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const void* q, int32_t hq,
+                                   int32_t window, float scale, void* out, int32_t out_dtype, float* lse,
+                                   cudaStream_t stream) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  if (qs_ && qs_->mode != DSA_MODE_PREFILL)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_window_attn_prefill needs a DSA_MODE_PREFILL query set");
+  DSA_TRY(check_qs(qs_, kv, &qs));
+  DSA_TRY(check_heads(hq, kv));
+  DSA_TRY(check_window_call(window, q, out, out_dtype, scale));
+  if (!dense_pool_ok(kv)) return fail(DSA_ERR_UNSUPPORTED, "window prefill needs num_blocks * 64 <= 2^32");
+  DSA_TRY(ensure_setup());
+  dsa::AttnArgs a;
+  a.kv = kv;
+  a.qs = qs;
+  a.q = q;
+  a.hq = hq;
+  a.idx = nullptr;
+  a.n_sel = nullptr;
+  a.slot = nullptr;
+  a.k = 0;
+  a.prefix = 0;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  DSA_CUDA("window prefill launch", dsa::launch_dense_attn(a, qs.n_q, nullptr, stream, window));
+  return DSA_OK;
 }
 
 dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t* q_idx, int32_t hq, int32_t prefix,

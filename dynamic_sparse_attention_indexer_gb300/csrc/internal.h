@@ -78,8 +78,14 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_prefix_attn(const KV& kv, const QS& qs, const void* q, int hq, int prefix, float scale,
                                float2* pre_ml, float* pre_o, cudaStream_t st);
 // Prefill attention of the first n_dense queries of the set as a masked dense
-// pass on tcgen05 (k_dense.cu); mask_ws holds dense_mask_bytes(qs, n_dense).
-cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st);
+// pass on tcgen05 (k_dense.cu).  window <= 0: the attended sets of the
+// selections (a.idx, a.n_sel, a.prefix), with mask_ws holding
+// dense_mask_bytes(qs, n_dense); window > 0: the causal window of that many
+// positions ending at each query (no workspace).
+cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st, int window = 0);
+// Decode window attention's index lists: idx[b][j] = L_b - min(window, L_b) + j,
+// n_sel[b] = min(window, L_b), -1 past it (k_misc.cu).
+cudaError_t launch_window_idx(const KV& kv, int window, int32_t* idx, int32_t* n_sel, cudaStream_t st);
 size_t dense_mask_bytes(const QS& qs, int n_dense);
 int dense_tile_queries(int group);
 cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,

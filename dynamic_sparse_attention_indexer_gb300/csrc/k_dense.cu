@@ -88,6 +88,7 @@ struct DenseParams {
   void* out;
   float* lse;
   int num_blocks, n_dense, nq_pad, pos0, hq, hkv, group, qt, n_super, out_dtype;
+  int window;  // > 0: the attended set is the causal window [pos - window + 1, pos] (no bitmap)
   float scale_log2;
 };
 
@@ -183,9 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = (p.n_super - 1 - blockIdx.x / p.hkv) * 2 * p.qt;  // heaviest tiles first
   const int q_last = min(q0 + 2 * p.qt, p.n_dense) - 1;
   const int pos_last = p.pos0 + q_last;
-  const int nc = pos_last / kBlock + 1;  // blocks of 64 positions the tiles see
-  const int ns = (nc + 1) / 2;           // steps of two blocks
-  const int last_rows = pos_last - (ns - 1) * 2 * kBlock + 1;  // positions of the last step in range (1..128)
+  // blocks of 64 positions the tiles see: from block 0, or, with a window, from
+  // the block holding the first query's first window position
+  const int c_begin = p.window > 0 ? max(0, p.pos0 + q0 - p.window + 1) / kBlock : 0;
+  const int nc = pos_last / kBlock + 1 - c_begin;
+  const int ns = (nc + 1) / 2;  // steps of two blocks
+  const int last_rows = pos_last - c_begin * kBlock - (ns - 1) * 2 * kBlock + 1;  // positions of the last step in range (1..128)
   if (tid == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------- producer
-    const int mwords = min(2 * p.qt, p.nq_pad - q0);  // even: q0 and nq_pad are even
+    const int mwords = p.window > 0 ? 0 : min(2 * p.qt, p.nq_pad - q0);  // even: q0 and nq_pad are even
     if (lane == 0) {
       tma_prefetch_map(&qmap);
       tma_prefetch_map(&kmap);
@@ -227,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k_issued = 0, v_issued = 0;
     for (int i = 0; i < ns; ++i) {
       const int c0 = 2 * i, nb = c0 + 1 < nc ? 2 : 1;  // blocks in this step
-      if ((c0 & 31) == 0) blk_next = c0 + lane < nc ? load_block(p.bt, 0, 0, c0 + lane, p.num_blocks, &g_status) : 0;
+      if ((c0 & 31) == 0)
+        blk_next = c0 + lane < nc ? load_block(p.bt, 0, 0, c_begin + c0 + lane, p.num_blocks, &g_status) : 0;
       const int b0 = __shfl_sync(0xffffffffu, blk_next, c0 & 31);
       const int b1 = __shfl_sync(0xffffffffu, blk_next, (c0 + 1) & 31);
       const int s = i % kStages;
@@ -239,8 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < nb; ++a) {
           for (int x = 0; x < 2; ++x)
             tma_load_4d(st + x * kKVHalf + a * kKVBlockHalf, &kmap, 0, x, g, (a ? b1 : b0) * kBlock, &k_full[s]);
-          bulk_g2s(base + kOffMask + (s * 2 + a) * kMaskChunk, p.mask + (size_t)(c0 + a) * p.nq_pad + q0,
-                   (uint32_t)mwords * 8u, &k_full[s]);
+          if (mwords > 0)
+            bulk_g2s(base + kOffMask + (s * 2 + a) * kMaskChunk, p.mask + (size_t)(c_begin + c0 + a) * p.nq_pad + q0,
+                     (uint32_t)mwords * 8u, &k_full[s]);
         }
       }
       k_issued = i + 1;
@@ -353,7 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // refills the stage only after every softmax warp has read them (m_free)
       if (!(ok = warp_wait(&k_full[s], (i / kStages) & 1))) break;
       uint64_t w[2] = {0ull, 0ull};
-      if (valid) {
+      if (valid && p.window > 0) {  // the window [qpos - window + 1, qpos] within each block of the step
+        const int qpos = p.pos0 + qd;
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          const int first = (c_begin + 2 * i + a) * kBlock;
+          const int lo = max(qpos - p.window + 1 - first, 0), hi = min(qpos - first, kBlock - 1);
+          if (2 * i + a < nc && lo <= hi)
+            w[a] = (hi == kBlock - 1 ? ~0ull : (1ull << (hi + 1)) - 1ull) & ~((1ull << lo) - 1ull);
+        }
+      } else if (valid) {
         w[0] = reinterpret_cast<const uint64_t*>(base + kOffMask + (s * 2) * kMaskChunk)[mword];
         if (2 * i + 1 < nc) w[1] = reinterpret_cast<const uint64_t*>(base + kOffMask + (s * 2 + 1) * kMaskChunk)[mword];
       }
@@ -607,7 +622,7 @@ cudaError_t setup_dense_kernels() {
   return e;
 }
 
-cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st) {
+cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st, int window) {
   if (n_dense <= 0) return cudaSuccess;
   const int group = a.hq / a.kv.hkv;
   const int qt = dense_tile_queries(group);
@@ -620,11 +635,13 @@ cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cud
       !encode_rows(&kmap, a.kv.k_cache, a.kv.hkv, (uint64_t)a.kv.num_blocks * kBlock, slot_bytes, 1, kBlock) ||
       !encode_rows(&vmap, a.kv.v_cache, a.kv.hkv, (uint64_t)a.kv.num_blocks * kBlock, slot_bytes, 1, kBlock))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(mask, 0, (size_t)nq_pad * chunks * 8, st);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(dense_mask_kernel, dim3((n_dense + 7) / 8), dim3(256), 0, st, 1, a.idx, a.n_sel, a.k, a.prefix,
-                 a.qs.pos0, n_dense, nq_pad, mask);
-  if (e != cudaSuccess) return e;
+  if (window <= 0) {  // the attended-position bitmap of the selections
+    cudaError_t e = cudaMemsetAsync(mask, 0, (size_t)nq_pad * chunks * 8, st);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dense_mask_kernel, dim3((n_dense + 7) / 8), dim3(256), 0, st, 1, a.idx, a.n_sel, a.k, a.prefix,
+                   a.qs.pos0, n_dense, nq_pad, mask);
+    if (e != cudaSuccess) return e;
+  }
   DenseParams p;
   p.bt = a.kv.block_table + (size_t)a.qs.seq * a.kv.max_blocks;
   p.mask = mask;
@@ -640,6 +657,7 @@ cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cud
   p.qt = qt;
   p.n_super = (n_dense + 2 * qt - 1) / (2 * qt);
   p.out_dtype = a.out_dtype;
+  p.window = window > 0 ? window : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   return launch_pdl(p.scale_log2 > 0.f ? dense_attn_kernel<true> : dense_attn_kernel<false>,
                     dim3(p.n_super * a.kv.hkv), dim3(kThreads), kSmem, st, 1, qmap, kmap, vmap, p);

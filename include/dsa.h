@@ -247,6 +247,31 @@ int32_t dsa_prefill_dense_queries(const dsa_paged_kv* kv, const dsa_query_set* q
 size_t dsa_prefill_attn_workspace_size(const dsa_paged_kv* kv, const dsa_query_set* qs, int32_t k,
                                        int32_t num_q_heads, int32_t prefix_len, int32_t n_dense);
 
+/* ------------------------------- local sliding-window attention (sibling) --- */
+/* The hybrid attention's local sub-module ("Qwen3.5在摩尔线程MTT S5000上的原生推理
+ * 优化实践", §2.3: global sparse attention, local sliding-window attention and
+ * cross-modal attention side by side).  The page gives no definition; the
+ * reading taken: query token i at position pos_i attends the causal window
+ * [max(0, pos_i - window + 1), pos_i] of its own sequence, no prefix, no
+ * selection.  Same q / out / lse layout, head rules (num_q_heads <= 64, group
+ * <= 16) and softmax as the sparse attention above; window in [1, 2^24].
+ * Decode form: the newest token of every sequence (pos = context_len - 1),
+ * through the sparse attention kernels over the window's positions; the
+ * workspace holds the window's index lists and the attention partials,
+ * dsa_window_workspace_size bytes. */
+size_t dsa_window_workspace_size(const dsa_paged_kv* kv, int32_t num_q_heads, int32_t window);
+dsa_status dsa_window_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t num_q_heads,
+                                  int32_t window, float softmax_scale, void* out, int32_t out_dtype,
+                                  float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+/* Prefill form: the queries of `qs` (mode DSA_MODE_PREFILL) through the masked
+ * dense pass of dsa_sparse_attn_prefill, its mask the window, its position range
+ * starting at the block of each query tile's first window position; no
+ * workspace.  As there, the K and V rows of every position in a tile's range
+ * must be finite (any written cache row is). */
+dsa_status dsa_window_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q,
+                                   int32_t num_q_heads, int32_t window, float softmax_scale, void* out,
+                                   int32_t out_dtype, float* lse, cudaStream_t stream);
+
 /* ---------------------------------------------------- fused decode step --- */
 /* Steps 1-4 for one decode token per sequence, in one call: scores (written to
  * `scores`, [batch][ld]), top-k (idx, n_sel) and attention (out, lse), with the

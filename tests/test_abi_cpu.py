@@ -159,6 +159,24 @@ def test_argument_checks(lib):
         assert lib.dsa_sparse_attn_prefill_split(C.byref(kv), C.byref(qs10), 0x60000, 8, 0x80000, 0x90000, 8, 0,
                                                  0.1, n, 0xB0000, 0, None, 0xA0000, 1 << 30, None) == INVALID
     assert lib.dsa_prefill_dense_queries(C.byref(kv), C.byref(qs), 8, 8, 0) == -1   # a decode query set
+    # window attention: window >= 1, a prefill query set for the prefill form,
+    # at most 64 query heads, a large enough workspace
+    assert lib.dsa_window_attn_decode(C.byref(kv), 0x60000, 8, 0, 0.1, 0xB0000, 0, None, 0xA0000, 1 << 30,
+                                      None) == INVALID
+    assert lib.dsa_window_attn_decode(C.byref(kv8), 0x60000, 128, 16, 0.1, 0xB0000, 0, None, 0xA0000, 1 << 30,
+                                      None) == UNSUPPORTED
+    assert lib.dsa_window_attn_decode(C.byref(kv), 0x60000, 8, 16, 0.1, 0xB0000, 0, None, 0xA0000, 16,
+                                      None) == WORKSPACE
+    assert lib.dsa_window_attn_decode(C.byref(kv), 0x60008, 8, 16, 0.1, 0xB0000, 0, None, 0xA0000, 1 << 30,
+                                      None) == INVALID
+    assert lib.dsa_window_workspace_size(C.byref(kv), 8, 16) >= 2 * 16 * 4
+    assert lib.dsa_window_workspace_size(C.byref(kv), 8, 0) == 0
+    assert lib.dsa_window_attn_prefill(C.byref(kv), C.byref(qs), 0x60000, 8, 16, 0.1, 0xB0000, 0, None,
+                                       None) == INVALID
+    assert lib.dsa_window_attn_prefill(C.byref(kv), C.byref(qs10), 0x60000, 8, -3, 0.1, 0xB0000, 0, None,
+                                       None) == INVALID
+    assert lib.dsa_window_attn_prefill(C.byref(kv), C.byref(qs10), 0x60000, 8, 16, float("nan"), 0xB0000, 0,
+                                       None, None) == INVALID
     # prefill attention refuses a decode query set
     assert lib.dsa_sparse_attn_prefill(C.byref(kv), C.byref(qs), 0x60000, 8, 0x80000, 0x90000, 8, 0, 0.1,
                                        0xB0000, 0, None, None, 0, None) == INVALID
