@@ -370,7 +370,12 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
              "attention_gather_only": lambda: dsa.sparse_attn_prefill(kv, qs, w["q"], idx, n_sel, k, P, out_g,
                                                                       None, ws_gather, n_dense=0),
              # the local sliding-window sibling on the same chunk, not part of it
-             "window": lambda: dsa.window_attn_prefill(kv, qs, w["q"], WINDOW, out_g)}
+             "window": lambda: dsa.window_attn_prefill(kv, qs, w["q"], WINDOW, out_g),
+             # scores + top-k in one kernel, the scores never written (same indices;
+             # not part of the chunk, which takes the faster separate calls)
+             "select_fused": lambda: dsa.prefill_select(kv, qs, w["q_idx"], P, k, idx_f, n_sel_f)}
+    idx_f = torch.empty_like(idx)
+    n_sel_f = torch.empty_like(n_sel)
     st = torch.cuda.current_stream(dev)
     for _ in range(max(1, warmup)):
         for f in calls.values():

@@ -175,6 +175,12 @@ def prefill_attn_workspace_size(kv: PagedKV, qs, k: int, num_q_heads: int, prefi
     return int(lib().dsa_prefill_attn_workspace_size(kv.ref, C.byref(qs), k, num_q_heads, prefix_len, n_dense))
 
 
+def prefill_select(kv: PagedKV, qs, q_idx, prefix_len: int, k: int, idx, n_sel):
+    """Prefill scores and top-k in one call, the scores never materialised."""
+    _check(lib().dsa_prefill_select(kv.ref, C.byref(qs), _ptr(q_idx), prefix_len, k, _ptr(idx), _ptr(n_sel),
+                                    _stream(q_idx.device)))
+
+
 def window_workspace_size(kv: PagedKV, num_q_heads: int, window: int) -> int:
     return int(lib().dsa_window_workspace_size(kv.ref, num_q_heads, window))
 

@@ -23,7 +23,8 @@ LIB = os.path.join(PKG, "libdsa_gb300.so")
 PROBE_LIB = os.path.join(PKG, "libdsa_probe.so")
 PROBE_SOURCES = ["probe_peaks.cu"]
 SOURCES = ["api.cpp", "kv_alloc.cpp", "k_index.cu", "k_topk.cu", "k_attn.cu", "k_misc.cu",
-           "k_topk_static.cu", "k_prefix.cu", "k_dense.cu"]
+           "k_topk_static.cu", "k_prefix.cu", "k_dense.cu",
+           "k_pselect.cu"]
 HEADERS = ["common.cuh", "select.cuh", "internal.h", "attn_tile.cuh", "score_walk.cuh", "tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

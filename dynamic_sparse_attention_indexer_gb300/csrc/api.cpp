@@ -49,6 +49,7 @@ dsa_status ensure_setup() {
   if ((e = dsa::setup_attn_kernels()) != cudaSuccess) return cuda_fail("setup (attention kernels)", e);
   if ((e = dsa::setup_prefix_kernels()) != cudaSuccess) return cuda_fail("setup (prefix kernel)", e);
   if ((e = dsa::setup_dense_kernels()) != cudaSuccess) return cuda_fail("setup (dense prefill kernel)", e);
+  if ((e = dsa::setup_pselect_kernels()) != cudaSuccess) return cuda_fail("setup (fused prefill selection)", e);
   done[dev] = true;
   return DSA_OK;
 }
@@ -449,6 +450,7 @@ dsa_status dsa_check_device_status(cudaStream_t stream, int32_t* code) {
   DSA_CUDA("status (prefix attention)", dsa::read_clear_status_prefix(&c, stream));
   DSA_CUDA("status (cache)", dsa::read_clear_status_misc(&c, stream));
   DSA_CUDA("status (dense prefill attention)", dsa::read_clear_status_dense(&c, stream));
+  DSA_CUDA("status (fused prefill selection)", dsa::read_clear_status_pselect(&c, stream));
   *code = c;
   return DSA_OK;
 }
@@ -602,6 +604,22 @@ size_t dsa_prefill_attn_workspace_size(const dsa_paged_kv* kv_, const dsa_query_
   }
   if (n_dense < 0) n_dense = auto_dense_queries(kv, qs, k, hq, prefix);
   return prefill_plan(kv, qs, k, hq, prefix, n_dense).total;
+}
+
+dsa_status dsa_prefill_select(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const int8_t* q_idx,
+                              int32_t prefix, int32_t k, int32_t* idx, int32_t* n_sel, cudaStream_t stream) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  if (qs_ && qs_->mode != DSA_MODE_PREFILL)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_prefill_select needs a DSA_MODE_PREFILL query set");
+  DSA_TRY(check_qs(qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  if (!q_idx || !aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx must be non-NULL and 16-byte aligned");
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  DSA_TRY(ensure_setup());
+  DSA_CUDA("fused prefill selection launch", dsa::launch_prefill_select(kv, qs, q_idx, prefix, k, idx, n_sel, stream));
+  return DSA_OK;
 }
 
 size_t dsa_window_workspace_size(const dsa_paged_kv* kv_, int32_t hq, int32_t window) {

@@ -88,6 +88,9 @@ cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cud
 cudaError_t launch_window_idx(const KV& kv, int window, int32_t* idx, int32_t* n_sel, cudaStream_t st);
 size_t dense_mask_bytes(const QS& qs, int n_dense);
 int dense_tile_queries(int group);
+// Prefill index scores and top-k in one kernel, the scores never written (k_pselect.cu).
+cudaError_t launch_prefill_select(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix, int k, int32_t* idx,
+                                  int32_t* n_sel, cudaStream_t st);
 cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
                             const int8_t* idx_k, cudaStream_t st);
 cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, const int32_t* n_sel, int k,
@@ -99,6 +102,7 @@ cudaError_t setup_topk_kernels();
 cudaError_t setup_attn_kernels();
 cudaError_t setup_prefix_kernels();
 cudaError_t setup_dense_kernels();
+cudaError_t setup_pselect_kernels();
 
 // Device status words, one per kernel file: each reads its word into *code
 // (if *code is still 0) and clears it.
@@ -108,6 +112,7 @@ cudaError_t read_clear_status_attn(int* code, cudaStream_t st);
 cudaError_t read_clear_status_prefix(int* code, cudaStream_t st);
 cudaError_t read_clear_status_misc(int* code, cudaStream_t st);
 cudaError_t read_clear_status_dense(int* code, cudaStream_t st);
+cudaError_t read_clear_status_pselect(int* code, cudaStream_t st);
 
 // Used by the allocation-free top-k entry point (defined in api.cpp).
 dsa_status prepare_decode_topk(const dsa_paged_kv* kv, const int32_t* scores, int32_t ld, int32_t prefix,

@@ -159,6 +159,11 @@ def test_argument_checks(lib):
         assert lib.dsa_sparse_attn_prefill_split(C.byref(kv), C.byref(qs10), 0x60000, 8, 0x80000, 0x90000, 8, 0,
                                                  0.1, n, 0xB0000, 0, None, 0xA0000, 1 << 30, None) == INVALID
     assert lib.dsa_prefill_dense_queries(C.byref(kv), C.byref(qs), 8, 8, 0) == -1   # a decode query set
+    # fused prefill selection: a prefill query set, k >= 1, aligned q_idx, outputs present
+    assert lib.dsa_prefill_select(C.byref(kv), C.byref(qs), 0x60000, 0, 8, 0x80000, 0x90000, None) == INVALID
+    assert lib.dsa_prefill_select(C.byref(kv), C.byref(qs10), 0x60000, 0, 0, 0x80000, 0x90000, None) == INVALID
+    assert lib.dsa_prefill_select(C.byref(kv), C.byref(qs10), 0x60004, 0, 8, 0x80000, 0x90000, None) == INVALID
+    assert lib.dsa_prefill_select(C.byref(kv), C.byref(qs10), 0x60000, 0, 8, None, 0x90000, None) == INVALID
     # window attention: window >= 1, a prefill query set for the prefill form,
     # at most 64 query heads, a large enough workspace
     assert lib.dsa_window_attn_decode(C.byref(kv), 0x60000, 8, 0, 0.1, 0xB0000, 0, None, 0xA0000, 1 << 30,

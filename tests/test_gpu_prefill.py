@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import harness as H
+import oracle.dsa_oracle as O
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -180,3 +181,84 @@ def test_full_prefill_16k(lib):
     d = np.diff(np.where(valid, idx, np.iinfo(np.int32).max), axis=1)
     assert np.all(d[valid[:, 1:]] > 0)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ----------------------------------------------- scores + top-k in one kernel
+def _fused_select(spec, seed=5, q_idx_fill=None):
+    w_cpu = synth.make_workload(spec, seed, "cpu")
+    w_cpu["seq"] = 0
+    if q_idx_fill is not None:
+        w_cpu["q_idx"].fill_(q_idx_fill)
+    w = H.on(w_cpu, DEV)
+    kv = H.paged_kv(w)
+    T, k, P = spec.num_queries, spec.k, spec.prefix_len
+    qs = H.dsa.query_set(H.dsa.MODE_PREFILL, T, 0, spec.pos0)
+    idx = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
+    n_sel = torch.full((T,), -7, dtype=torch.int32, device=DEV)
+    H.dsa.prefill_select(kv, qs, w["q_idx"], P, k, idx, n_sel)
+    assert H.dsa.check_device_status() == 0
+    return w_cpu, idx.cpu().numpy(), n_sel.cpu().numpy()
+
+
+def _check_fused_against_oracle(w_cpu, idx, n_sel, rows=None):
+    wn = synth.to_numpy(w_cpu)
+    T = int(wn["num_queries"])
+    for i in (range(T) if rows is None else rows):
+        r = O.prefill_query(wn, i)
+        assert int(n_sel[i]) == r["n_sel"], f"n_sel of query {i}"
+        assert np.array_equal(idx[i], r["idx"]), f"idx of query {i}"
+
+
+@pytest.mark.parametrize("case", ["from_zero", "continuation", "no_prefix", "group_of_3_rows"])
+def test_fused_select_matches_oracle(lib, case):
+    """Queries with fewer candidates than k (all taken), at the edge, and with
+    a real selection in the same 128-query CTA; pass-1 window path."""
+    spec = {"from_zero": _prefill_spec(T=400, pos0=0, P=64, k=100),
+            "continuation": _prefill_spec(T=300, pos0=1000, P=100, k=256),
+            "no_prefix": _prefill_spec(T=260, pos0=0, P=0, k=40),
+            "group_of_3_rows": _prefill_spec(T=129, pos0=700, P=130, k=80, hq=24, hkv=8)}[case]
+    _check_fused_against_oracle(*_fused_select(spec))
+
+
+@pytest.mark.parametrize("lo,hi", [(-128, 127), (-16, 16), (-1, 1)])
+def test_fused_select_value_ranges(lib, lo, hi):
+    """Full int8 (f16 products, scores past the pass-1 window: the three-level
+    radix path), [-16, 16] (e4m3 products, scores up to 16384: radix path),
+    [-1, 1] (scores in [-64, 64]: heavy ties at the threshold)."""
+    spec = _prefill_spec(T=300, pos0=400, P=64, k=90, idx_lo=lo, idx_hi=hi)
+    _check_fused_against_oracle(*_fused_select(spec))
+
+
+def test_fused_select_all_ties(lib):
+    """A zero indexer query: every score 0, the k lowest candidate positions."""
+    spec = _prefill_spec(T=200, pos0=300, P=32, k=64)
+    w_cpu, idx, n_sel = _fused_select(spec, q_idx_fill=0)
+    for i in range(200):
+        pos = 300 + i
+        n = min(64, pos + 1 - 32)
+        assert int(n_sel[i]) == n
+        assert np.array_equal(idx[i][:n], np.arange(32, 32 + n)) and np.all(idx[i][n:] == -1)
+    _check_fused_against_oracle(w_cpu, idx, n_sel, rows=[0, 31, 199])
+
+
+def test_fused_select_full_16k_equals_separate_steps(lib):
+    """The 16K chunk: the fused kernel's indices and counts equal, bit for bit
+    and on every row, those of dsa_index_scores + dsa_topk_select (checked
+    against the oracle in test_full_prefill_16k), and the oracle on sampled rows."""
+    spec = synth.CONFIGS[4]
+    w = synth.make_workload(spec, 1004, DEV)
+    res = H.run_prefill(w)
+    kv = H.paged_kv(w)
+    T, k, P = spec.num_queries, spec.k, spec.prefix_len
+    qs = H.dsa.query_set(H.dsa.MODE_PREFILL, T, 0, 0)
+    idx = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
+    n_sel = torch.full((T,), -7, dtype=torch.int32, device=DEV)
+    H.dsa.prefill_select(kv, qs, w["q_idx"], P, k, idx, n_sel)
+    assert H.dsa.check_device_status() == 0
+    assert torch.equal(n_sel, res["n_sel"])
+    assert torch.equal(idx, res["idx"])
+    rows = sorted(set(np.random.default_rng(11).integers(0, T, size=24).tolist()) | {0, P, P + k, T - 1})
+    ref = H.oracle_indices_all(w, k, P, rows=rows)
+    idx_h, n_h = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for i in rows:
+        assert int(n_h[i]) == ref[i]["n_sel"] and np.array_equal(idx_h[i], ref[i]["idx"]), f"query {i}"
