@@ -209,6 +209,43 @@ def prefill_query(w: dict, i: int, scale: float | None = None) -> dict:
 
 
 # --------------------------------------------------------------------------
+# Per-KV-head indexer (section 2.4, "per head" state; the next row of the scope)
+# --------------------------------------------------------------------------
+def decode_query_heads(w: dict, b: int, scale: float | None = None) -> dict:
+    """Decode with one indexer head per KV head.  Reading taken (the article
+    keeps the KV state per head, section 2.4, and does not say whether the
+    selection is per head): KV head g has its own indexer query q_idx[b][g] and
+    keys idx_cache[block][g][row], scores, selects its own top-k, and the query
+    heads of group g attend the prefix plus that selection.
+
+    w["idx_cache"]: [num_blocks][Hkv][64][D]; w["q_idx"]: [B][Hkv][D]."""
+    d = w["k_cache"].shape[-1]
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    hkv = int(w["num_kv_heads"])
+    q_heads = w["q"][b]
+    group = q_heads.shape[0] // hkv
+    pos = int(w["context_lens"][b]) - 1
+    bt_row = w["block_table"][b]
+    P, k = int(w["prefix_len"]), int(w["k"])
+    res = {"idx": [], "n_sel": [], "scores": [], "attended": [],
+           "out": np.zeros(q_heads.shape, dtype=np.float64), "lse": np.zeros(q_heads.shape[0], dtype=np.float64)}
+    for g in range(hkv):
+        ts, s = index_scores(w["q_idx"][b][g], w["idx_cache"][:, g], bt_row, P, pos)
+        idx, n_sel = topk_select(ts, s, k)
+        positions = attended_positions(P, pos, idx, n_sel)
+        kr = fetch_rows(w["k_cache"], bt_row, positions, head=g)
+        vr = fetch_rows(w["v_cache"], bt_row, positions, head=g)
+        o, l = softmax_attention(q_heads[g * group:(g + 1) * group], kr, vr, scale)
+        res["out"][g * group:(g + 1) * group] = o
+        res["lse"][g * group:(g + 1) * group] = l
+        res["idx"].append(idx)
+        res["n_sel"].append(n_sel)
+        res["scores"].append(s)
+        res["attended"].append(positions)
+    return res
+
+
+# --------------------------------------------------------------------------
 # Local sliding-window attention, the hybrid attention's local sibling
 # ("Qwen3.5在摩尔线程MTT S5000上的原生推理优化实践", section 2.3)
 # --------------------------------------------------------------------------

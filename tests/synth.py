@@ -43,6 +43,7 @@ class Spec:
     pos0: int = 0                  # prefill: position of query 0
     spare_blocks: int = 0          # extra unused blocks in the pool
     kv_layout: str = "adjacent"    # "adjacent": K and V of a slot in one row; "separate": two arrays
+    idx_heads: int = 1             # 1: one indexer key per position; num_kv_heads: one per (position, KV head)
 
 
 # The five workloads of the headline measurement plan.
@@ -123,12 +124,15 @@ def make_workload(spec: Spec, seed: int, device="cpu") -> dict:
         mask = torch.rand((pool, BLOCK, hkv), generator=_gen(seed, "outliers", device),
                           device=device) < spec.outlier_frac
         k_cache[mask] = (k_cache[mask].float() * spec.outlier_scale).to(torch.bfloat16)
-    idx_cache = torch.randint(spec.idx_lo, spec.idx_hi + 1, (pool, BLOCK, IDX_DIM),
+    # per-head indexer: [pool][Hkv][64][64] (a head's keys of a block contiguous) and q_idx [nq][Hkv][64]
+    idx_shape = (pool, BLOCK, IDX_DIM) if spec.idx_heads == 1 else (pool, spec.idx_heads, BLOCK, IDX_DIM)
+    idx_cache = torch.randint(spec.idx_lo, spec.idx_hi + 1, idx_shape,
                               generator=_gen(seed, "idx_cache", device), device=device,
                               dtype=torch.int8)
     nq = spec.batch if spec.mode == "decode" else spec.num_queries
     q = _randn_bf16((nq, hq, HEAD_DIM), _gen(seed, "q", device), device)
-    q_idx = torch.randint(spec.idx_lo, spec.idx_hi + 1, (nq, IDX_DIM),
+    q_shape = (nq, IDX_DIM) if spec.idx_heads == 1 else (nq, spec.idx_heads, IDX_DIM)
+    q_idx = torch.randint(spec.idx_lo, spec.idx_hi + 1, q_shape,
                           generator=_gen(seed, "q_idx", device), device=device, dtype=torch.int8)
     out = {
         "spec": spec, "seed": seed, "mode": spec.mode,

@@ -41,6 +41,10 @@ MUTANTS = {
                           "return np.arange(max(0, pos - window), pos + 1, dtype=np.int64)"),
     "window_excludes_self": ("return np.arange(max(0, pos - window + 1), pos + 1, dtype=np.int64)",
                              "return np.arange(max(0, pos - window + 1), pos, dtype=np.int64)"),
+    "heads_share_head0_keys": ("ts, s = index_scores(w[\"q_idx\"][b][g], w[\"idx_cache\"][:, g], bt_row, P, pos)",
+                               "ts, s = index_scores(w[\"q_idx\"][b][g], w[\"idx_cache\"][:, 0], bt_row, P, pos)"),
+    "heads_attend_head0_rows": ("kr = fetch_rows(w[\"k_cache\"], bt_row, positions, head=g)",
+                                "kr = fetch_rows(w[\"k_cache\"], bt_row, positions, head=0)"),
     "value_rows_from_key_cache": ("vr = fetch_rows(v_cache, bt_row, positions, head=g)",
                                   "vr = fetch_rows(k_cache, bt_row, positions, head=g)"),
 }

@@ -375,6 +375,72 @@ def test_window_of_one():
     assert check_window_of_one()
 
 
+def _heads_workload(**kw):
+    spec = synth.small_spec(lens=(300, 190, 777), batch=3, prefix_len=64, hq=8, hkv=2, k=40, idx_heads=2, **kw)
+    return synth.to_numpy(synth.make_workload(spec, 3, "cpu"))
+
+
+def check_heads_with_equal_indexers_share_the_selection(mod=O):
+    """Per-head indexer whose heads all carry the same keys and query: every
+    head selects what the shared indexer selects, and the outputs equal the
+    shared path's (the per-head reading reduces to the pinned shared one)."""
+    w = _heads_workload()
+    w_shared = dict(w)
+    w_shared["idx_cache"] = w["idx_cache"][:, 0]
+    w_shared["q_idx"] = w["q_idx"][:, 0]
+    w_heads = dict(w)
+    w_heads["idx_cache"] = np.repeat(w["idx_cache"][:, :1], 2, axis=1)
+    w_heads["q_idx"] = np.repeat(w["q_idx"][:, :1], 2, axis=1)
+    for b in range(3):
+        r1 = mod.decode_query(w_shared, b)
+        r2 = mod.decode_query_heads(w_heads, b)
+        for g in range(2):
+            if not (np.array_equal(r2["idx"][g], r1["idx"]) and r2["n_sel"][g] == r1["n_sel"]):
+                return False
+        if not (np.allclose(r2["out"], r1["out"], rtol=0, atol=1e-12) and np.allclose(r2["lse"], r1["lse"], rtol=0, atol=1e-12)):
+            return False
+    return True
+
+
+def test_heads_with_equal_indexers_share_the_selection():
+    assert check_heads_with_equal_indexers_share_the_selection()
+
+
+def check_heads_are_independent(mod=O):
+    """Head 1's indexer query zero: all its scores tie, so it selects the k
+    lowest candidate positions, while head 0 keeps its own top-k; swapping the
+    two KV heads (caches, indexers and query heads) swaps the results."""
+    w = _heads_workload()
+    w["q_idx"] = w["q_idx"].copy()
+    w["q_idx"][:, 1] = 0
+    for b in range(3):
+        r = mod.decode_query_heads(w, b)
+        pos = int(w["context_lens"][b]) - 1
+        n = min(40, pos + 1 - 64)
+        if not (r["n_sel"][1] == n and np.array_equal(r["idx"][1][:n], np.arange(64, 64 + n))):
+            return False
+        ts, s = mod.index_scores(w["q_idx"][b][0], w["idx_cache"][:, 0], w["block_table"][b], 64, pos)
+        idx0, _ = mod.topk_select(ts, s, 40)
+        if not np.array_equal(r["idx"][0], idx0):
+            return False
+        sw = dict(w)
+        for name in ("k_cache", "v_cache"):
+            sw[name] = w[name][:, :, ::-1]
+        sw["idx_cache"] = w["idx_cache"][:, ::-1]
+        sw["q_idx"] = w["q_idx"][:, ::-1]
+        sw["q"] = np.concatenate([w["q"][:, 4:], w["q"][:, :4]], axis=1)
+        r2 = mod.decode_query_heads(sw, b)
+        if not (np.array_equal(r2["idx"][0], r["idx"][1]) and np.array_equal(r2["idx"][1], r["idx"][0])):
+            return False
+        if not np.allclose(np.concatenate([r2["out"][4:], r2["out"][:4]]), r["out"], rtol=0, atol=1e-12):
+            return False
+    return True
+
+
+def test_heads_are_independent():
+    assert check_heads_are_independent()
+
+
 def check_block_table_permutation(mod=O):
     """Re-laying the cache under another block permutation changes nothing."""
     w = _small_workload(lens=(777,), batch=1, prefix_len=64, hq=8, hkv=2, k=100)
