@@ -19,6 +19,7 @@ same run by the microbenchmarks of libdsa_probe.so.  The reference arm
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -129,6 +130,22 @@ def window_decode_line(spec, lens, ms, peak, peak_kind):
     return {"kernel": "dsa_window_attn_decode per call in a graph: window_idx_kernel + sparse_attn_kernel + "
                       "attn_combine_kernel", "window": WINDOW, "ms": ms, "bound": "hbm", "achieved": gbs,
             "peak": peak, "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes, "peak_kind": peak_kind}
+
+
+def heads_decode_line(spec, lens, n_sel_heads, ms, peak, peak_kind):
+    """The decode step with one indexer head per KV head against the bytes it
+    must move: every KV head's non-prefix indexer keys and its indexer query,
+    the block-table entries, each KV head's own K and V rows (prefix plus its
+    selection), Q, the bf16 output and the index lists."""
+    P, hkv, hq = spec.prefix_len, spec.num_kv_heads, spec.num_q_heads
+    idx_bytes = sum(max(0, L - P) * 64 * hkv + math.ceil(L / 64) * 4 for L in lens) + 64 * hkv * len(lens)
+    rows = sum(min(P, L) + int(n) for L, ns in zip(lens, n_sel_heads) for n in ns)
+    nbytes = idx_bytes + rows * 512 + 2 * len(lens) * hq * 128 * 2 + len(lens) * hkv * spec.k * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "dsa_decode_step_heads per call in a graph: head_table_kernel + the scoring, selection and "
+                      "attention kernels over (sequence, KV head) rows", "ms": ms,
+            "tokens_per_s": len(lens) / (ms * 1e-3), "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+            "frac": gbs / peak, "algorithmic_bytes": nbytes, "peak_kind": peak_kind}
 
 
 def profiled_attention_traffic():
@@ -642,6 +659,29 @@ def run_gpu(args, rank, world, local_rank):
 
     win_ms = per_launch_ms(graph_of(win_call), reps)
     del win_ws
+
+    # the per-KV-head indexer form on a workload of the same shapes whose
+    # indexer keys and queries carry one head per KV head
+    hkv_d = spec.num_kv_heads
+    wh = synth.make_workload(dataclasses.replace(spec, idx_heads=hkv_d), 4241 + 104729 * rank, dev)
+    kvh = H.paged_kv(wh)
+    hb = {"scores": torch.empty((B * hkv_d, H.round4(wh["max_context_len"])), dtype=torch.int32, device=dev),
+          "idx": torch.empty((B, hkv_d, k), dtype=torch.int32, device=dev),
+          "n_sel": torch.empty((B, hkv_d), dtype=torch.int32, device=dev)}
+    heads_ws = dsa.make_workspace(dsa.heads_workspace_size(kvh, hq_d, k, P), dev)
+
+    def heads_call(l):
+        dsa.decode_step_heads(kvh, wh["q"], wh["q_idx"], P, k, hb["scores"], hb["idx"], hb["n_sel"], win_out,
+                              None, heads_ws)
+
+    heads_call(0)
+    torch.cuda.synchronize()
+    assert dsa.check_device_status(dev) == 0
+    heads_ms = per_launch_ms(graph_of(heads_call), reps)
+    heads_lens = [int(x) for x in wh["context_lens"].tolist()]
+    heads_nsel = hb["n_sel"].tolist()
+    del wh, kvh, hb, heads_ws
+    torch.cuda.empty_cache()
     step(0)
     torch.cuda.synchronize()
 
@@ -711,7 +751,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # --- aggregate over ranks (max time, summed tokens)
     agg = reduce_over_ranks({"ms": local_ms, "e2e_s": e2e_s, "e2e_api_s": e2e_api_s, "attn_ms": attn_ms,
-                             "index_ms": index_ms, "win_ms": win_ms}, "max")
+                             "index_ms": index_ms, "win_ms": win_ms, "heads_ms": heads_ms}, "max")
     tokens = reduce_over_ranks({"tok": float(B * args.steps), "e2e_tok": float(B * n_e2e)}, "sum")
 
     # --- prefill chunk and its peaks (rank 0)
@@ -761,6 +801,7 @@ def run_gpu(args, rank, world, local_rank):
                      "peak_kind": peak_kind},
         "indexer": {"ms": agg["index_ms"], "achieved_gbs": ab["indexer"] / (agg["index_ms"] * 1e-3) / 1e9},
         "window_decode": window_decode_line(spec, lens, agg["win_ms"], peak, peak_kind),
+        "heads_decode": heads_decode_line(spec, heads_lens, heads_nsel, agg["heads_ms"], peak, peak_kind),
         "clocks": clock_info,
         "e2e": {"value": tokens["e2e_tok"] / agg["e2e_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

@@ -84,7 +84,7 @@ class PagedKV:
         self.struct = _abi.PagedKV(
             _ptr(k_cache), _ptr(v_cache), _ptr(idx_cache), _ptr(block_table), _ptr(context_lens),
             int(k_cache.shape[0]), int(k_cache.shape[1]), self.num_kv_heads, int(k_cache.shape[3]),
-            int(idx_cache.shape[2]), int(block_table.shape[1]), self.batch, self.max_context_len, row)
+            int(idx_cache.shape[-1]), int(block_table.shape[1]), self.batch, self.max_context_len, row)
 
     @property
     def ref(self):
@@ -173,6 +173,22 @@ def prefill_dense_queries(kv: PagedKV, qs, k: int, num_q_heads: int, prefix_len:
 
 def prefill_attn_workspace_size(kv: PagedKV, qs, k: int, num_q_heads: int, prefix_len: int, n_dense: int) -> int:
     return int(lib().dsa_prefill_attn_workspace_size(kv.ref, C.byref(qs), k, num_q_heads, prefix_len, n_dense))
+
+
+def heads_workspace_size(kv: PagedKV, num_q_heads: int, k: int, prefix_len: int) -> int:
+    return int(lib().dsa_heads_workspace_size(kv.ref, num_q_heads, k, prefix_len))
+
+
+def decode_step_heads(kv: PagedKV, q, q_idx, prefix_len: int, k: int, scores, idx, n_sel, out, lse=None, ws=None,
+                      softmax_scale: float | None = None):
+    """The decode step with one indexer head per KV head: q_idx [B][Hkv][64],
+    the indexer cache [blocks][Hkv][64][64], scores [B * Hkv][ld], idx
+    [B][Hkv][k], n_sel [B][Hkv]."""
+    scale = 1.0 / math.sqrt(HEAD_DIM) if softmax_scale is None else softmax_scale
+    p, n = _ws(ws)
+    _check(lib().dsa_decode_step_heads(kv.ref, _ptr(q), _ptr(q_idx), int(q.shape[1]), prefix_len, k, scale,
+                                       _ptr(scores), int(scores.stride(0)), _ptr(idx), _ptr(n_sel), _ptr(out),
+                                       _out_dtype(out), _ptr(lse), p, n, _stream(q.device)))
 
 
 def prefill_select(kv: PagedKV, qs, q_idx, prefix_len: int, k: int, idx, n_sel):

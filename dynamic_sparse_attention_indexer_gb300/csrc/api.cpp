@@ -383,6 +383,39 @@ dsa_status check_window_call(int32_t window, const void* q, const void* out, int
   return DSA_OK;
 }
 
+// Per-KV-head indexer decode: the (sequence, KV head) pairs run the scoring and
+// selection as sequences of their own (virtual block table and context lengths
+// in the workspace), the attention as one query per pair over its KV head.
+struct HeadsPlan {
+  dsa::KV kv2;    // the virtual sequences (scoring and selection)
+  dsa::QS qs2;
+  dsa::KV kva;    // the attention's view of the cache: one KV head per query
+  size_t bt2 = 0, lens2 = 0, sel = 0, total = 0;
+  Layout L;
+};
+
+dsa_status heads_plan(const dsa::KV& kv, int32_t hq, int32_t k, int32_t prefix, HeadsPlan* out) {
+  if ((int64_t)kv.batch * kv.hkv > dsa::kMaxDecodeBatch)
+    return fail(DSA_ERR_UNSUPPORTED, "per-head indexer: batch x num_kv_heads above %d", dsa::kMaxDecodeBatch);
+  if ((int64_t)kv.num_blocks * kv.hkv >= (int64_t(1) << 31) / 64)
+    return fail(DSA_ERR_UNSUPPORTED, "per-head indexer: num_blocks x num_kv_heads x 64 must stay below 2^31");
+  HeadsPlan h;
+  h.kv2 = kv;
+  h.kv2.num_blocks = kv.num_blocks * kv.hkv;
+  h.kv2.batch = kv.batch * kv.hkv;
+  h.qs2 = dsa::QS{DSA_MODE_DECODE, h.kv2.batch, 0, 0};
+  h.kva = kv;
+  h.kva.hkv = 1;
+  h.kva.adjacent = false;
+  h.bt2 = 0;
+  h.lens2 = up256((size_t)h.kv2.batch * (size_t)kv.max_blocks * 4);
+  h.sel = h.lens2 + up256((size_t)h.kv2.batch * 4);
+  h.L = layout(h.kv2, h.qs2, k, hq / kv.hkv, prefix);
+  h.total = h.sel + h.L.total;
+  *out = h;
+  return DSA_OK;
+}
+
 }  // namespace
 
 namespace dsa {
@@ -619,6 +652,70 @@ dsa_status dsa_prefill_select(const dsa_paged_kv* kv_, const dsa_query_set* qs_,
   if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
   DSA_TRY(ensure_setup());
   DSA_CUDA("fused prefill selection launch", dsa::launch_prefill_select(kv, qs, q_idx, prefix, k, idx, n_sel, stream));
+  return DSA_OK;
+}
+
+size_t dsa_heads_workspace_size(const dsa_paged_kv* kv_, int32_t hq, int32_t k, int32_t prefix) {
+  dsa::KV kv{};
+  if (check_kv(kv_, &kv) != DSA_OK || check_heads(hq, kv) != DSA_OK || check_k_prefix(k, prefix) != DSA_OK) return 0;
+  HeadsPlan h;
+  if (heads_plan(kv, hq, k, prefix, &h) != DSA_OK) return 0;
+  return h.total;
+}
+
+dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const int8_t* q_idx, int32_t hq,
+                                 int32_t prefix, int32_t k, float scale, int32_t* scores, int32_t ld, int32_t* idx,
+                                 int32_t* n_sel, void* out, int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  dsa::KV kv{};
+  DSA_TRY(check_kv(kv_, &kv));
+  const dsa_query_set qs_ = {DSA_MODE_DECODE, kv.batch, 0, 0};
+  dsa::QS qs{};
+  DSA_TRY(check_qs(&qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  DSA_TRY(check_heads(hq, kv));
+  HeadsPlan h;
+  DSA_TRY(heads_plan(kv, hq, k, prefix, &h));
+  DSA_TRY(check_tiles(kv, h.qs2, k, prefix));
+  if (!q_idx || !aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx must be non-NULL and 16-byte aligned");
+  DSA_TRY(check_scores(scores, ld, h.kv2, h.qs2));
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  if (!q || !aligned16(q) || !out || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  if (out_dtype != DSA_OUT_BF16 && out_dtype != DSA_OUT_F32)
+    return fail(DSA_ERR_INVALID_ARG, "out_dtype %d is neither DSA_OUT_BF16 nor DSA_OUT_F32", out_dtype);
+  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  DSA_TRY(check_ws(ws, ws_bytes, h.total));
+  DSA_TRY(ensure_setup());
+  char* w = static_cast<char*>(ws);
+  int32_t* bt2 = reinterpret_cast<int32_t*>(w + h.bt2);
+  int32_t* lens2 = reinterpret_cast<int32_t*>(w + h.lens2);
+  DSA_CUDA("head table launch", dsa::launch_head_table(kv, bt2, lens2, stream));
+  dsa::KV kv2 = h.kv2;
+  kv2.block_table = bt2;
+  kv2.context_lens = lens2;
+  const dsa::SelState s2 = sel_state(h.L, w + h.sel, false);  // no cache slots: they would be virtual
+  // the scoring kernel reads block ids and lengths before its dependency wait:
+  // the virtual ones come from the kernel just launched, so no early start
+  DSA_CUDA("decode index launch", dsa::launch_decode_index(kv2, q_idx, prefix, scores, ld, &s2, k, stream, false));
+  DSA_CUDA("decode selection launch", dsa::launch_decode_select(kv2, scores, ld, prefix, k, s2, idx, n_sel, stream));
+  dsa::AttnArgs a;
+  a.kv = h.kva;
+  a.qs = h.qs2;
+  a.q = q;
+  a.hq = hq / kv.hkv;
+  a.idx = idx;
+  a.n_sel = n_sel;
+  a.slot = nullptr;
+  a.k = k;
+  a.prefix = prefix;
+  a.scale = scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.ws = attn_ws(h.L, w + h.sel);
+  a.hsplit = kv.hkv;
+  DSA_CUDA("decode attention launch", dsa::launch_sparse_attn(a, stream));
   return DSA_OK;
 }
 

@@ -148,6 +148,22 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// The same launch without programmatic dependent launch: the kernel starts only
+// once the previous work of the stream has completed (for a kernel that reads
+// inputs before its dependency wait, when the previous kernel produces them).
+template <typename... Params, typename... Args>
+cudaError_t launch_ordered(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                           Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // ------------------------------------------------------------------ cp.async
 // 16-byte async copy; src_bytes = 0 writes zeros (zero fill) without reading.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {

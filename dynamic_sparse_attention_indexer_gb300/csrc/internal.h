@@ -59,11 +59,16 @@ struct AttnArgs {
   int out_dtype;
   float* lse;
   AttnWs ws;
+  int hsplit = 1;  // decode with a per-KV-head indexer: query qi is (sequence qi / hsplit, KV head qi % hsplit)
 };
 
 // Kernel launches (return the launch error, if any).
 cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, int* scores, int ld,
-                                const SelState* sel, int k, cudaStream_t st);
+                                const SelState* sel, int k, cudaStream_t st, bool early = true);
+// Per-KV-head indexer: the virtual block table and context lengths of the
+// (sequence, KV head) pairs, bt2[b * hkv + h][j] = bt[b][j] * hkv + h (-1 for an
+// id outside the pool), lens2[b * hkv + h] = lens[b] (k_misc.cu).
+cudaError_t launch_head_table(const KV& kv, int32_t* bt2, int32_t* lens2, cudaStream_t st);
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                const SelState& sel, cudaStream_t st);
 // Whether the decode selection of this batch runs with one CTA per SM.

@@ -85,6 +85,7 @@ struct AttnParams {
   float* lse;
   const float2* pre_ml;  // prefill: the prefix part of every query, computed per tile of
   const float* pre_o;    // queries beforehand ([n_q][hq] and [n_q][hq][128]), or null
+  int hsplit;            // decode, per-KV-head indexer: query qi is (sequence qi / hsplit, head qi % hsplit)
 };
 
 // 32-bit division when the products fit (the common case), 64-bit otherwise.
@@ -99,12 +100,15 @@ __device__ __forceinline__ int cta_of(int T, int G, int x) {
 
 struct QueryInfo {
   int qi, seq, n_pre, rows;
+  int hoff;  // bf16 offset of the query's KV head inside a cache row (per-head indexer), else 0
 };
 __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi) {
   QueryInfo qf;
   qf.qi = qi;
-  qf.seq = p.mode == 0 ? qi : p.seq;
-  const int pos = p.mode == 0 ? min(__ldg(p.ctx + qi), p.max_ctx) - 1 : p.pos0 + qi;
+  const int hh = p.mode == 0 && p.hsplit > 1 ? qi % p.hsplit : 0;
+  qf.seq = p.mode == 0 ? (qi - hh) / p.hsplit : p.seq;
+  qf.hoff = hh * kHeadDim;
+  const int pos = p.mode == 0 ? min(__ldg(p.ctx + qf.seq), p.max_ctx) - 1 : p.pos0 + qi;
   qf.n_pre = p.pre_ml ? 0 : max(0, min(p.prefix, pos + 1));  // with pre_ml every row is a selected one
   qf.rows = qf.n_pre + min(max(__ldg(p.nsel + qi), 0), p.k);
   return qf;
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
           if (active(t0, u)) {
             const int r = c >> shift, part = c & shift;  // part 1: the V of a separate layout
             const size_t sl = (size_t)resolve(p, v0[u]);
-            const __nv_bfloat16* src = (part ? p.vc : p.kc) + sl * p.row_stride;
+            const __nv_bfloat16* src = (part ? p.vc : p.kc) + sl * p.row_stride + t0.qf.hoff;
             bulk_g2s(st + r * p.pitch + part * p.v_off, src, p.cbytes, &full[s]);
           }
         }
@@ -681,6 +685,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.pre_ml = a.ws.pre_ml;
   p.pre_o = a.ws.pre_o;
+  p.hsplit = a.hsplit > 1 ? a.hsplit : 1;
   p.rows_per_q = p.pre_ml ? a.k : a.prefix + a.k;
   p.units = (int)((long long)a.qs.n_q * p.rows_per_q);
   p.part_o = a.ws.part_o;

@@ -475,7 +475,7 @@ static int index_grid(const KV& kv, int prefix) {
 }
 
 cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, int* scores, int ld,
-                                const SelState* sel, int k, cudaStream_t st) {
+                                const SelState* sel, int k, cudaStream_t st, bool early) {
   DecodeIndexParams p;
   p.idx_cache = kv.idx_cache;
   p.bt = kv.block_table;
@@ -495,13 +495,14 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
   // take an SM), a smaller ring lets them be resident beside the scoring CTAs
   // before those end (measured at 128K, B = 8: step 48.3 -> 47.9 us; where the
   // selection has one CTA per SM the larger ring streams faster).
-  if (sel && !decode_select_spread(kv, prefix))
-    return launch_pdl(decode_index_kernel<true, kIdxStagesShared>, dim3(grid), dim3(kIdxThreads),
-                      idx_smem_bytes(kIdxStagesShared), st, 1, p);
-  if (sel)
-    return launch_pdl(decode_index_kernel<true, kIdxStages>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1,
-                      p);
-  return launch_pdl(decode_index_kernel<false, kIdxStages>, dim3(grid), dim3(kIdxThreads), idx_smem_bytes(), st, 1, p);
+  auto kern = sel && !decode_select_spread(kv, prefix) ? decode_index_kernel<true, kIdxStagesShared>
+               : sel                                    ? decode_index_kernel<true, kIdxStages>
+                                                        : decode_index_kernel<false, kIdxStages>;
+  const size_t smem = sel && !decode_select_spread(kv, prefix) ? idx_smem_bytes(kIdxStagesShared) : idx_smem_bytes();
+  // early = false: the block table or context lengths come from the previous
+  // kernel of the stream, so the pre-wait reads must not start before it ends.
+  if (!early) return launch_ordered(kern, dim3(grid), dim3(kIdxThreads), smem, st, p);
+  return launch_pdl(kern, dim3(grid), dim3(kIdxThreads), smem, st, 1, p);
 }
 
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,

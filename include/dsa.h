@@ -308,6 +308,33 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
                            int32_t* n_sel, void* out, int32_t out_dtype, float* lse,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------ per-KV-head indexer, decode --- */
+/* The fused decode step with one indexer head per KV head (§2.4 keeps the KV
+ * state per head; whether the selection is per head the article does not say,
+ * and dsa_decode_step reads it as one selection per token): KV head g scores
+ * its own indexer keys against its own indexer query, selects its own top-k
+ * (same rule as dsa_topk_select: ties to the lower position, the prefix never
+ * scored) and its num_q_heads / num_kv_heads query heads attend the prefix plus
+ * that selection.  Layouts that differ from dsa_decode_step:
+ *   kv->idx_cache : int8 [num_blocks][num_kv_heads][64][64] (a head's keys of a
+ *                   block contiguous)
+ *   q_idx         : int8 [batch][num_kv_heads][64]
+ *   scores        : int32 [batch * num_kv_heads][ld], ld >= max_context_len
+ *   idx, n_sel    : int32 [batch][num_kv_heads][k] and [batch][num_kv_heads]
+ * q / out / lse as in dsa_decode_step.  batch * num_kv_heads <= 2048.  The
+ * workspace (dsa_heads_workspace_size bytes) holds a virtual block table of the
+ * (sequence, head) pairs, their histograms and the attention partials.  The
+ * scoring kernel of this call starts only after the previous work of the
+ * stream has finished (its block ids come from the call's first kernel).  The
+ * attention copies each selected row per KV head (256-byte K and V pieces)
+ * instead of one piece per position. */
+size_t dsa_heads_workspace_size(const dsa_paged_kv* kv, int32_t num_q_heads, int32_t k, int32_t prefix_len);
+dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv, const void* q, const int8_t* q_idx,
+                                 int32_t num_q_heads, int32_t prefix_len, int32_t k, float softmax_scale,
+                                 int32_t* scores, int32_t ld, int32_t* idx, int32_t* n_sel, void* out,
+                                 int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
 /* ------------------------------------------- decode top-k without scratch --- */
 /* The article has no counterpart to this call.  It is for callers that cannot
  * allocate device memory: for example a plugin running inside a serving process

@@ -256,3 +256,35 @@ def test_no_alloc_topk_refuses_batches_beyond_the_static_scratch(lib):
         assert st == want, (batch, st, lib.dsa_last_error_message())
         if want == UNSUPPORTED:
             assert b"static" in lib.dsa_last_error_message()
+
+
+def test_per_head_decode_checks(lib):
+    """The per-KV-head decode step runs one selection per (sequence, KV head):
+    batch x num_kv_heads is held to the decode selection's 2048 rows, the
+    scores matrix has one row per (sequence, KV head), and the usual pointer,
+    dtype and workspace checks apply before anything reaches the GPU."""
+    import torch
+    fn = lib.dsa_decode_step_heads
+    kv = _kv()                                    # 2 sequences, 2 KV heads, contexts up to 500
+    ws = lib.dsa_heads_workspace_size(C.byref(kv), 8, 16, 0)
+    # the virtual block table (one row per (sequence, KV head)) comes first
+    assert ws >= 2 * 2 * 8 * 4 > 0
+    assert lib.dsa_heads_workspace_size(C.byref(_kv(batch=4)), 8, 16, 0) > ws
+    assert lib.dsa_heads_workspace_size(C.byref(kv), 8, 0, 0) == 0       # invalid k
+    assert lib.dsa_heads_workspace_size(C.byref(kv), 5, 16, 0) == 0      # heads not a multiple of Hkv
+    call = lambda kv=kv, q=0x60000, qi=0x70000, hq=8, k=16, ld=512, ws_bytes=ws, odt=0, scale=0.1: fn(
+        C.byref(kv), q, qi, hq, 0, k, scale, 0x80000, ld, 0x90000, 0xA0000, 0xB0000, odt, None, 0xC0000,
+        ws_bytes, None)
+    assert call(qi=0x70004) == INVALID            # misaligned indexer query
+    assert call(qi=None) == INVALID
+    assert call(q=0x60008) == INVALID             # misaligned query
+    assert call(odt=5) == INVALID
+    assert call(scale=float("inf")) == INVALID
+    assert call(ld=100) == INVALID                # a score row shorter than the longest context
+    assert call(ws_bytes=ws - 1) == WORKSPACE
+    assert call(hq=128) == UNSUPPORTED            # more than 64 query heads
+    big = _kv(batch=1025, max_context_len=500)    # 1025 x 2 (sequence, head) rows
+    assert call(kv=big, ws_bytes=1 << 40) == UNSUPPORTED
+    assert lib.dsa_heads_workspace_size(C.byref(big), 8, 16, 0) == 0
+    if not torch.cuda.is_available():
+        assert call() == CUDA                     # every argument valid: the call reaches the runtime

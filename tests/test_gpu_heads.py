@@ -1,0 +1,65 @@
+"""Decode with one indexer head per KV head on the GPU against the CPU oracle:
+each KV head's scores and selection bit-exact, its query heads' attention
+over the prefix plus that selection within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import oracle.dsa_oracle as O
+import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+dsa = H.dsa
+
+
+def _run(spec, seed=5, out_dtype=torch.bfloat16, seqs=None):
+    w_cpu = synth.make_workload(spec, seed, "cpu")
+    w = H.on(w_cpu, DEV)
+    wn = synth.to_numpy(w_cpu)
+    kv = H.paged_kv(w)
+    B, hq, hkv, k, P = spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.k, spec.prefix_len
+    ld = H.round4(int(max(w_cpu["context_lens"])))
+    scores = torch.zeros((B * hkv, ld), dtype=torch.int32, device=DEV)
+    idx = torch.full((B, hkv, k), -7, dtype=torch.int32, device=DEV)
+    n_sel = torch.full((B, hkv), -7, dtype=torch.int32, device=DEV)
+    out = torch.empty((B, hq, 128), dtype=out_dtype, device=DEV)
+    lse = torch.empty((B, hq), dtype=torch.float32, device=DEV)
+    ws = dsa.make_workspace(dsa.heads_workspace_size(kv, hq, k, P), DEV)
+    dsa.decode_step_heads(kv, w["q"], w["q_idx"], P, k, scores, idx, n_sel, out, lse, ws)
+    assert dsa.check_device_status() == 0
+    sc, ix, ns = scores.cpu().numpy(), idx.cpu().numpy(), n_sel.cpu().numpy()
+    o, ls = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b in (range(B) if seqs is None else seqs):
+        r = O.decode_query_heads(wn, b)
+        pos = int(wn["context_lens"][b]) - 1
+        for g in range(hkv):
+            if pos >= P:
+                assert np.array_equal(sc[b * hkv + g, P:pos + 1], r["scores"][g]), f"scores of sequence {b} head {g}"
+            assert int(ns[b, g]) == r["n_sel"][g], f"n_sel of sequence {b} head {g}"
+            assert np.array_equal(ix[b, g], r["idx"][g]), f"idx of sequence {b} head {g}"
+        H.assert_close(o[b], r["out"], f"out of sequence {b}")
+        H.assert_close(ls[b], r["lse"], f"lse of sequence {b}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (16, 4), (32, 2), (8, 8)])
+def test_heads_small(lib, hq, hkv):
+    """Contexts inside the prefix, at its edge, with fewer and more candidates
+    than k, over groups of 4, 4, 16 and 1 query heads."""
+    spec = synth.small_spec(lens=(40, 64, 65, 300, 777, 1500), batch=6, prefix_len=64, hq=hq, hkv=hkv, k=100,
+                            idx_heads=hkv)
+    _run(spec)
+
+
+def test_heads_fp32_separate_arrays_full_int8(lib):
+    spec = synth.small_spec(lens=(900, 2113), batch=2, prefix_len=32, hq=16, hkv=4, k=64, idx_heads=4,
+                            kv_layout="separate", idx_lo=-128, idx_hi=127)
+    _run(spec, out_dtype=torch.float32)
+
+
+def test_heads_32k(lib):
+    """B = 4 sequences of 32K positions, 8 KV heads: 32 (sequence, head)
+    selections of k = 2048 from ~31.7K candidates each, every one bit-exact."""
+    spec = synth.Spec("heads 32K", "decode", 4, (32768, 30000, 32768, 17000), 1024, 64, 8, 2048, idx_heads=8)
+    _run(spec)
