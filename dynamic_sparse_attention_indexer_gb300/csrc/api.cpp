@@ -167,8 +167,10 @@ Layout layout(const dsa::KV& kv, const dsa::QS& qs, int k, int hq, int prefix) {
     L.pre_ml = take((size_t)qs.n_q * (size_t)hq * 8);
     L.pre_o = take((size_t)qs.n_q * (size_t)hq * 128 * 4);
   }
-  L.part_o = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 128 * 4);
-  L.part_ml = take((size_t)dsa::kMaxAttnCtas * 2 * (size_t)hq * 8);
+  // two partial slots per CTA and pass; decode may walk two passes
+  const size_t slots = qs.mode == DSA_MODE_DECODE ? 4 : 2;
+  L.part_o = take((size_t)dsa::kMaxAttnCtas * slots * (size_t)hq * 128 * 4);
+  L.part_ml = take((size_t)dsa::kMaxAttnCtas * slots * (size_t)hq * 8);
   L.total = off;
   return L;
 }
@@ -179,6 +181,20 @@ dsa::SelState sel_state(const Layout& L, void* ws, bool with_slot) {
   s.coarse = reinterpret_cast<int*>(w + L.coarse);
   s.slot = with_slot ? reinterpret_cast<int*>(w + L.slot) : nullptr;
   return s;
+}
+
+// The fused decode step's overlap: the selection's clusters are capped so
+// that they hold at most half of the SMs, and the attention's first pass (the
+// prefix rows, before its wait) runs over the CTAs that find an SM free
+// while the selection runs.
+void overlap_shape(const dsa::KV& kv, int prefix, int* c_cap, int* prefix_ctas) {
+  const int sms = dsa::attn_grid_ctas();
+  int c = 16;
+  while (c > 1 && c * kv.batch > sms / 2) c >>= 1;
+  *c_cap = c;
+  const int held = dsa::decode_select_ctas(kv, prefix, c);
+  const int free_ctas = sms - held;
+  *prefix_ctas = free_ctas > sms / 4 ? free_ctas : sms / 4;
 }
 
 dsa::AttnWs attn_ws(const Layout& L, void* ws) {
@@ -698,8 +714,12 @@ dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const i
   // the scoring kernel reads block ids and lengths before its dependency wait:
   // the virtual ones come from the kernel just launched, so no early start
   DSA_CUDA("decode index launch", dsa::launch_decode_index(kv2, q_idx, prefix, scores, ld, &s2, k, stream, false));
-  DSA_CUDA("decode selection launch", dsa::launch_decode_select(kv2, scores, ld, prefix, k, s2, idx, n_sel, stream));
+  int c_cap, prefix_ctas;
+  overlap_shape(h.kv2, prefix, &c_cap, &prefix_ctas);
+  DSA_CUDA("decode selection launch",
+           dsa::launch_decode_select(kv2, scores, ld, prefix, k, s2, idx, n_sel, stream, c_cap));
   dsa::AttnArgs a;
+  a.prefix_ctas = prefix_ctas;
   a.kv = h.kva;
   a.qs = h.qs2;
   a.q = q;
@@ -820,9 +840,13 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv_, const void* q, const int8_t*
   DSA_TRY(check_ws(ws, ws_bytes, L.total));
   DSA_TRY(ensure_setup());
   const dsa::SelState s = sel_state(L, ws, true);
+  int c_cap, prefix_ctas;
+  overlap_shape(kv, prefix, &c_cap, &prefix_ctas);
   DSA_CUDA("decode index launch", dsa::launch_decode_index(kv, q_idx, prefix, scores, ld, &s, k, stream));
-  DSA_CUDA("decode selection launch", dsa::launch_decode_select(kv, scores, ld, prefix, k, s, idx, n_sel, stream));
+  DSA_CUDA("decode selection launch",
+           dsa::launch_decode_select(kv, scores, ld, prefix, k, s, idx, n_sel, stream, c_cap));
   dsa::AttnArgs a;
+  a.prefix_ctas = prefix_ctas;
   a.kv = kv;
   a.qs = qs;
   a.q = q;

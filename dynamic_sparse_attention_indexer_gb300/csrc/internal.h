@@ -40,8 +40,9 @@ constexpr int kMaxQHeads = 64;          // query heads per token the attention k
 struct AttnWs {
   float2* pre_ml;   // prefill with a prefix: [n_q][Hq] prefix part (max in log2 units, sum), else null
   float* pre_o;     // [n_q][Hq][128] its unnormalised output
-  float* part_o;    // [kMaxAttnCtas][2][Hq][128]  per-CTA partials of split queries (unnormalised O)
-  float2* part_ml;  // [kMaxAttnCtas][2][Hq]       (max in log2 units, sum of weights)
+  float* part_o;    // [kMaxAttnCtas][slots][Hq][128]  per-CTA partials of split queries (unnormalised O);
+                    // two slots per pass: 4 in decode (two passes), 2 in prefill
+  float2* part_ml;  // [kMaxAttnCtas][slots][Hq]       (max in log2 units, sum of weights)
 };
 
 struct AttnArgs {
@@ -60,6 +61,8 @@ struct AttnArgs {
   float* lse;
   AttnWs ws;
   int hsplit = 1;  // decode with a per-KV-head indexer: query qi is (sequence qi / hsplit, KV head qi % hsplit)
+  int prefix_ctas = 0;  // decode: > 0 walks the prefix rows first, over that many CTAs, before the wait on
+                        // the previous kernel (only where that kernel is the step's own selection)
 };
 
 // Kernel launches (return the launch error, if any).
@@ -73,8 +76,15 @@ cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int 
                                const SelState& sel, cudaStream_t st);
 // Whether the decode selection of this batch runs with one CTA per SM.
 bool decode_select_spread(const KV& kv, int prefix);
+// c_cap: at most that many CTAs per sequence (the fused step leaves SMs to the
+// attention's first pass).
 cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
-                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st);
+                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st,
+                                 int c_cap = 16);
+// CTAs the decode selection of this batch launches with that cap.
+int decode_select_ctas(const KV& kv, int prefix, int c_cap);
+// CTAs of the persistent attention grid on the current device.
+int attn_grid_ctas();
 cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix,
                                  int* scores, int ld, cudaStream_t st);
 cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k,

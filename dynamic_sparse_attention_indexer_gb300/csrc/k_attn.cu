@@ -77,9 +77,13 @@ struct AttnParams {
   int v_off;         // shared-memory offset of a row's V from its K: piece (adjacent) or rows * pitch
   float scale_log2;
   int units;         // n_q * rows_per_q attended-row slots (< 2^31, checked on the host)
-  int rows_per_q;    // prefix + k (k when the prefix part comes from pre_ml)
-  float* part_o;     // [grid][2 slots][hq][128]
-  float2* part_ml;   // [grid][2 slots][hq]
+  int rows_per_q;    // prefix + k (k when the prefix part comes from pre_ml); with two passes
+                     // the second pass's: max(k, min(prefix, max_ctx))
+  int two_pass;      // decode: the prefix rows first, before the wait on the previous kernel
+  int units1;        // first pass: n_q * prefix row slots, over CTAs [0, grid1)
+  int grid1;
+  float* part_o;     // [grid][passes][2 slots][hq][128]
+  float2* part_ml;   // [grid][passes][2 slots][hq]
   void* out;
   int out_dtype;
   float* lse;
@@ -102,13 +106,28 @@ struct QueryInfo {
   int qi, seq, n_pre, rows;
   int hoff;  // bf16 offset of the query's KV head inside a cache row (per-head indexer), else 0
 };
-__device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi) {
+// pass 0 (two-pass decode only): the query's prefix rows when its context
+// reaches past the prefix, else none; pass 1 then holds its selected rows, or
+// (context inside the prefix) its whole causal range.  The first pass reads
+// no selection output: it runs before the wait on the previous kernel.
+__device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi, int pass) {
   QueryInfo qf;
   qf.qi = qi;
   const int hh = p.mode == 0 && p.hsplit > 1 ? qi % p.hsplit : 0;
   qf.seq = p.mode == 0 ? (qi - hh) / p.hsplit : p.seq;
   qf.hoff = hh * kHeadDim;
   const int pos = p.mode == 0 ? min(__ldg(p.ctx + qf.seq), p.max_ctx) - 1 : p.pos0 + qi;
+  if (p.two_pass) {
+    const bool past = pos + 1 > p.prefix;
+    if (pass == 0) {
+      qf.n_pre = past ? p.prefix : 0;
+      qf.rows = qf.n_pre;
+    } else {
+      qf.n_pre = past ? 0 : max(0, pos + 1);
+      qf.rows = qf.n_pre + (past ? min(max(__ldg(p.nsel + qi), 0), p.k) : 0);
+    }
+    return qf;
+  }
   qf.n_pre = p.pre_ml ? 0 : max(0, min(p.prefix, pos + 1));  // with pre_ml every row is a selected one
   qf.rows = qf.n_pre + min(max(__ldg(p.nsel + qi), 0), p.k);
   return qf;
@@ -123,28 +142,49 @@ enum : int { kFirst = 1, kLast = 2, kWhole = 4, kHead = 8 };  // kHead: the segm
 // within one.  Empty tiles are skipped, but a segment's last tile is always
 // kept so that the segment closes.  A segment is the run of a query's rows
 // inside one CTA's range.
+// Two-pass decode walks two such sequences one after the other: first the
+// prefix row slots (P per query) over CTAs [0, grid1), then the selected-row
+// slots over every CTA; each pass leaves its own partials, and a query is
+// never written out directly (the combine merges both passes).
 struct Cursor {
-  int x, x_begin, x_end, qi, seg_start;
+  int x, x_begin, x_end, qi, seg_start, pass, rpq;
   QueryInfo qf;
   bool fresh;
 };
 struct Tile {
   QueryInfo qf;
-  int r0, nvalid, flags, slot;
+  int r0, nvalid, flags, slot;  // slot: partial index of this CTA, (pass, first / later segment)
 };
 
-__device__ __forceinline__ void cursor_init(Cursor& c, const AttnParams& p) {
-  c.x_begin = range_begin(p.units, gridDim.x, blockIdx.x);
-  c.x_end = range_begin(p.units, gridDim.x, blockIdx.x + 1);
+__device__ __forceinline__ void cursor_pass(Cursor& c, const AttnParams& p, int pass) {
+  c.pass = pass;
+  if (pass == 0) {
+    const int g1 = p.grid1;
+    c.x_begin = (int)blockIdx.x < g1 ? range_begin(p.units1, g1, blockIdx.x) : 0;
+    c.x_end = (int)blockIdx.x < g1 ? range_begin(p.units1, g1, blockIdx.x + 1) : 0;
+    c.rpq = p.prefix;
+  } else {
+    c.x_begin = range_begin(p.units, gridDim.x, blockIdx.x);
+    c.x_end = range_begin(p.units, gridDim.x, blockIdx.x + 1);
+    c.rpq = p.rows_per_q;
+  }
   c.x = c.x_begin;
   c.qi = -1;
   c.seg_start = c.x_begin;
   c.fresh = false;
 }
+__device__ __forceinline__ void cursor_init(Cursor& c, const AttnParams& p) { cursor_pass(c, p, p.two_pass ? 0 : 1); }
 
 __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* t) {
-  const int RPQ = p.rows_per_q;
-  while (c.x < c.x_end) {
+  for (;;) {
+    if (c.x >= c.x_end) {
+      if (c.pass == 1) return false;
+      // The selected rows come from the previous kernel of the stream.
+      pdl_wait();
+      cursor_pass(c, p, 1);
+      continue;
+    }
+    const int RPQ = c.rpq;
     const int x = c.x;
     const int qi = x / RPQ;
     const int r = x - qi * RPQ;
@@ -152,7 +192,7 @@ __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* 
     c.x = x + min(min(c.x_end, q_end) - x, p.rows);
     if (qi != c.qi) {
       c.qi = qi;
-      c.qf = query_info(p, qi);
+      c.qf = query_info(p, qi, c.pass);
       c.seg_start = x;
       c.fresh = true;
     }
@@ -163,13 +203,12 @@ __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* 
     t->r0 = r;
     t->nvalid = nvalid;
     t->flags = (c.fresh ? kFirst : 0) | (last ? kLast : 0) |
-               (last && c.seg_start == qi * RPQ && c.x == q_end ? kWhole : 0) |
+               (!p.two_pass && last && c.seg_start == qi * RPQ && c.x == q_end ? kWhole : 0) |
                (c.fresh && c.seg_start == qi * RPQ ? kHead : 0);
-    t->slot = c.seg_start == c.x_begin ? 0 : 1;
+    t->slot = (p.two_pass ? 2 * c.pass : 0) + (c.seg_start == c.x_begin ? 0 : 1);
     c.fresh = false;
     return true;
   }
-  return false;
 }
 
 // Cache slots are fetched two tiles ahead of their use, in up to two
@@ -237,7 +276,9 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.group;
-  if (range_begin(p.units, gridDim.x, blockIdx.x) >= range_begin(p.units, gridDim.x, blockIdx.x + 1)) return;
+  const bool none1 = !p.two_pass || (int)blockIdx.x >= p.grid1 ||
+                     range_begin(p.units1, p.grid1, blockIdx.x) >= range_begin(p.units1, p.grid1, blockIdx.x + 1);
+  if (none1 && range_begin(p.units, gridDim.x, blockIdx.x) >= range_begin(p.units, gridDim.x, blockIdx.x + 1)) return;
 
   // Set-up that touches no global memory runs before the wait on the previous kernel.
   if (tid == 0) {
@@ -251,7 +292,14 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
     mbar_fence_init();
   }
   __syncthreads();
-  pdl_wait();
+  // Two-pass decode: the prefix rows, Q, context lengths and block table are
+  // inputs no kernel of the step writes (a context inside the prefix, whose
+  // newest row the step's cache write may have just written, has its rows in
+  // the second pass), and this kernel starts only after the selection kernel
+  // has passed its own wait, i.e. after the scoring kernel and everything
+  // before it completed.  The first pass therefore runs before the wait; each
+  // thread waits when its walk reaches the second pass.
+  if (!p.two_pass) pdl_wait();
   pdl_trigger();
 
   if (warp < kProducerWarps) {
@@ -469,8 +517,6 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         ++seg;
       }
       load_q(hs, s_q, g, G, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_empty);
       reset_state(hs);
       if (p.pre_ml && (t.flags & kHead)) {
         // The query's prefix part is the starting state of the segment that
@@ -497,12 +543,17 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
     const uint8_t* sk = smem + s * kStageBytes + g * (kHeadDim * 2);
     attend_rows(hs, sk, sk + p.v_off, p.pitch, t.nvalid, p.scale_log2, lane);
     __syncwarp();
+    // The Q slot is released only after the segment's first tile of math, whose
+    // products consume the Q fragments: released right after load_q, the next
+    // segment's Q copy was seen landing in the slot while a warp still read it
+    // (measured: wrong prefix partials with one-tile segments).
+    if (lane == 0 && (t.flags & kFirst)) mbar_arrive(q_empty);
     if (lane == 0) mbar_arrive(&empty[s]);
 
     if (t.flags & kLast) {
       total_sums(hs);
       const size_t head0 = (size_t)t.qf.qi * p.hq + (size_t)g * G;
-      const size_t sl = (size_t)blockIdx.x * 2 + t.slot;
+      const size_t sl = (size_t)blockIdx.x * (p.two_pass ? 4 : 2) + t.slot;
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -634,6 +685,95 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnPa
   }
 }
 
+// Merge for two-pass decode: block (qi, hb) merges query heads hb * 4 ..
+// hb * 4 + 3 of query qi over the partials of both passes (the CTAs whose
+// prefix range and whose selected range cut the query); a head has four
+// warps as above, warp s taking the partials s, s + 4, ... of the combined list.
+__global__ void __launch_bounds__(kCombThreads) attn_combine2_kernel(const AttnParams p, int grid_ctas) {
+  __shared__ float4 s_acc[kCombHeads][kCombSplit][32];
+  __shared__ float2 s_ml[kCombHeads][kCombSplit];
+  const int qi = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hg = warp / kCombSplit, sub = warp % kCombSplit;
+  const int h = blockIdx.y * kCombHeads + hg;
+  // CTA ranges over each pass's row slots: c0 .. c0 + n0 - 1 (prefix pass, grid1
+  // CTAs), c1 .. c1 + n1 - 1 (selected pass, every CTA); the first CTA of a
+  // range holds the query in its slot 0 if its range starts with the query.
+  int n0 = 0, c0 = 0, f0 = 0;
+  if (p.grid1 > 0 && p.units1 > 0) {
+    const int first = qi * p.prefix;
+    c0 = cta_of(p.units1, p.grid1, first);
+    n0 = cta_of(p.units1, p.grid1, first + p.prefix - 1) - c0 + 1;
+    f0 = range_begin(p.units1, p.grid1, c0) >= first ? 0 : 1;
+  }
+  const int first1 = qi * p.rows_per_q;
+  const int c1 = cta_of(p.units, grid_ctas, first1);
+  const int n1 = cta_of(p.units, grid_ctas, first1 + p.rows_per_q - 1) - c1 + 1;
+  const int f1 = range_begin(p.units, grid_ctas, c1) >= first1 ? 0 : 1;
+  const int n = n0 + n1;
+  const float4* part_o = reinterpret_cast<const float4*>(p.part_o);
+  pdl_wait();
+  pdl_trigger();
+  if (h < p.hq) {
+    float M = -INFINITY, Lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = sub; i0 < n; i0 += kCombSplit * kCombBatch) {
+      float2 ml[kCombBatch];
+      float4 v[kCombBatch];
+#pragma unroll
+      for (int u = 0; u < kCombBatch; ++u) {
+        const int i = i0 + u * kCombSplit;
+        if (i < n) {
+          const int sl = i < n0 ? (c0 + i) * 4 + (i == 0 ? f0 : 0)
+                                : (c1 + i - n0) * 4 + 2 + (i == n0 ? f1 : 0);
+          const int ph = sl * p.hq + h;  // < 4 * 320 * 64
+          ml[u] = __ldg(&p.part_ml[ph]);
+          v[u] = __ldg(&part_o[ph * (kHeadDim / 4) + lane]);
+        }
+      }
+      float Mb = M;
+#pragma unroll
+      for (int u = 0; u < kCombBatch; ++u)
+        if (i0 + u * kCombSplit < n) Mb = fmaxf(Mb, ml[u].x);
+      const float Ms = Mb == -INFINITY ? 0.f : Mb;
+      const float a = exp2f(M - Ms);
+      Lsum *= a;
+      acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+#pragma unroll
+      for (int u = 0; u < kCombBatch; ++u)
+        if (i0 + u * kCombSplit < n) {
+          const float w = exp2f(ml[u].x - Ms);
+          Lsum += w * ml[u].y;
+          acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+        }
+      M = Mb;
+    }
+    s_acc[hg][sub][lane] = acc;
+    if (lane == 0) s_ml[hg][sub] = make_float2(M, Lsum);
+  }
+  __syncthreads();
+  if (h < p.hq && sub == 0) {
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kCombSplit; ++s) Mx = fmaxf(Mx, s_ml[hg][s].x);
+    const float Ms = Mx == -INFINITY ? 0.f : Mx;
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kCombSplit; ++s) {
+      const float2 st = s_ml[hg][s];
+      const float4 av = s_acc[hg][s][lane];
+      const float w = exp2f(st.x - Ms);
+      L += w * st.y;
+      o.x += w * av.x; o.y += w * av.y; o.z += w * av.z; o.w += w * av.w;
+    }
+    const float r = 1.f / L;
+    const size_t head = (size_t)qi * p.hq + h;
+    write_out4(p, head, lane, make_float4(o.x * r, o.y * r, o.z * r, o.w * r));
+    if (lane == 0 && p.lse) p.lse[head] = (Ms + log2f(L)) * 0.69314718055994531f;
+  }
+}
+
 int g_attn_grid[64] = {};
 
 }  // namespace
@@ -652,6 +792,12 @@ cudaError_t setup_attn_kernels() {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess && dev >= 0 && dev < 64) g_attn_grid[dev] = sms < kMaxAttnCtas ? sms : kMaxAttnCtas;
   return e;
+}
+
+int attn_grid_ctas() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return (dev >= 0 && dev < 64 && g_attn_grid[dev] > 0) ? g_attn_grid[dev] : 148;
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
@@ -687,6 +833,14 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.pre_o = a.ws.pre_o;
   p.hsplit = a.hsplit > 1 ? a.hsplit : 1;
   p.rows_per_q = p.pre_ml ? a.k : a.prefix + a.k;
+  p.two_pass = 0;
+  p.units1 = 0;
+  p.grid1 = 0;
+  if (a.prefix_ctas > 0 && a.qs.mode == DSA_MODE_DECODE && !p.pre_ml && a.prefix > 0 && a.kv.max_ctx > a.prefix) {
+    p.two_pass = 1;
+    p.rows_per_q = a.k > a.prefix ? a.k : a.prefix;
+    p.units1 = (int)((long long)a.qs.n_q * a.prefix);
+  }
   p.units = (int)((long long)a.qs.n_q * p.rows_per_q);
   p.part_o = a.ws.part_o;
   p.part_ml = a.ws.part_ml;
@@ -697,6 +851,10 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   cudaGetDevice(&dev);
   int grid = (dev >= 0 && dev < 64 && g_attn_grid[dev] > 0) ? g_attn_grid[dev] : 148;
   if (grid > p.units) grid = p.units;
+  if (p.two_pass) {
+    p.grid1 = a.prefix_ctas < grid ? a.prefix_ctas : grid;
+    if (p.grid1 > p.units1) p.grid1 = p.units1;
+  }
   cudaError_t e;
   if (p.pre_ml) {  // prefill: the prefix part of every query first, per tile of queries
     e = launch_prefix_attn(a.kv, a.qs, a.q, a.hq, a.prefix, a.scale, a.ws.pre_ml, a.ws.pre_o, st);
@@ -710,7 +868,11 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   else
     e = ps ? launch_pdl(sparse_attn_kernel<2, true>, dim3(grid), block, kSmemBytes, st, 1, p)
            : launch_pdl(sparse_attn_kernel<2, false>, dim3(grid), block, kSmemBytes, st, 1, p);
-  if (e != cudaSuccess || grid < 2) return e;
+  if (e != cudaSuccess) return e;
+  if (p.two_pass)
+    return launch_pdl(attn_combine2_kernel, dim3(a.qs.n_q, (a.hq + kCombHeads - 1) / kCombHeads),
+                      dim3(kCombThreads), 0, st, 1, p, grid);
+  if (grid < 2) return e;
   return launch_pdl(attn_combine_kernel, dim3(grid - 1), dim3(kCombThreads), 0, st, 1, p, grid);
 }
 

@@ -639,12 +639,13 @@ cudaError_t setup_topk_kernels() {
 }
 
 // CTAs per sequence (about one round of scores each, at most 8, 16 where
-// supported) and whether every cluster fits with one CTA per SM.
-static void select_shape(const KV& kv, int prefix, int* c_out, bool* spread) {
+// supported, at most c_cap) and whether every cluster fits with one CTA per SM.
+static void select_shape(const KV& kv, int prefix, int c_cap, int* c_out, bool* spread) {
   int dev = 0;
   cudaGetDevice(&dev);
   const bool known = dev >= 0 && dev < 64;
-  const int c_max = (known && g_sel16[dev]) ? 16 : 8;
+  int c_max = (known && g_sel16[dev]) ? 16 : 8;
+  if (c_cap < c_max) c_max = c_cap < 1 ? 1 : c_cap;
   const long long n_max = (long long)kv.max_ctx - prefix;
   int c = 1;
   while (c < c_max && n_max > (long long)c * kSelRound) c *= 2;
@@ -656,12 +657,19 @@ static void select_shape(const KV& kv, int prefix, int* c_out, bool* spread) {
 bool decode_select_spread(const KV& kv, int prefix) {
   int c;
   bool spread;
-  select_shape(kv, prefix, &c, &spread);
+  select_shape(kv, prefix, 16, &c, &spread);
   return spread;
 }
 
+int decode_select_ctas(const KV& kv, int prefix, int c_cap) {
+  int c;
+  bool spread;
+  select_shape(kv, prefix, c_cap, &c, &spread);
+  return c * kv.batch;
+}
+
 cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
-                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
+                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st, int c_cap) {
   SelectParams p;
   p.scores = scores;
   p.ctx = kv.context_lens;
@@ -682,7 +690,7 @@ cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, in
   // and give the CTA 1024 threads (8 positions each instead of 16).
   int c;
   bool spread;
-  select_shape(kv, prefix, &c, &spread);
+  select_shape(kv, prefix, c_cap, &c, &spread);
   const dim3 grid(c, kv.batch);
   if (spread) {
     const dim3 block(kSelThreadsSpread);

@@ -301,7 +301,12 @@ dsa_status dsa_window_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* 
  * kernel starts: written by host copies, by kernels launched without early
  * completion (every kernel not launched with programmatic dependent launch, and
  * dsa_kv_write), or earlier.  Everything else (the newest token's cache rows,
- * q, q_idx, the workspace and the outputs) is touched only after the wait. */
+ * q, q_idx, the workspace and the outputs) is touched only after the wait.
+ * Inside the step the attention walks every sequence's prefix rows first (of
+ * sequences whose context reaches past the prefix), while the selection still
+ * runs on part of the SMs, and the selected rows after it; by then the scoring
+ * kernel, and so every kernel before the step, has completed.  The selection's
+ * clusters are kept to at most half of the SMs to leave room for that pass. */
 dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* q_idx,
                            int32_t num_q_heads, int32_t prefix_len, int32_t k,
                            float softmax_scale, int32_t* scores, int32_t ld, int32_t* idx,

@@ -30,12 +30,17 @@ def test_decode_small_fused(lib, layout):
 
 
 def test_decode_small_split_calls_match_fused(lib):
+    """The separate calls and the fused step select the same positions; their
+    outputs agree within the attention tolerance (the fused step walks the
+    prefix rows in a pass of their own, so its partial states are merged in
+    another order)."""
     spec = synth.small_spec(lens=(3000, 513, 4100), k=300, hq=16, hkv=4)
     a = _run(spec, split_api=True)
     w = H.on(synth.make_workload(spec, 11, "cpu"), DEV)
     b = H.run_decode_step(w)
     assert torch.equal(a["idx"], b["idx"]) and torch.equal(a["n_sel"], b["n_sel"])
-    assert torch.equal(a["out"], b["out"]) and torch.equal(a["lse"], b["lse"])
+    H.assert_close(b["out"].float().cpu().numpy(), a["out"].float().cpu().numpy(), "fused out vs separate calls")
+    H.assert_close(b["lse"].cpu().numpy(), a["lse"].cpu().numpy(), "fused lse vs separate calls")
 
 
 @pytest.mark.parametrize("lens,prefix,k", [
