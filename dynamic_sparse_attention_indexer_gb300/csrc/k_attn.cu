@@ -517,6 +517,12 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         ++seg;
       }
       load_q(hs, s_q, g, G, lane);
+      // The slot is refilled by a bulk copy (async proxy): order the ldmatrix
+      // reads before it (without the proxy fence, the next segment's Q was
+      // seen landing while a warp still read the slot).
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_empty);
       reset_state(hs);
       if (p.pre_ml && (t.flags & kHead)) {
         // The query's prefix part is the starting state of the segment that
@@ -542,12 +548,8 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
     }
     const uint8_t* sk = smem + s * kStageBytes + g * (kHeadDim * 2);
     attend_rows(hs, sk, sk + p.v_off, p.pitch, t.nvalid, p.scale_log2, lane);
+    fence_proxy_async_smem();  // the stage is refilled by bulk copies as well
     __syncwarp();
-    // The Q slot is released only after the segment's first tile of math, whose
-    // products consume the Q fragments: released right after load_q, the next
-    // segment's Q copy was seen landing in the slot while a warp still read it
-    // (measured: wrong prefix partials with one-tile segments).
-    if (lane == 0 && (t.flags & kFirst)) mbar_arrive(q_empty);
     if (lane == 0) mbar_arrive(&empty[s]);
 
     if (t.flags & kLast) {

@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         w[0] = reinterpret_cast<const uint64_t*>(base + kOffMask + (s * 2) * kMaskChunk)[mword];
         if (2 * i + 1 < nc) w[1] = reinterpret_cast<const uint64_t*>(base + kOffMask + (s * 2 + 1) * kMaskChunk)[mword];
       }
+      fence_proxy_async_smem();  // the mask words are refilled by a bulk copy
       __syncwarp();
       if (lane == 0) mbar_arrive(&m_free[s]);
       // The step's 128 positions in two halves of 64.  Each half's S is read from

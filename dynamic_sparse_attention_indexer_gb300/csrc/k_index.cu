@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
         if (want_hist) atomicAdd(&whist[coarse_bin(mine)], 1);
       }
     }
+    fence_proxy_async_smem();  // the stage is refilled by bulk copies
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
