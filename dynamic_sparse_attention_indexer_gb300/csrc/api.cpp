@@ -193,6 +193,13 @@ void overlap_shape(const dsa::KV& kv, int prefix, int* c_cap, int* prefix_ctas) 
   while (c > 1 && c * kv.batch > sms / 2) c >>= 1;
   *c_cap = c;
   const int held = dsa::decode_select_ctas(kv, prefix, c);
+  if (held <= kv.batch) {
+    // one CTA per sequence: a short selection, nothing to overlap (8K, B = 32:
+    // one pass 48.5 us, two passes 48.9 us)
+    *c_cap = 16;
+    *prefix_ctas = 0;
+    return;
+  }
   const int free_ctas = sms - held;
   *prefix_ctas = free_ctas > sms / 4 ? free_ctas : sms / 4;
 }

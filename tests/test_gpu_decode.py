@@ -60,6 +60,17 @@ def test_decode_group_sizes(lib, hq, hkv, layout):
     _run(synth.small_spec(hq=hq, hkv=hkv, lens=(900, 1800), kv_layout=layout))
 
 
+@pytest.mark.parametrize("hq,hkv,layout", [(64, 8, "adjacent"), (64, 8, "separate"), (16, 2, "adjacent")])
+def test_decode_two_pass_mixed_contexts(lib, hq, hkv, layout):
+    """A long context makes the selection take several CTAs per sequence, so
+    the step walks every sequence's prefix rows in a pass of their own, before
+    its wait on the selection; beside it, contexts inside the prefix, at its
+    edge and just past it (the first two have all their rows in the second
+    pass), and prefix segments of one tile."""
+    _run(synth.small_spec(batch=5, lens=(20000, 40, 64, 65, 300), prefix_len=64, k=100, hq=hq, hkv=hkv,
+                          kv_layout=layout))
+
+
 @pytest.mark.parametrize("lens", [
     (12000, 16500),          # top-k cluster of 2 CTAs per sequence (longest context 16.5K)
     (30000, 9000, 21000),    # 4 CTAs per sequence
