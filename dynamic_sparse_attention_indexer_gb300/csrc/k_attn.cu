@@ -150,6 +150,7 @@ struct Cursor {
   int x, x_begin, x_end, qi, seg_start, pass, rpq;
   QueryInfo qf;
   bool fresh;
+  bool hold;  // stop at the end of the prefix pass instead of waiting for the second
 };
 struct Tile {
   QueryInfo qf;
@@ -173,12 +174,15 @@ __device__ __forceinline__ void cursor_pass(Cursor& c, const AttnParams& p, int 
   c.seg_start = c.x_begin;
   c.fresh = false;
 }
-__device__ __forceinline__ void cursor_init(Cursor& c, const AttnParams& p) { cursor_pass(c, p, p.two_pass ? 0 : 1); }
+__device__ __forceinline__ void cursor_init(Cursor& c, const AttnParams& p) {
+  c.hold = false;
+  cursor_pass(c, p, p.two_pass ? 0 : 1);
+}
 
 __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* t) {
   for (;;) {
     if (c.x >= c.x_end) {
-      if (c.pass == 1) return false;
+      if (c.pass == 1 || c.hold) return false;
       // The selected rows come from the previous kernel of the stream.
       pdl_wait();
       cursor_pass(c, p, 1);
@@ -323,8 +327,21 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
       auto row_of = [&](const Tile& tl, int u) {
         return tl.r0 + min((pt + u * kProducerThreads) >> shift, tl.nvalid - 1);
       };
+      // Two-pass decode: the look-ahead stops at the end of the prefix pass, so
+      // that every prefix tile goes out before the wait on the previous kernel
+      // (looking two tiles ahead into the second pass held the last prefix
+      // tiles back until the selection ended); the second phase then starts
+      // its own look-ahead behind the wait.
       Cursor cur;
       cursor_init(cur, p);
+      cur.hold = p.two_pass;
+      const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
+      int n = 0, seg = 0;
+      for (int phase = 0; phase < 2 && !*s_abort; ++phase) {
+      if (phase == 1) {
+        if (!p.two_pass) break;
+        cur.hold = false;  // the next tile switches to the second pass, after the wait
+      }
       Tile t0, t1, t2;  // issued now, next, the one after
       bool h0 = next_tile(cur, p, &t0);
       bool h1 = h0 && next_tile(cur, p, &t1);
@@ -338,8 +355,6 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         if (h0 && active(t0, u)) v0[u] = fetch_second(p, t0.qf, row_of(t0, u), fetch_first(p, t0.qf, row_of(t0, u)));
         if (h1 && active(t1, u)) f1[u] = fetch_first(p, t1.qf, row_of(t1, u));
       }
-      const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
-      int n = 0, seg = 0;
       while (h0) {
         const int s = n % kStages;
         if (n >= kStages && !mbar_wait(&empty[s], ((n / kStages) - 1) & 1)) {
@@ -388,6 +403,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         t1 = t2;
         h1 = h2;
         h2 = more && next_tile(cur, p, &t2);
+      }
       }
     } else {
       // Producer warp w < kStages issues the tiles n with n % kStages == w, all
