@@ -218,18 +218,25 @@ def decode_query_heads(w: dict, b: int, scale: float | None = None) -> dict:
     keys idx_cache[block][g][row], scores, selects its own top-k, and the query
     heads of group g attend the prefix plus that selection.
 
-    w["idx_cache"]: [num_blocks][Hkv][64][D]; w["q_idx"]: [B][Hkv][D]."""
+    w["idx_cache"]: [num_blocks][Hkv][64][D]; w["q_idx"]: [B][Hkv][D].
+
+    With w["block_table_heads"] ([Hkv][B][max_blocks], the per-head block
+    bitmaps of the KV allocator, section 2.4) head g finds its positions
+    through its own table: its indexer keys, K and V rows are the head-g
+    slices of the blocks that table names, so a physical block can hold
+    different positions for different heads."""
     d = w["k_cache"].shape[-1]
     scale = 1.0 / np.sqrt(d) if scale is None else scale
     hkv = int(w["num_kv_heads"])
     q_heads = w["q"][b]
     group = q_heads.shape[0] // hkv
     pos = int(w["context_lens"][b]) - 1
-    bt_row = w["block_table"][b]
+    tables = w.get("block_table_heads")
     P, k = int(w["prefix_len"]), int(w["k"])
     res = {"idx": [], "n_sel": [], "scores": [], "attended": [],
            "out": np.zeros(q_heads.shape, dtype=np.float64), "lse": np.zeros(q_heads.shape[0], dtype=np.float64)}
     for g in range(hkv):
+        bt_row = w["block_table"][b] if tables is None else tables[g][b]
         ts, s = index_scores(w["q_idx"][b][g], w["idx_cache"][:, g], bt_row, P, pos)
         idx, n_sel = topk_select(ts, s, k)
         positions = attended_positions(P, pos, idx, n_sel)

@@ -47,6 +47,8 @@ MUTANTS = {
                                 "kr = fetch_rows(w[\"k_cache\"], bt_row, positions, head=0)"),
     "value_rows_from_key_cache": ("vr = fetch_rows(v_cache, bt_row, positions, head=g)",
                                   "vr = fetch_rows(k_cache, bt_row, positions, head=g)"),
+    "heads_read_head0_table": ("bt_row = w[\"block_table\"][b] if tables is None else tables[g][b]",
+                               "bt_row = w[\"block_table\"][b] if tables is None else tables[0][b]"),
 }
 
 CHECKS = [getattr(pins, n) for n in dir(pins) if n.startswith("check_")]

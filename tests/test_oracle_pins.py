@@ -441,6 +441,55 @@ def test_heads_are_independent():
     assert check_heads_are_independent()
 
 
+def relocate_heads(w, seed=5):
+    """The same per-head workload re-laid out with one block table per KV head:
+    head g's slices of every block (K, V and indexer keys) move to block
+    perm_g[old id], a different permutation for each head, and head g's table
+    names the new ids.  Each physical block then holds, in its head-g slice,
+    positions that other heads keep elsewhere."""
+    nb = w["k_cache"].shape[0]
+    hkv = int(w["num_kv_heads"])
+    rng = np.random.default_rng(seed)
+    w2 = dict(w)
+    k2, v2, i2 = np.empty_like(w["k_cache"]), np.empty_like(w["v_cache"]), np.empty_like(w["idx_cache"])
+    tables = []
+    for g in range(hkv):
+        perm = rng.permutation(nb)  # old block id -> this head's new id
+        k2[perm, :, g] = w["k_cache"][:, :, g]
+        v2[perm, :, g] = w["v_cache"][:, :, g]
+        i2[perm, g] = w["idx_cache"][:, g]
+        bt = w["block_table"].copy()
+        bt[bt >= 0] = perm[bt[bt >= 0]]
+        tables.append(bt)
+    w2["k_cache"], w2["v_cache"], w2["idx_cache"] = k2, v2, i2
+    w2["block_table_heads"] = np.stack(tables)
+    return w2
+
+
+def check_heads_per_head_block_tables(mod=O):
+    """Per-head block tables (the allocator's per-head block bitmaps): each KV
+    head's data moved under its own permutation of the pool, each head reading
+    through its own table, gives the same selections and outputs as the
+    shared table over the original layout."""
+    w = _heads_workload()
+    w2 = relocate_heads(w)
+    if all(np.array_equal(w2["block_table_heads"][g], w["block_table"]) for g in range(2)):
+        return False  # the relocation must move something
+    for b in range(3):
+        r1, r2 = mod.decode_query_heads(w, b), mod.decode_query_heads(w2, b)
+        for g in range(2):
+            if not (np.array_equal(r1["idx"][g], r2["idx"][g]) and r1["n_sel"][g] == r2["n_sel"][g]
+                    and np.array_equal(r1["scores"][g], r2["scores"][g])):
+                return False
+        if not (np.array_equal(r1["out"], r2["out"]) and np.array_equal(r1["lse"], r2["lse"])):
+            return False
+    return True
+
+
+def test_heads_per_head_block_tables():
+    assert check_heads_per_head_block_tables()
+
+
 def check_block_table_permutation(mod=O):
     """Re-laying the cache under another block permutation changes nothing."""
     w = _small_workload(lens=(777,), batch=1, prefix_len=64, hq=8, hkv=2, k=100)
