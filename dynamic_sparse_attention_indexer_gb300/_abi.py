@@ -36,6 +36,12 @@ SIGNATURES = {
     "dsa_kv_free_blocks": (c_i32, [c_p, C.POINTER(c_i32), c_i32]),
     "dsa_kv_alloc_num_free": (c_i32, [c_p]),
     "dsa_kv_alloc_destroy": (None, [c_p]),
+    "dsa_kv_bitmap_create": (c_i32, [c_i32, c_i32, c_i32, c_p]),
+    "dsa_kv_bitmap_alloc": (c_i32, [c_p, c_i32, c_i32, c_i32, c_p]),
+    "dsa_kv_bitmap_free": (c_i32, [c_p, c_i32, c_i32, c_p, c_i32]),
+    "dsa_kv_bitmap_num_free": (c_i32, [c_p, c_i32, c_i32]),
+    "dsa_kv_bitmap_words": (c_i32, [c_p, c_i32, c_i32, c_p, c_i32]),
+    "dsa_kv_bitmap_destroy": (None, [c_p]),
     "dsa_kv_write": (c_i32, [PKV, c_p, c_i32, c_p, c_p, c_p, c_p]),
     "dsa_workspace_size": (C.c_size_t, [c_i32, PKV, PQS, c_i32, c_i32, c_i32]),
     "dsa_workspace_init": (c_i32, [c_p, C.c_size_t, c_p]),

@@ -138,6 +138,34 @@ dsa_status dsa_kv_free_blocks(dsa_kv_alloc* a, const int32_t* ids /* host */, in
 int32_t dsa_kv_alloc_num_free(const dsa_kv_alloc* a);
 void dsa_kv_alloc_destroy(dsa_kv_alloc* a);
 
+/* Block allocator with one block bitmap per (layer, KV head) (§2.4: the
+ * allocator knows the layer and the head and keeps an independent block bitmap
+ * per head, so that heads do not overwrite one another's blocks).  A (layer,
+ * head) holds the head-h slices of the blocks its bitmap marks, so the same
+ * block id may be held by several heads at once for different positions; the
+ * per-KV-head decode step (dsa_decode_step_heads) reads each head's blocks
+ * through that head's own block table.  Host-side, not thread-safe.
+ * create: num_layers, num_heads, num_blocks >= 1 (num_layers x num_heads <=
+ * 2^20), else DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED.
+ * alloc: the n lowest free ids of (layer, head) into out_ids (host, ascending);
+ * DSA_ERR_OOM and nothing taken when fewer are free; layer or head out of
+ * range, n < 0 or out_ids NULL with n > 0: DSA_ERR_INVALID_ARG.
+ * free: ids (host) must be held by (layer, head), each once; otherwise
+ * DSA_ERR_INVALID_ARG and nothing changes.
+ * num_free: free ids of (layer, head), -1 for a bad handle or index.
+ * words: copies the bitmap (bit i of word i / 64 set when block i is held)
+ * into words (host, at least ceil(num_blocks / 64) entries). */
+typedef struct dsa_kv_bitmap dsa_kv_bitmap;
+dsa_status dsa_kv_bitmap_create(int32_t num_layers, int32_t num_heads, int32_t num_blocks,
+                                dsa_kv_bitmap** out /* host */);
+dsa_status dsa_kv_bitmap_alloc(dsa_kv_bitmap* a, int32_t layer, int32_t head, int32_t n, int32_t* out_ids);
+dsa_status dsa_kv_bitmap_free(dsa_kv_bitmap* a, int32_t layer, int32_t head, const int32_t* ids /* host */,
+                              int32_t n);
+int32_t dsa_kv_bitmap_num_free(const dsa_kv_bitmap* a, int32_t layer, int32_t head);
+dsa_status dsa_kv_bitmap_words(const dsa_kv_bitmap* a, int32_t layer, int32_t head, uint64_t* words /* host */,
+                               int32_t n_words);
+void dsa_kv_bitmap_destroy(dsa_kv_bitmap* a);
+
 /* ------------------------------------------------------- cache write (§2.2) --- */
 /* Scatters ntok new tokens into the cache: token j goes to slot slot_mapping[j]
  * = block_id * 64 + row.  k, v: bf16 [ntok][num_kv_heads][128]; idx_k: int8
