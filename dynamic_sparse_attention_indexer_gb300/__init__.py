@@ -180,13 +180,21 @@ def heads_workspace_size(kv: PagedKV, num_q_heads: int, k: int, prefix_len: int)
 
 
 def decode_step_heads(kv: PagedKV, q, q_idx, prefix_len: int, k: int, scores, idx, n_sel, out, lse=None, ws=None,
-                      softmax_scale: float | None = None):
+                      softmax_scale: float | None = None, block_table_heads=None):
     """The decode step with one indexer head per KV head: q_idx [B][Hkv][64],
     the indexer cache [blocks][Hkv][64][64], scores [B * Hkv][ld], idx
-    [B][Hkv][k], n_sel [B][Hkv]."""
+    [B][Hkv][k], n_sel [B][Hkv]; block_table_heads: int32 [Hkv][B][max_blocks],
+    one block table per KV head, or None for the shared one."""
     scale = 1.0 / math.sqrt(HEAD_DIM) if softmax_scale is None else softmax_scale
     p, n = _ws(ws)
-    _check(lib().dsa_decode_step_heads(kv.ref, _ptr(q), _ptr(q_idx), int(q.shape[1]), prefix_len, k, scale,
+    if block_table_heads is not None:
+        hkv, B, mb = kv.num_kv_heads, kv.batch, int(kv.block_table.shape[1])
+        if (tuple(block_table_heads.shape) != (hkv, B, mb) or block_table_heads.dtype != kv.block_table.dtype
+                or not block_table_heads.is_contiguous() or block_table_heads.device != kv.block_table.device):
+            raise ValueError("block_table_heads must be a contiguous int32 [num_kv_heads][batch][max_blocks] tensor "
+                             "on the cache's device")
+    _check(lib().dsa_decode_step_heads(kv.ref, _ptr(q), _ptr(q_idx), _ptr(block_table_heads), int(q.shape[1]),
+                                       prefix_len, k, scale,
                                        _ptr(scores), int(scores.stride(0)), _ptr(idx), _ptr(n_sel), _ptr(out),
                                        _out_dtype(out), _ptr(lse), p, n, _stream(q.device)))
 

@@ -57,7 +57,7 @@ SIGNATURES = {
     "dsa_prefill_dense_queries": (c_i32, [PKV, PQS, c_i32, c_i32, c_i32]),
     "dsa_prefill_attn_workspace_size": (C.c_size_t, [PKV, PQS, c_i32, c_i32, c_i32, c_i32]),
     "dsa_heads_workspace_size": (C.c_size_t, [PKV, c_i32, c_i32, c_i32]),
-    "dsa_decode_step_heads": (c_i32, [PKV, c_p, c_p, c_i32, c_i32, c_i32, C.c_float, c_p, c_i32, c_p, c_p,
+    "dsa_decode_step_heads": (c_i32, [PKV, c_p, c_p, c_p, c_i32, c_i32, c_i32, C.c_float, c_p, c_i32, c_p, c_p,
                                       c_p, c_i32, c_p, c_p, C.c_size_t, c_p]),
     "dsa_prefill_select": (c_i32, [PKV, PQS, c_p, c_i32, c_i32, c_p, c_p, c_p]),
     "dsa_window_workspace_size": (C.c_size_t, [PKV, c_i32, c_i32]),

@@ -413,7 +413,7 @@ struct HeadsPlan {
   dsa::KV kv2;    // the virtual sequences (scoring and selection)
   dsa::QS qs2;
   dsa::KV kva;    // the attention's view of the cache: one KV head per query
-  size_t bt2 = 0, lens2 = 0, sel = 0, total = 0;
+  size_t bt2 = 0, bt3 = 0, lens2 = 0, sel = 0, total = 0;
   Layout L;
 };
 
@@ -431,7 +431,8 @@ dsa_status heads_plan(const dsa::KV& kv, int32_t hq, int32_t k, int32_t prefix, 
   h.kva.hkv = 1;
   h.kva.adjacent = false;
   h.bt2 = 0;
-  h.lens2 = up256((size_t)h.kv2.batch * (size_t)kv.max_blocks * 4);
+  h.bt3 = up256((size_t)h.kv2.batch * (size_t)kv.max_blocks * 4);
+  h.lens2 = h.bt3 + up256((size_t)h.kv2.batch * (size_t)kv.max_blocks * 4);
   h.sel = h.lens2 + up256((size_t)h.kv2.batch * 4);
   h.L = layout(h.kv2, h.qs2, k, hq / kv.hkv, prefix);
   h.total = h.sel + h.L.total;
@@ -686,8 +687,9 @@ size_t dsa_heads_workspace_size(const dsa_paged_kv* kv_, int32_t hq, int32_t k, 
   return h.total;
 }
 
-dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const int8_t* q_idx, int32_t hq,
-                                 int32_t prefix, int32_t k, float scale, int32_t* scores, int32_t ld, int32_t* idx,
+dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const int8_t* q_idx,
+                                 const int32_t* block_table_heads, int32_t hq, int32_t prefix, int32_t k, float scale,
+                                 int32_t* scores, int32_t ld, int32_t* idx,
                                  int32_t* n_sel, void* out, int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,
                                  cudaStream_t stream) {
   dsa::KV kv{};
@@ -701,6 +703,8 @@ dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const i
   DSA_TRY(heads_plan(kv, hq, k, prefix, &h));
   DSA_TRY(check_tiles(kv, h.qs2, k, prefix));
   if (!q_idx || !aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx must be non-NULL and 16-byte aligned");
+  if (block_table_heads && (reinterpret_cast<uintptr_t>(block_table_heads) & 3))
+    return fail(DSA_ERR_INVALID_ARG, "block_table_heads must be 4-byte aligned");
   DSA_TRY(check_scores(scores, ld, h.kv2, h.qs2));
   if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
   if (!q || !aligned16(q) || !out || !aligned16(out))
@@ -712,8 +716,9 @@ dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const i
   DSA_TRY(ensure_setup());
   char* w = static_cast<char*>(ws);
   int32_t* bt2 = reinterpret_cast<int32_t*>(w + h.bt2);
+  int32_t* bt3 = reinterpret_cast<int32_t*>(w + h.bt3);
   int32_t* lens2 = reinterpret_cast<int32_t*>(w + h.lens2);
-  DSA_CUDA("head table launch", dsa::launch_head_table(kv, bt2, lens2, stream));
+  DSA_CUDA("head table launch", dsa::launch_head_table(kv, block_table_heads, bt2, bt3, lens2, stream));
   dsa::KV kv2 = h.kv2;
   kv2.block_table = bt2;
   kv2.context_lens = lens2;
@@ -728,6 +733,8 @@ dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const i
   dsa::AttnArgs a;
   a.prefix_ctas = prefix_ctas;
   a.kv = h.kva;
+  a.kv.block_table = bt3;  // row b * hkv + h: head h's blocks of sequence b
+  a.bt_per_query = 1;
   a.qs = h.qs2;
   a.q = q;
   a.hq = hq / kv.hkv;

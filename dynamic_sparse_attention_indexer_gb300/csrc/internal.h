@@ -61,6 +61,7 @@ struct AttnArgs {
   float* lse;
   AttnWs ws;
   int hsplit = 1;  // decode with a per-KV-head indexer: query qi is (sequence qi / hsplit, KV head qi % hsplit)
+  int bt_per_query = 0;  // kv.block_table has one row per query (qi), not per sequence
   int prefix_ctas = 0;  // decode: > 0 walks the prefix rows first, over that many CTAs, before the wait on
                         // the previous kernel (only where that kernel is the step's own selection)
 };
@@ -71,7 +72,11 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
 // Per-KV-head indexer: the virtual block table and context lengths of the
 // (sequence, KV head) pairs, bt2[b * hkv + h][j] = bt[b][j] * hkv + h (-1 for an
 // id outside the pool), lens2[b * hkv + h] = lens[b] (k_misc.cu).
-cudaError_t launch_head_table(const KV& kv, int32_t* bt2, int32_t* lens2, cudaStream_t st);
+// bt_heads: per-head block tables [hkv][batch][max_blocks] (the per-head block
+// bitmaps of the allocator), or null for the shared table.  bt3[b * hkv + h][j]:
+// the block id itself (head h's table row), for the attention.
+cudaError_t launch_head_table(const KV& kv, const int32_t* bt_heads, int32_t* bt2, int32_t* bt3, int32_t* lens2,
+                              cudaStream_t st);
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                const SelState& sel, cudaStream_t st);
 // Whether the decode selection of this batch runs with one CTA per SM.

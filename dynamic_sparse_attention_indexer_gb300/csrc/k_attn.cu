@@ -90,6 +90,7 @@ struct AttnParams {
   const float2* pre_ml;  // prefill: the prefix part of every query, computed per tile of
   const float* pre_o;    // queries beforehand ([n_q][hq] and [n_q][hq][128]), or null
   int hsplit;            // decode, per-KV-head indexer: query qi is (sequence qi / hsplit, head qi % hsplit)
+  int bt_per_query;      // the block table has one row per query (per-head tables), not per sequence
 };
 
 // 32-bit division when the products fit (the common case), 64-bit otherwise.
@@ -104,6 +105,7 @@ __device__ __forceinline__ int cta_of(int T, int G, int x) {
 
 struct QueryInfo {
   int qi, seq, n_pre, rows;
+  int bt_row;  // row of the block table: the query's (per-head tables) or its sequence's
   int hoff;  // bf16 offset of the query's KV head inside a cache row (per-head indexer), else 0
 };
 // pass 0 (two-pass decode only): the query's prefix rows when its context
@@ -115,6 +117,7 @@ __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi, int
   qf.qi = qi;
   const int hh = p.mode == 0 && p.hsplit > 1 ? qi % p.hsplit : 0;
   qf.seq = p.mode == 0 ? (qi - hh) / p.hsplit : p.seq;
+  qf.bt_row = p.bt_per_query ? qi : qf.seq;
   qf.hoff = hh * kHeadDim;
   const int pos = p.mode == 0 ? min(__ldg(p.ctx + qf.seq), p.max_ctx) - 1 : p.pos0 + qi;
   if (p.two_pass) {
@@ -226,7 +229,7 @@ struct RowRef {
   int lo;  // row inside the block, or -1
 };
 __device__ __forceinline__ int fetch_first(const AttnParams& p, const QueryInfo& qf, int r) {
-  if (r < qf.n_pre) return __ldg(p.bt + (size_t)qf.seq * p.max_blocks + (r >> 6));
+  if (r < qf.n_pre) return __ldg(p.bt + (size_t)qf.bt_row * p.max_blocks + (r >> 6));
   const size_t e = (size_t)qf.qi * p.k + (r - qf.n_pre);
   return p.slot ? __ldg(p.slot + e) : __ldg(p.idx + e);
 }
@@ -238,7 +241,7 @@ __device__ __forceinline__ RowRef fetch_second(const AttnParams& p, const QueryI
     set_status(&g_status, kStBadBlock);
     pos = 0;
   }
-  return RowRef{__ldg(p.bt + (size_t)qf.seq * p.max_blocks + (pos >> 6)), pos & 63};
+  return RowRef{__ldg(p.bt + (size_t)qf.bt_row * p.max_blocks + (pos >> 6)), pos & 63};
 }
 __device__ __forceinline__ int resolve(const AttnParams& p, RowRef v) {
   if (v.lo < 0) {
@@ -850,6 +853,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.pre_ml = a.ws.pre_ml;
   p.pre_o = a.ws.pre_o;
   p.hsplit = a.hsplit > 1 ? a.hsplit : 1;
+  p.bt_per_query = a.bt_per_query;
   p.rows_per_q = p.pre_ml ? a.k : a.prefix + a.k;
   p.two_pass = 0;
   p.units1 = 0;

@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 typedef enum dsa_status {
   DSA_OK = 0,
@@ -360,9 +360,18 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
  * scoring kernel of this call starts only after the previous work of the
  * stream has finished (its block ids come from the call's first kernel).  The
  * attention copies each selected row per KV head (256-byte K and V pieces)
- * instead of one piece per position. */
+ * instead of one piece per position.
+ * block_table_heads (device, or NULL): one block table per KV head, int32
+ * [num_kv_heads][batch][max_blocks_per_seq], the tables of the per-(layer,
+ * head) block bitmaps (dsa_kv_bitmap_*): head g then reads its positions'
+ * indexer keys, K and V from the head-g slices of the blocks its own table
+ * names, so that one physical block can hold different positions for
+ * different heads.  NULL: every head uses kv->block_table.  Ids outside the
+ * pool are reported through the device status, as for kv->block_table.
+ * (ABI version 3 added this argument.) */
 size_t dsa_heads_workspace_size(const dsa_paged_kv* kv, int32_t num_q_heads, int32_t k, int32_t prefix_len);
 dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv, const void* q, const int8_t* q_idx,
+                                 const int32_t* block_table_heads /* device or NULL */,
                                  int32_t num_q_heads, int32_t prefix_len, int32_t k, float softmax_scale,
                                  int32_t* scores, int32_t ld, int32_t* idx, int32_t* n_sel, void* out,
                                  int32_t out_dtype, float* lse, void* ws, size_t ws_bytes,

@@ -44,6 +44,7 @@ class Spec:
     spare_blocks: int = 0          # extra unused blocks in the pool
     kv_layout: str = "adjacent"    # "adjacent": K and V of a slot in one row; "separate": two arrays
     idx_heads: int = 1             # 1: one indexer key per position; num_kv_heads: one per (position, KV head)
+    head_tables: bool = False      # per-head indexer: one block table per KV head (block_table_heads)
 
 
 # The five workloads of the headline measurement plan.
@@ -102,6 +103,18 @@ def make_workload(spec: Spec, seed: int, device="cpu") -> dict:
     for b, n in enumerate(nblk_seq):
         bt[b, :n] = perm[off:off + n]
         off += n
+    # Per-head block tables (the per-head block bitmaps of the allocator): each
+    # KV head deals its own seeded permutation of the pool in the same way, so a
+    # physical block holds, in each head's slice, positions of another sequence.
+    bt_heads = None
+    if spec.head_tables:
+        bt_heads = torch.full((spec.num_kv_heads, spec.batch, max_blocks), -1, dtype=torch.int32)
+        for h in range(spec.num_kv_heads):
+            ph = torch.randperm(pool, generator=_gen(seed, f"block_perm_head{h}", "cpu")).to(torch.int32)
+            off = 0
+            for b, n in enumerate(nblk_seq):
+                bt_heads[h, b, :n] = ph[off:off + n]
+                off += n
 
     hkv, hq = spec.num_kv_heads, spec.num_q_heads
     # The same values in either layout (each array drawn from its own stream).
@@ -146,6 +159,8 @@ def make_workload(spec: Spec, seed: int, device="cpu") -> dict:
     }
     if spec.kv_layout == "adjacent":
         out["kv"] = kv  # the one array behind the k_cache / v_cache views
+    if bt_heads is not None:
+        out["block_table_heads"] = bt_heads.to(device)
     return out
 
 

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(raw, n), f"{n} declared in dsa.h but not exported"
         assert n in _abi.SIGNATURES, f"{n} has no ctypes signature"
-    assert lib.dsa_abi_version() == 2
+    assert lib.dsa_abi_version() == 3
     assert lib.dsa_status_string(OOM) == b"DSA_ERR_OOM"
 
 
@@ -272,10 +272,11 @@ def test_per_head_decode_checks(lib):
     assert lib.dsa_heads_workspace_size(C.byref(_kv(batch=4)), 8, 16, 0) > ws
     assert lib.dsa_heads_workspace_size(C.byref(kv), 8, 0, 0) == 0       # invalid k
     assert lib.dsa_heads_workspace_size(C.byref(kv), 5, 16, 0) == 0      # heads not a multiple of Hkv
-    call = lambda kv=kv, q=0x60000, qi=0x70000, hq=8, k=16, ld=512, ws_bytes=ws, odt=0, scale=0.1: fn(
-        C.byref(kv), q, qi, hq, 0, k, scale, 0x80000, ld, 0x90000, 0xA0000, 0xB0000, odt, None, 0xC0000,
+    call = lambda kv=kv, q=0x60000, qi=0x70000, hq=8, k=16, ld=512, ws_bytes=ws, odt=0, scale=0.1, bth=None: fn(
+        C.byref(kv), q, qi, bth, hq, 0, k, scale, 0x80000, ld, 0x90000, 0xA0000, 0xB0000, odt, None, 0xC0000,
         ws_bytes, None)
     assert call(qi=0x70004) == INVALID            # misaligned indexer query
+    assert call(bth=0x50002) == INVALID           # misaligned per-head block tables
     assert call(qi=None) == INVALID
     assert call(q=0x60008) == INVALID             # misaligned query
     assert call(odt=5) == INVALID
@@ -288,3 +289,4 @@ def test_per_head_decode_checks(lib):
     assert lib.dsa_heads_workspace_size(C.byref(big), 8, 16, 0) == 0
     if not torch.cuda.is_available():
         assert call() == CUDA                     # every argument valid: the call reaches the runtime
+        assert call(bth=0x50000) == CUDA          # with per-head block tables as well

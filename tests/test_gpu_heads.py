@@ -27,7 +27,8 @@ def _run(spec, seed=5, out_dtype=torch.bfloat16, seqs=None):
     out = torch.empty((B, hq, 128), dtype=out_dtype, device=DEV)
     lse = torch.empty((B, hq), dtype=torch.float32, device=DEV)
     ws = dsa.make_workspace(dsa.heads_workspace_size(kv, hq, k, P), DEV)
-    dsa.decode_step_heads(kv, w["q"], w["q_idx"], P, k, scores, idx, n_sel, out, lse, ws)
+    dsa.decode_step_heads(kv, w["q"], w["q_idx"], P, k, scores, idx, n_sel, out, lse, ws,
+                          block_table_heads=w.get("block_table_heads"))
     assert dsa.check_device_status() == 0
     sc, ix, ns = scores.cpu().numpy(), idx.cpu().numpy(), n_sel.cpu().numpy()
     o, ls = out.float().cpu().numpy(), lse.cpu().numpy()
@@ -62,4 +63,15 @@ def test_heads_32k(lib):
     """B = 4 sequences of 32K positions, 8 KV heads: 32 (sequence, head)
     selections of k = 2048 from ~31.7K candidates each, every one bit-exact."""
     spec = synth.Spec("heads 32K", "decode", 4, (32768, 30000, 32768, 17000), 1024, 64, 8, 2048, idx_heads=8)
+    _run(spec)
+
+
+@pytest.mark.parametrize("hq,hkv,layout", [(8, 2, "adjacent"), (64, 8, "adjacent"), (16, 4, "separate")])
+def test_heads_per_head_block_tables(lib, hq, hkv, layout):
+    """One block table per KV head (the allocator's per-head block bitmaps):
+    each head reads its indexer keys, K and V from the head slices of the blocks
+    its own table names, which hold other sequences' positions for the other
+    heads.  Contexts inside and at the edge of the prefix, and a long one."""
+    spec = synth.small_spec(lens=(40, 64, 65, 777, 20000), batch=5, prefix_len=64, hq=hq, hkv=hkv, k=100,
+                            idx_heads=hkv, head_tables=True, kv_layout=layout)
     _run(spec)
