@@ -277,6 +277,24 @@ def window_query(w: dict, pos: int, q_heads: np.ndarray, seq: int, window: int,
 # --------------------------------------------------------------------------
 # Cache write and block allocation (section 2.4, KDA)
 # --------------------------------------------------------------------------
+def kv_write_heads(k_cache, v_cache, idx_cache, slot_mapping_heads, k_new, v_new, idx_new):
+    """Cache write with one slot per (token, KV head), the write side of the
+    per-head block bitmaps (section 2.4: heads must not overwrite one
+    another's blocks): token j's head-h K, V and indexer key go to the head-h
+    slice of slot slot_mapping_heads[j][h] only.  k_new, v_new: [ntok][Hkv][d];
+    idx_new: [ntok][Hkv][D]; idx_cache: [num_blocks][Hkv][64][D].  Returns
+    updated copies (inputs untouched)."""
+    kc, vc, ic = k_cache.copy(), v_cache.copy(), idx_cache.copy()
+    slots = np.asarray(slot_mapping_heads, dtype=np.int64)
+    for j in range(slots.shape[0]):
+        for h in range(slots.shape[1]):
+            blk, row = divmod(int(slots[j, h]), BLOCK)
+            kc[blk, row, h] = k_new[j, h]
+            vc[blk, row, h] = v_new[j, h]
+            ic[blk, h, row] = idx_new[j, h]
+    return kc, vc, ic
+
+
 def kv_write(k_cache, v_cache, idx_cache, slot_mapping, k_new, v_new, idx_new):
     """Scatter new tokens into their slots; slot = block_id * 64 + row.
     k_new, v_new: [ntok][Hkv][d]; idx_new: [ntok][D].  Returns updated copies

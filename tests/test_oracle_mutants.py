@@ -49,6 +49,8 @@ MUTANTS = {
                                   "vr = fetch_rows(k_cache, bt_row, positions, head=g)"),
     "heads_read_head0_table": ("bt_row = w[\"block_table\"][b] if tables is None else tables[g][b]",
                                "bt_row = w[\"block_table\"][b] if tables is None else tables[0][b]"),
+    "heads_write_every_head": ("            kc[blk, row, h] = k_new[j, h]\n",
+                               "            kc[blk, row] = k_new[j, h]\n"),
 }
 
 CHECKS = [getattr(pins, n) for n in dir(pins) if n.startswith("check_")]

@@ -551,3 +551,31 @@ def check_kv_write(mod=O):
 
 def test_kv_write_scatter():
     assert check_kv_write()
+
+
+def check_kv_write_heads(mod=O):
+    """Per-head write: each head's values land in its own slice of its own
+    slot, nothing else changes, and two heads given the same block keep both
+    their values (no write conflict between heads)."""
+    rng = np.random.default_rng(6)
+    kc = np.zeros((3, 64, 2, 8))
+    vc = np.zeros((3, 64, 2, 8))
+    ic = np.zeros((3, 2, 64, 4), dtype=np.int64)
+    slots = np.array([[5, 5], [64 * 2 + 63, 64 + 7], [64 + 1, 3]])  # token 0: both heads in slot 5
+    kn = rng.standard_normal((3, 2, 8)) + 10.0  # nonzero everywhere
+    vn = rng.standard_normal((3, 2, 8)) + 10.0
+    inn = rng.integers(1, 9, size=(3, 2, 4))
+    k2, v2, i2 = mod.kv_write_heads(kc, vc, ic, slots, kn, vn, inn)
+    ok = True
+    for j in range(3):
+        for h in range(2):
+            blk, row = divmod(int(slots[j, h]), 64)
+            ok &= np.array_equal(k2[blk, row, h], kn[j, h]) and np.array_equal(v2[blk, row, h], vn[j, h])
+            ok &= np.array_equal(i2[blk, h, row], inn[j, h])
+    ok &= np.count_nonzero(k2) == kn.size and np.count_nonzero(v2) == vn.size and np.count_nonzero(i2) == inn.size
+    ok &= np.count_nonzero(kc) == 0
+    return bool(ok)
+
+
+def test_kv_write_heads():
+    assert check_kv_write_heads()
