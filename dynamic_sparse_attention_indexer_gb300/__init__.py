@@ -121,6 +121,14 @@ def kv_write(kv: PagedKV, slot_mapping, k, v, idx_k):
                               _ptr(idx_k), _stream(kv.k_cache.device)))
 
 
+def kv_write_heads(kv: PagedKV, slot_mapping_heads, k, v, idx_k):
+    """Per-head cache write: slot_mapping_heads int32 [ntok][Hkv], k / v bf16
+    [ntok][Hkv][128], idx_k int8 [ntok][Hkv][64] (indexer cache
+    [blocks][Hkv][64][64])."""
+    _check(lib().dsa_kv_write_heads(kv.ref, _ptr(slot_mapping_heads), int(slot_mapping_heads.shape[0]), _ptr(k),
+                                    _ptr(v), _ptr(idx_k), _stream(kv.k_cache.device)))
+
+
 def index_scores(kv: PagedKV, qs, q_idx, prefix_len: int, scores, ws=None):
     p, n = _ws(ws)
     _check(lib().dsa_index_scores(kv.ref, C.byref(qs), _ptr(q_idx), prefix_len, _ptr(scores),

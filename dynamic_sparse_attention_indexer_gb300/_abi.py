@@ -43,6 +43,7 @@ SIGNATURES = {
     "dsa_kv_bitmap_words": (c_i32, [c_p, c_i32, c_i32, c_p, c_i32]),
     "dsa_kv_bitmap_destroy": (None, [c_p]),
     "dsa_kv_write": (c_i32, [PKV, c_p, c_i32, c_p, c_p, c_p, c_p]),
+    "dsa_kv_write_heads": (c_i32, [PKV, c_p, c_i32, c_p, c_p, c_p, c_p]),
     "dsa_workspace_size": (C.c_size_t, [c_i32, PKV, PQS, c_i32, c_i32, c_i32]),
     "dsa_workspace_init": (c_i32, [c_p, C.c_size_t, c_p]),
     "dsa_index_scores": (c_i32, [PKV, PQS, c_p, c_i32, c_p, c_i32, c_p, C.c_size_t, c_p]),

@@ -552,6 +552,21 @@ dsa_status dsa_kv_write(const dsa_paged_kv* kv_, const int32_t* slots, int32_t n
   return DSA_OK;
 }
 
+dsa_status dsa_kv_write_heads(const dsa_paged_kv* kv_, const int32_t* slots, int32_t ntok, const void* k,
+                              const void* v, const int8_t* idx_k, cudaStream_t stream) {
+  dsa::KV kv{};
+  DSA_TRY(check_kv(kv_, &kv));
+  if (ntok < 0) return fail(DSA_ERR_INVALID_ARG, "ntok (%d) must be >= 0", ntok);
+  if (ntok == 0) return DSA_OK;
+  if (!slots || !k || !v || !idx_k)
+    return fail(DSA_ERR_INVALID_ARG, "slot_mapping_heads, k, v and idx_k must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(slots) & 3) || !aligned16(k) || !aligned16(v) || !aligned16(idx_k))
+    return fail(DSA_ERR_INVALID_ARG, "slot_mapping_heads must be 4-byte aligned, k, v and idx_k 16-byte aligned");
+  DSA_TRY(ensure_setup());
+  DSA_CUDA("kv_write_heads launch", dsa::launch_kv_write_heads(kv, slots, ntok, k, v, idx_k, stream));
+  return DSA_OK;
+}
+
 dsa_status dsa_index_scores(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const int8_t* q_idx, int32_t prefix,
                             int32_t* scores, int32_t ld, void* ws, size_t ws_bytes, cudaStream_t stream) {
   (void)ws;

@@ -111,6 +111,10 @@ int dense_tile_queries(int group);
 // Prefill index scores and top-k in one kernel, the scores never written (k_pselect.cu).
 cudaError_t launch_prefill_select(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix, int k, int32_t* idx,
                                   int32_t* n_sel, cudaStream_t st);
+// Per-head write: slots [ntok][hkv], k / v [ntok][hkv][128], idx_k [ntok][hkv][64]
+// into the head slices (indexer cache [blocks][hkv][64][64]).
+cudaError_t launch_kv_write_heads(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
+                                  const int8_t* idx_k, cudaStream_t st);
 cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
                             const int8_t* idx_k, cudaStream_t st);
 cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, const int32_t* n_sel, int k,

@@ -55,6 +55,34 @@ __global__ void kv_write_kernel(const WriteParams p) {
   }
 }
 
+// Per-head write (the write side of the per-head block bitmaps): one CTA per
+// token, head h's K and V (16 chunks each) into the head-h slice of slot
+// slots[j][h], and its indexer key (4 chunks) into the head-h keys of that block
+// (indexer cache [blocks][hkv][64][64]).  Other heads' slices are not touched.
+__global__ void kv_write_heads_kernel(const WriteParams p) {
+  const int j = blockIdx.x;
+  for (int c = threadIdx.x; c < p.hkv * 36; c += blockDim.x) {
+    const int h = c / 36, r = c - h * 36;
+    const int slot = __ldg(p.slots + (size_t)j * p.hkv + h);
+    const int blk = slot >> 6, row = slot & 63;
+    if (slot < 0 || blk >= p.num_blocks) {
+      if (r == 0) set_status(&g_status, kStBadBlock);
+      continue;
+    }
+    if (r < 32) {
+      const bool is_v = r >= 16;
+      const int cc = r & 15;
+      const __nv_bfloat16* src = (is_v ? p.v : p.k) + ((size_t)j * p.hkv + h) * kHeadDim + cc * 8;
+      __nv_bfloat16* dst = (is_v ? p.vc : p.kc) + (size_t)slot * p.row_stride + h * kHeadDim + cc * 8;
+      *reinterpret_cast<int4*>(dst) = __ldg(reinterpret_cast<const int4*>(src));
+    } else {
+      const int ch = r - 32;
+      *reinterpret_cast<int4*>(p.ic + (((size_t)blk * p.hkv + h) * kBlock + row) * kIdxDim + ch * 16) =
+          __ldg(reinterpret_cast<const int4*>(p.ik + ((size_t)j * p.hkv + h) * kIdxDim + ch * 16));
+    }
+  }
+}
+
 struct GatherParams {
   const __nv_bfloat16* kc;
   const __nv_bfloat16* vc;
@@ -138,6 +166,24 @@ cudaError_t launch_head_table(const KV& kv, const int32_t* bt_heads, int32_t* bt
 cudaError_t launch_window_idx(const KV& kv, int window, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
   const int bx = min((window + 255) / 256, 64);
   return launch_pdl(window_idx_kernel, dim3(bx, kv.batch), dim3(256), 0, st, 1, kv.context_lens, window, idx, n_sel);
+}
+
+cudaError_t launch_kv_write_heads(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
+                                  const int8_t* idx_k, cudaStream_t st) {
+  WriteParams p;
+  p.kc = static_cast<__nv_bfloat16*>(const_cast<void*>(kv.k_cache));
+  p.vc = static_cast<__nv_bfloat16*>(const_cast<void*>(kv.v_cache));
+  p.ic = const_cast<int8_t*>(kv.idx_cache);
+  p.slots = slots;
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.ik = idx_k;
+  p.ntok = ntok;
+  p.hkv = kv.hkv;
+  p.num_blocks = kv.num_blocks;
+  p.row_stride = kv.row_stride;
+  kv_write_heads_kernel<<<ntok, 128, 0, st>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,

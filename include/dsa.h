@@ -173,6 +173,18 @@ void dsa_kv_bitmap_destroy(dsa_kv_bitmap* a);
  * and are skipped. */
 dsa_status dsa_kv_write(const dsa_paged_kv* kv, const int32_t* slot_mapping, int32_t ntok,
                         const void* k, const void* v, const int8_t* idx_k, cudaStream_t stream);
+/* Per-head write, for caches whose heads keep their own block tables (the
+ * per-(layer, head) block bitmaps, dsa_kv_bitmap_*): token j's head-h K, V and
+ * indexer key go to the head-h slice of slot slot_mapping_heads[j][h] only, so
+ * heads given the same block never overwrite one another.  slot_mapping_heads:
+ * int32 [ntok][num_kv_heads] (device); k, v: bf16 [ntok][num_kv_heads][128];
+ * idx_k: int8 [ntok][num_kv_heads][64]; kv->idx_cache: int8
+ * [num_blocks][num_kv_heads][64][64] (the per-KV-head indexer's layout).
+ * Slots outside the pool set DSA_ERR_BAD_BLOCK_TABLE on the device and are
+ * skipped; two (token, head) pairs naming the same slot and head write in no
+ * set order. */
+dsa_status dsa_kv_write_heads(const dsa_paged_kv* kv, const int32_t* slot_mapping_heads, int32_t ntok,
+                              const void* k, const void* v, const int8_t* idx_k, cudaStream_t stream);
 
 /* -------------------------------------------------------------- workspace --- */
 /* Bytes of workspace an op needs for these sizes (0 when it needs none, or on

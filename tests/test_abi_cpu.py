@@ -189,6 +189,12 @@ def test_argument_checks(lib):
     assert lib.dsa_kv_write(C.byref(kv), 0x1000, -1, 0x2000, 0x3000, 0x4000, None) == INVALID
     assert lib.dsa_kv_write(C.byref(kv), 0x1000, 4, 0x2008, 0x3000, 0x4000, None) == INVALID
     assert lib.dsa_kv_write(C.byref(kv), 0x1000, 0, 0x2008, 0x3000, 0x4000, None) == DSA_OK  # nothing to do
+    # per-head write: negative count, misaligned slots or sources, missing pointers
+    assert lib.dsa_kv_write_heads(C.byref(kv), 0x1000, -1, 0x2000, 0x3000, 0x4000, None) == INVALID
+    assert lib.dsa_kv_write_heads(C.byref(kv), 0x1002, 4, 0x2000, 0x3000, 0x4000, None) == INVALID
+    assert lib.dsa_kv_write_heads(C.byref(kv), 0x1000, 4, 0x2000, 0x3008, 0x4000, None) == INVALID
+    assert lib.dsa_kv_write_heads(C.byref(kv), 0x1000, 4, 0x2000, 0x3000, None, None) == INVALID
+    assert lib.dsa_kv_write_heads(C.byref(kv), 0x1000, 0, 0x2008, 0x3000, 0x4000, None) == DSA_OK
 
 
 def test_valid_call_without_gpu_reports_cuda_error(lib):

@@ -75,3 +75,31 @@ def test_heads_per_head_block_tables(lib, hq, hkv, layout):
     spec = synth.small_spec(lens=(40, 64, 65, 777, 20000), batch=5, prefix_len=64, hq=hq, hkv=hkv, k=100,
                             idx_heads=hkv, head_tables=True, kv_layout=layout)
     _run(spec)
+
+
+def test_kv_write_heads_bitwise(lib):
+    """Per-head cache write against the oracle, bitwise: each head's K, V and
+    indexer key in its own slot's head slice, with two heads of one token sent
+    to the same slot and heads of different tokens sharing blocks."""
+    spec = synth.small_spec(lens=(500,), batch=1, hkv=4, hq=16, idx_heads=4, spare_blocks=4)
+    w_cpu = synth.make_workload(spec, 4, "cpu")
+    w = H.on(w_cpu, DEV)
+    kv = H.paged_kv(w)
+    g = torch.Generator().manual_seed(1)
+    n, hkv = 9, 4
+    nb = w_cpu["k_cache"].shape[0]
+    slots = torch.stack([torch.randperm(nb * 64, generator=g)[:n] for _ in range(hkv)], dim=1).to(torch.int32)
+    slots[0, 1] = slots[0, 0]  # two heads of one token, one slot
+    # within a head no slot repeats, so the order of the writes does not matter
+    assert all(len(set(slots[:, h].tolist())) == n for h in range(hkv))
+    kn = torch.randn((n, hkv, 128), generator=g).to(torch.bfloat16)
+    vn = torch.randn((n, hkv, 128), generator=g).to(torch.bfloat16)
+    inn = torch.randint(-8, 9, (n, hkv, 64), generator=g, dtype=torch.int8)
+    dsa.kv_write_heads(kv, slots.to(DEV), kn.to(DEV), vn.to(DEV), inn.to(DEV))
+    assert dsa.check_device_status() == 0
+    wn = synth.to_numpy(w_cpu)
+    kc, vc, ic = O.kv_write_heads(wn["k_cache"], wn["v_cache"], wn["idx_cache"], slots.numpy(),
+                                  kn.double().numpy(), vn.double().numpy(), inn.numpy().astype(np.int64))
+    assert np.array_equal(w["k_cache"].double().cpu().numpy(), kc)
+    assert np.array_equal(w["v_cache"].double().cpu().numpy(), vc)
+    assert np.array_equal(w["idx_cache"].cpu().numpy().astype(np.int64), ic)
