@@ -103,3 +103,31 @@ def test_kv_write_heads_bitwise(lib):
     assert np.array_equal(w["k_cache"].double().cpu().numpy(), kc)
     assert np.array_equal(w["v_cache"].double().cpu().numpy(), vc)
     assert np.array_equal(w["idx_cache"].cpu().numpy().astype(np.int64), ic)
+
+
+def test_heads_bad_block_ids_set_status_not_fault(lib):
+    """A block id outside the pool in a head's own block table, and a per-head
+    write slot outside it, are reported through the status word: the kernels
+    read block 0 in its place (or skip the write) and the context stays usable
+    (a valid call right after gives results equal to the oracle's)."""
+    spec = synth.small_spec(lens=(300, 900), batch=2, prefix_len=64, hq=8, hkv=2, k=40, idx_heads=2,
+                            head_tables=True)
+    w = H.on(synth.make_workload(spec, 3, "cpu"), DEV)
+    kv = H.paged_kv(w)
+    nb = w["k_cache"].shape[0]
+    bad = w["block_table_heads"].clone()
+    bad[1, 1, 5] = nb + 5  # head 1, sequence 1, block-table entry 5 (positions 320-383)
+    ld = H.round4(int(w["max_context_len"]))
+    scores = torch.zeros((2 * 2, ld), dtype=torch.int32, device=DEV)
+    idx = torch.empty((2, 2, 40), dtype=torch.int32, device=DEV)
+    n_sel = torch.empty((2, 2), dtype=torch.int32, device=DEV)
+    out = torch.empty((2, 8, 128), dtype=torch.bfloat16, device=DEV)
+    ws = dsa.make_workspace(dsa.heads_workspace_size(kv, 8, 40, 64), DEV)
+    dsa.decode_step_heads(kv, w["q"], w["q_idx"], 64, 40, scores, idx, n_sel, out, None, ws, block_table_heads=bad)
+    assert dsa.check_device_status() == 4  # DSA_ERR_BAD_BLOCK_TABLE
+    slots = torch.tensor([[nb * 64 + 3, 5]], dtype=torch.int32, device=DEV)  # head 0's slot outside the pool
+    kn = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device=DEV)
+    dsa.kv_write_heads(kv, slots, kn, kn, torch.zeros((1, 2, 64), dtype=torch.int8, device=DEV))
+    assert dsa.check_device_status() == 4  # DSA_ERR_BAD_BLOCK_TABLE
+    assert dsa.check_device_status() == 0  # read and cleared
+    _run(spec, seed=3)  # the context is usable: a valid call matches the oracle
