@@ -388,13 +388,17 @@ __global__ void __launch_bounds__(NTH) decode_select_kernel(const SelectParams p
 }
 
 // ---------------------------------------------------------------- prefill ---
-// One warp per query row (many rows of at most a few ten thousand candidates),
-// no CTA-wide barrier: three passes over the row's scores (the row stays in L2
-// after the first): a 1024-bin coarse histogram in the warp's shared memory and
-// the threshold window from it; the counts per one-score bin of the window and
-// above it, which give the exact threshold tau and the tie quota; then an ordered
-// compaction by warp scans.  An edge bin falls back to a warp radix select.
-constexpr int kRowWarps = 8;
+// One CTA of 256 threads per query row, heaviest rows first: a 1024-bin coarse
+// histogram of the row's scores in shared memory and the threshold window from
+// it; the counts per one-score bin of the window and above it, which give the
+// exact threshold tau and the tie quota; then an ordered compaction, each thread
+// over its own contiguous run of the row after scans of its counts above and at
+// tau.  The first pass reads the row from HBM with the whole CTA, and the later
+// passes follow at once, while the row is still in L2: with one warp per row
+// (about 7,300 rows in flight) the rows of a 16K chunk fell out of L2 between
+// passes (16K chunk: 0.454 -> 0.383 ms).  An edge bin falls back to an exact
+// block radix select.
+constexpr int kRowThreads = 256;
 
 struct RowTopkParams {
   const int32_t* scores;
@@ -415,150 +419,122 @@ __device__ __forceinline__ int4 row_chunk(const int32_t* row, int c, int t_lo, i
   return x;
 }
 
-__global__ void __launch_bounds__(32 * kRowWarps) prefill_topk_kernel(const RowTopkParams p) {
-  __shared__ int s_hist[kRowWarps][kCoarseBins];
-  __shared__ int s_fine[kRowWarps][kFineBins];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int i = blockIdx.x * kRowWarps + w;
-  if (i >= p.n_q) return;
-  int* hist = s_hist[w];
-  int* fine = s_fine[w];
+__global__ void __launch_bounds__(kRowThreads) prefill_topk_kernel(const RowTopkParams p) {
+  __shared__ int s_hist[kCoarseBins];
+  __shared__ int s_cnt[1 + kFineBins];  // above the window, fine bins
+  __shared__ int s_misc[4];
+  __shared__ int s_scratch[272];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = p.n_q - 1 - (int)blockIdx.x;  // the longest rows first
   const int pos = p.pos0 + i;
   const int n_cand = max(0, pos - p.prefix + 1);
   int32_t* out = p.idx + (size_t)i * p.k;
   if (n_cand <= p.k) {  // every candidate is selected
-    for (int j = lane; j < p.k; j += 32) out[j] = j < n_cand ? p.prefix + j : -1;
-    if (lane == 0) p.n_sel[i] = n_cand;
+    for (int j = tid; j < p.k; j += kRowThreads) out[j] = j < n_cand ? p.prefix + j : -1;
+    if (tid == 0) p.n_sel[i] = n_cand;
     return;
   }
   const int32_t* row = p.scores + (size_t)i * p.ld;
   const int t_lo = p.prefix, t_hi = pos + 1;
   const int c0 = t_lo >> 2, c1 = (t_hi + 3) >> 2;  // chunks covering [t_lo, t_hi), all inside the row's ld entries
   // Pass 1: coarse histogram.
-  for (int b = lane; b < kCoarseBins; b += 32) hist[b] = 0;
-  __syncwarp();
+  for (int b = tid; b < kCoarseBins; b += kRowThreads) s_hist[b] = 0;
+  if (tid <= kFineBins) s_cnt[tid] = 0;
+  __syncthreads();
 #pragma unroll 4
-  for (int c = c0 + lane; c < c1; c += 32) {
+  for (int c = c0 + tid; c < c1; c += kRowThreads) {
     const int4 x = row_chunk(row, c, t_lo, t_hi);
-    if (x.x != INT_MIN) atomicAdd(&hist[coarse_bin(x.x)], 1);
-    if (x.y != INT_MIN) atomicAdd(&hist[coarse_bin(x.y)], 1);
-    if (x.z != INT_MIN) atomicAdd(&hist[coarse_bin(x.z)], 1);
-    if (x.w != INT_MIN) atomicAdd(&hist[coarse_bin(x.w)], 1);
+    if (x.x != INT_MIN) atomicAdd(&s_hist[coarse_bin(x.x)], 1);
+    if (x.y != INT_MIN) atomicAdd(&s_hist[coarse_bin(x.y)], 1);
+    if (x.z != INT_MIN) atomicAdd(&s_hist[coarse_bin(x.z)], 1);
+    if (x.w != INT_MIN) atomicAdd(&s_hist[coarse_bin(x.w)], 1);
   }
-  __syncwarp();
-  int beta, above_win;
-  warp_hist_threshold(hist, kCoarseBins, p.k, lane, &beta, &above_win);
+  __syncthreads();
+  if (warp == 0) {
+    int beta, above_win;
+    warp_hist_threshold(s_hist, kCoarseBins, p.k, lane, &beta, &above_win);
+    if (lane == 0) s_misc[0] = beta;
+  }
+  __syncthreads();
+  const int beta = s_misc[0];
   int lo, width;
   if (beta > 0 && beta < kCoarseBins - 1) {
     lo = (beta - kCoarseOff) << kCoarseShift;
     width = kFineBins;
-  } else {
-    // The k-th largest lies outside the histogram's range: exact radix select,
-    // four passes of 8-bit digits of u = s ^ 0x80000000 (256 bins in `hist`).
-    uint32_t prefix = 0, mask = 0;
-    int kk = p.k;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      __syncwarp();
-      for (int b = lane; b < 256; b += 32) hist[b] = 0;
-      __syncwarp();
-      for (int c = c0 + lane; c < c1; c += 32) {
-        const int4 x = row_chunk(row, c, t_lo, t_hi);
-        const int v4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t uu = (uint32_t)v4[u] ^ 0x80000000u;
-          if (v4[u] != INT_MIN && (uu & mask) == prefix) atomicAdd(&hist[(uu >> shift) & 255], 1);
-        }
-      }
-      __syncwarp();
-      int dsel, acc;
-      warp_hist_threshold(hist, 256, kk, lane, &dsel, &acc);
-      kk -= acc;
-      prefix |= (uint32_t)dsel << shift;
-      mask |= 0xFFu << shift;
-    }
-    lo = (int)(prefix ^ 0x80000000u);
+  } else {  // the k-th largest lies outside the histogram's range: exact radix select
+    int tau_r, n_gt_r;
+    block_radix_select(row + t_lo, n_cand, p.k, s_scratch, &tau_r, &n_gt_r);
+    lo = tau_r;
     width = 1;
   }
   // Pass 2: counts per one-score bin of the window and above it.
-  if (lane < kFineBins) fine[lane] = 0;
-  __syncwarp();
   int my_above = 0;
 #pragma unroll 4
-  for (int c = c0 + lane; c < c1; c += 32) {
+  for (int c = c0 + tid; c < c1; c += kRowThreads) {
     const int4 x = row_chunk(row, c, t_lo, t_hi);
     const int v4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int v = v4[u];
       if (v >= lo + width) ++my_above;
-      else if (v >= lo) atomicAdd(&fine[v - lo], 1);
+      else if (v >= lo) atomicAdd(&s_cnt[1 + v - lo], 1);
     }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
-  __syncwarp();
-  // Lanes as fine bins: the k-th largest lies in bin f*, the highest whose
-  // suffix reaches k - above; cum = candidates above it inside the window.
-  const int kk = p.k - my_above;
-  int suf = lane < width ? fine[lane] : 0;
+  if (lane == 0 && my_above) atomicAdd(&s_cnt[0], my_above);
+  __syncthreads();
+  // Lanes of warp 0 as fine bins: the k-th largest lies in bin f*, the highest
+  // whose suffix reaches k - above; cum = candidates above it inside the window.
+  if (warp == 0) {
+    const int kk = p.k - s_cnt[0];
+    int suf = lane < width ? s_cnt[1 + (lane & 15)] : 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_down_sync(0xffffffffu, suf, o);
-    if (lane + o < 32) suf += y;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += y;
+    }
+    const uint32_t reach = __ballot_sync(0xffffffffu, lane < width && suf >= kk);
+    const int fstar = reach ? 31 - __clz(reach) : 0;
+    const int cum = __shfl_sync(0xffffffffu, suf, fstar + 1);  // fstar + 1 <= 16: the suffix past the window is 0
+    if (lane == 0) {
+      s_misc[1] = lo + fstar;
+      s_misc[2] = kk - cum;
+    }
   }
-  const uint32_t reach = __ballot_sync(0xffffffffu, lane < width && suf >= kk);
-  const int fstar = reach ? 31 - __clz(reach) : 0;
-  const int cum = __shfl_sync(0xffffffffu, suf, fstar + 1);  // fstar + 1 <= 16: the suffix past the window is 0
-  const int tau = lo + fstar, quota = kk - cum;
-  // Pass 3: ordered compaction, 128 positions (32 chunks) per step.
-  int carry_ties = 0, carry_out = 0;
-  for (int cb = c0; cb < c1; cb += 32) {
-    const int c = cb + lane;
-    int4 x = make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
-    if (c < c1) x = row_chunk(row, c, t_lo, t_hi);
+  __syncthreads();
+  const int tau = s_misc[1], quota = s_misc[2];
+  // Pass 3: ordered compaction.  Thread t takes the chunks [a, e) of the row;
+  // scans of its counts at and above tau give the ties and the selected
+  // positions before it.
+  const int per = (c1 - c0 + kRowThreads - 1) / kRowThreads;
+  const int a = min(c1, c0 + tid * per), e = min(c1, a + per);
+  int n_gt = 0, n_eq = 0;
+  for (int c = a; c < e; ++c) {
+    const int4 x = row_chunk(row, c, t_lo, t_hi);
+    n_gt += (x.x > tau) + (x.y > tau) + (x.z > tau) + (x.w > tau);
+    n_eq += (x.x == tau) + (x.y == tau) + (x.z == tau) + (x.w == tau);
+  }
+  int tot_eq, tot_gt;
+  const int eq_before = block_exclusive_scan(n_eq, s_scratch, &tot_eq);
+  const int gt_before = block_exclusive_scan(n_gt, s_scratch, &tot_gt);
+  int tr = eq_before;
+  int o = gt_before + min(eq_before, quota);
+  for (int c = a; c < e; ++c) {
+    const int4 x = row_chunk(row, c, t_lo, t_hi);
     const int v4[4] = {x.x, x.y, x.z, x.w};
-    uint32_t gt_m = 0, eq_m = 0;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      gt_m |= (uint32_t)(v4[u] > tau) << u;
-      eq_m |= (uint32_t)(v4[u] == tau) << u;
-    }
-    int n_eq = __popc(eq_m), x_eq = n_eq;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x_eq, o);
-      if (lane >= o) x_eq += y;
-    }
-    int tr = carry_ties + x_eq - n_eq;
-    carry_ties += __shfl_sync(0xffffffffu, x_eq, 31);
-    uint32_t keep = gt_m;
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if ((eq_m >> u) & 1) {
-        if (tr < quota) keep |= 1u << u;
-        ++tr;
-      }
-    const int n_keep = __popc(keep);
-    int x_k = n_keep;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x_k, o);
-      if (lane >= o) x_k += y;
-    }
-    int o = carry_out + x_k - n_keep;
-    carry_out += __shfl_sync(0xffffffffu, x_k, 31);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if ((keep >> u) & 1) {
+      const int v = v4[u];
+      if (v > tau || (v == tau && tr++ < quota)) {
         if (o < p.k) out[o] = 4 * c + u;
         ++o;
       }
+    }
   }
-  const int n_out = min(carry_out, p.k);
-  for (int j = n_out + lane; j < p.k; j += 32) out[j] = -1;
-  if (lane == 0) p.n_sel[i] = n_out;
+  const int n_out = min(tot_gt + min(tot_eq, quota), p.k);
+  for (int j = n_out + tid; j < p.k; j += kRowThreads) out[j] = -1;
+  if (tid == 0) p.n_sel[i] = n_out;
 }
 
 }  // namespace
@@ -724,7 +700,7 @@ cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int
   p.n_q = qs.n_q;
   p.idx = idx;
   p.n_sel = n_sel;
-  prefill_topk_kernel<<<(qs.n_q + kRowWarps - 1) / kRowWarps, 32 * kRowWarps, 0, st>>>(p);
+  prefill_topk_kernel<<<qs.n_q, kRowThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 
