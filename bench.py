@@ -390,7 +390,12 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
              "window": lambda: dsa.window_attn_prefill(kv, qs, w["q"], WINDOW, out_g),
              # scores + top-k in one kernel, the scores never written (same indices;
              # not part of the chunk, which takes the faster separate calls)
-             "select_fused": lambda: dsa.prefill_select(kv, qs, w["q_idx"], P, k, idx_f, n_sel_f)}
+             "select_fused": lambda: dsa.prefill_select(kv, qs, w["q_idx"], P, k, idx_f, n_sel_f),
+             # the whole chunk in one call: scores, top-k writing the dense pass's
+             # bitmap, attention (the chunk's time)
+             "step": lambda: dsa.prefill_step(kv, qs, w["q"], w["q_idx"], P, k, scores, idx, n_sel, out, lse,
+                                              ws_step)}
+    ws_step = dsa.make_workspace(dsa.prefill_attn_workspace_size(kv, qs, k, hq, P, -1), dev)
     idx_f = torch.empty_like(idx)
     n_sel_f = torch.empty_like(n_sel)
     st = torch.cuda.current_stream(dev)
@@ -412,7 +417,7 @@ def measure_prefill(dev, steps, warmup, probes, cpu_seconds):
         ms[name] = a.elapsed_time(b) / steps
     clock_info = clocks.stop()
     assert dsa.check_device_status(dev) == 0
-    total = ms["index"] + ms["topk"] + ms["attention"]
+    total = ms["step"]  # the chunk: one prefill_step call (the separate calls sum to index + topk + attention)
     pos = np.arange(T)
     causal_pairs = int(np.maximum(0, pos + 1 - P).sum())          # scored (query, key) pairs
     n_sel_h = n_sel.cpu().numpy().astype(np.int64)

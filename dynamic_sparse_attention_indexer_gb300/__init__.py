@@ -187,6 +187,18 @@ def heads_workspace_size(kv: PagedKV, num_q_heads: int, k: int, prefix_len: int)
     return int(lib().dsa_heads_workspace_size(kv.ref, num_q_heads, k, prefix_len))
 
 
+def prefill_step(kv: PagedKV, qs, q, q_idx, prefix_len: int, k: int, scores, idx, n_sel, out, lse=None, ws=None,
+                 softmax_scale: float | None = None):
+    """Scores, top-k and attention of one prefill chunk in one call (the
+    automatic dense / gathered split); ws: prefill_attn_workspace_size(kv, qs,
+    k, num_q_heads, prefix_len) bytes."""
+    scale = 1.0 / math.sqrt(HEAD_DIM) if softmax_scale is None else softmax_scale
+    p, n = _ws(ws)
+    _check(lib().dsa_prefill_step(kv.ref, C.byref(qs), _ptr(q), _ptr(q_idx), int(q.shape[1]), prefix_len, k, scale,
+                                  _ptr(scores), int(scores.stride(0)), _ptr(idx), _ptr(n_sel), _ptr(out),
+                                  _out_dtype(out), _ptr(lse), p, n, _stream(q.device)))
+
+
 def decode_step_heads(kv: PagedKV, q, q_idx, prefix_len: int, k: int, scores, idx, n_sel, out, lse=None, ws=None,
                       softmax_scale: float | None = None, block_table_heads=None):
     """The decode step with one indexer head per KV head: q_idx [B][Hkv][64],

@@ -64,6 +64,8 @@ SIGNATURES = {
     "dsa_window_workspace_size": (C.c_size_t, [PKV, c_i32, c_i32]),
     "dsa_window_attn_decode": (c_i32, [PKV, c_p, c_i32, c_i32, C.c_float, c_p, c_i32, c_p, c_p, C.c_size_t, c_p]),
     "dsa_window_attn_prefill": (c_i32, [PKV, PQS, c_p, c_i32, c_i32, C.c_float, c_p, c_i32, c_p, c_p]),
+    "dsa_prefill_step": (c_i32, [PKV, c_p, c_p, c_p, c_i32, c_i32, c_i32, C.c_float, c_p, c_i32, c_p, c_p, c_p,
+                                 c_i32, c_p, c_p, C.c_size_t, c_p]),
     "dsa_decode_step": (c_i32, [PKV, c_p, c_p, c_i32, c_i32, c_i32, C.c_float, c_p, c_i32, c_p, c_p,
                                 c_p, c_i32, c_p, c_p, C.c_size_t, c_p]),
     "dsa_topk_select_decode_noalloc": (c_i32, [PKV, c_p, c_i32, c_i32, c_i32, c_p, c_p, c_p]),

@@ -305,7 +305,7 @@ PrefillPlan prefill_plan(const dsa::KV& kv, const dsa::QS& qs, int32_t k, int32_
 dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const void* q, int32_t hq,
                      const int32_t* idx, const int32_t* n_sel, int32_t k, int32_t prefix, float scale, void* out,
                      int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream,
-                     int32_t n_dense = -1) {
+                     int32_t n_dense = -1, bool mask_ready = false) {
   dsa::KV kv{};
   dsa::QS qs{};
   DSA_TRY(check_kv(kv_, &kv));
@@ -342,7 +342,8 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
     a.out = out;
     a.out_dtype = out_dtype;
     a.lse = lse;
-    if (pl.n_dense > 0) DSA_CUDA("dense prefill attention launch", dsa::launch_dense_attn(a, pl.n_dense, ws, stream));
+    if (pl.n_dense > 0)
+      DSA_CUDA("dense prefill attention launch", dsa::launch_dense_attn(a, pl.n_dense, ws, stream, 0, mask_ready));
     if (pl.rest.n_q == 0) return DSA_OK;
     const size_t nd = (size_t)pl.n_dense, row = (size_t)hq * 128;
     a.qs = pl.rest;
@@ -608,6 +609,42 @@ dsa_status dsa_topk_select(const dsa_paged_kv* kv_, const dsa_query_set* qs_, co
     DSA_CUDA("top-k launch", dsa::launch_prefill_topk(qs, scores, ld, prefix, k, idx, n_sel, stream));
   }
   return DSA_OK;
+}
+
+dsa_status dsa_prefill_step(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const void* q, const int8_t* q_idx,
+                            int32_t hq, int32_t prefix, int32_t k, float scale, int32_t* scores, int32_t ld,
+                            int32_t* idx, int32_t* n_sel, void* out, int32_t out_dtype, float* lse, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  dsa::KV kv{};
+  dsa::QS qs{};
+  DSA_TRY(check_kv(kv_, &kv));
+  if (qs_ && qs_->mode != DSA_MODE_PREFILL)
+    return fail(DSA_ERR_INVALID_ARG, "dsa_prefill_step needs a DSA_MODE_PREFILL query set");
+  DSA_TRY(check_qs(qs_, kv, &qs));
+  DSA_TRY(check_k_prefix(k, prefix));
+  DSA_TRY(check_heads(hq, kv));
+  DSA_TRY(check_tiles(kv, qs, k, prefix));
+  if (!q_idx || !aligned16(q_idx)) return fail(DSA_ERR_INVALID_ARG, "q_idx must be non-NULL and 16-byte aligned");
+  DSA_TRY(check_scores(scores, ld, kv, qs));
+  if (!idx || !n_sel) return fail(DSA_ERR_INVALID_ARG, "idx and n_sel must be non-NULL");
+  if (!q || !aligned16(q) || !out || !aligned16(out))
+    return fail(DSA_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+  if (out_dtype != DSA_OUT_BF16 && out_dtype != DSA_OUT_F32)
+    return fail(DSA_ERR_INVALID_ARG, "out_dtype %d is neither DSA_OUT_BF16 nor DSA_OUT_F32", out_dtype);
+  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  const int n_dense = auto_dense_queries(kv, qs, k, hq, prefix);
+  const PrefillPlan pl = prefill_plan(kv, qs, k, hq, prefix, n_dense);
+  DSA_TRY(check_ws(ws, ws_bytes, pl.total));
+  DSA_TRY(ensure_setup());
+  // The top-k writes the dense queries' attended-position bitmap as it writes
+  // their index lists (the attention then needs no pass over the lists).
+  uint64_t* mask = n_dense > 0 ? static_cast<uint64_t*>(ws) : nullptr;
+  if (mask) DSA_CUDA("bitmap clear", cudaMemsetAsync(mask, 0, dsa::dense_mask_bytes(qs, n_dense), stream));
+  DSA_CUDA("index_scores launch", dsa::launch_prefill_index(kv, qs, q_idx, prefix, scores, ld, stream));
+  DSA_CUDA("top-k launch", dsa::launch_prefill_topk(qs, scores, ld, prefix, k, idx, n_sel, stream, mask, n_dense,
+                                                   (n_dense + 1) & ~1));
+  return attn_impl(kv_, qs_, q, hq, idx, n_sel, k, prefix, scale, out, out_dtype, lse, ws, ws_bytes, stream, n_dense,
+                   true);
 }
 
 dsa_status dsa_kv_gather(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const int32_t* idx, const int32_t* n_sel,

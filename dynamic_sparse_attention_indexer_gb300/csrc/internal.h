@@ -92,8 +92,11 @@ int decode_select_ctas(const KV& kv, int prefix, int c_cap);
 int attn_grid_ctas();
 cudaError_t launch_prefill_index(const KV& kv, const QS& qs, const int8_t* q_idx, int prefix,
                                  int* scores, int ld, cudaStream_t st);
+// mask: the dense pass's attended-position bitmap (dense_mask_bytes, zeroed), set
+// here for the first n_dense queries (nq_pad as in the dense pass), or null.
 cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k,
-                                int32_t* idx, int32_t* n_sel, cudaStream_t st);
+                                int32_t* idx, int32_t* n_sel, cudaStream_t st, uint64_t* mask = nullptr,
+                                int n_dense = 0, int nq_pad = 0);
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_prefix_attn(const KV& kv, const QS& qs, const void* q, int hq, int prefix, float scale,
                                float2* pre_ml, float* pre_o, cudaStream_t st);
@@ -102,7 +105,8 @@ cudaError_t launch_prefix_attn(const KV& kv, const QS& qs, const void* q, int hq
 // selections (a.idx, a.n_sel, a.prefix), with mask_ws holding
 // dense_mask_bytes(qs, n_dense); window > 0: the causal window of that many
 // positions ending at each query (no workspace).
-cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st, int window = 0);
+cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st, int window = 0,
+                              bool mask_ready = false);  // mask_ready: the bitmap is already in mask_ws
 // Decode window attention's index lists: idx[b][j] = L_b - min(window, L_b) + j,
 // n_sel[b] = min(window, L_b), -1 past it (k_misc.cu).
 cudaError_t launch_window_idx(const KV& kv, int window, int32_t* idx, int32_t* n_sel, cudaStream_t st);

@@ -623,7 +623,8 @@ cudaError_t setup_dense_kernels() {
   return e;
 }
 
-cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st, int window) {
+cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cudaStream_t st, int window,
+                              bool mask_ready) {
   if (n_dense <= 0) return cudaSuccess;
   const int group = a.hq / a.kv.hkv;
   const int qt = dense_tile_queries(group);
@@ -636,7 +637,7 @@ cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cud
       !encode_rows(&kmap, a.kv.k_cache, a.kv.hkv, (uint64_t)a.kv.num_blocks * kBlock, slot_bytes, 1, kBlock) ||
       !encode_rows(&vmap, a.kv.v_cache, a.kv.hkv, (uint64_t)a.kv.num_blocks * kBlock, slot_bytes, 1, kBlock))
     return cudaErrorInvalidValue;
-  if (window <= 0) {  // the attended-position bitmap of the selections
+  if (window <= 0 && !mask_ready) {  // the attended-position bitmap of the selections
     cudaError_t e = cudaMemsetAsync(mask, 0, (size_t)nq_pad * chunks * 8, st);
     if (e != cudaSuccess) return e;
     e = launch_pdl(dense_mask_kernel, dim3((n_dense + 7) / 8), dim3(256), 0, st, 1, a.idx, a.n_sel, a.k, a.prefix,

@@ -403,6 +403,8 @@ constexpr int kRowThreads = 256;
 struct RowTopkParams {
   const int32_t* scores;
   int ld, prefix, k, pos0, n_q;
+  uint64_t* mask;  // or null: the dense pass's attended-position bitmap [block][nq_pad] (zeroed), rows < n_dense
+  int n_dense, nq_pad;
   int32_t* idx;
   int32_t* n_sel;
 };
@@ -429,10 +431,22 @@ __global__ void __launch_bounds__(kRowThreads) prefill_topk_kernel(const RowTopk
   const int pos = p.pos0 + i;
   const int n_cand = max(0, pos - p.prefix + 1);
   int32_t* out = p.idx + (size_t)i * p.k;
+  uint64_t* mrow = p.mask && i < p.n_dense ? p.mask + i : nullptr;  // word c of this row at mrow[c * nq_pad]
   if (n_cand <= p.k) {  // every candidate is selected
     for (int j = tid; j < p.k; j += kRowThreads) out[j] = j < n_cand ? p.prefix + j : -1;
     if (tid == 0) p.n_sel[i] = n_cand;
+    if (mrow) {  // the prefix and every candidate: the whole causal range [0, pos]
+      const int n = pos + 1;
+      for (int c = tid; c < ((n + 63) >> 6); c += kRowThreads)
+        mrow[(size_t)c * p.nq_pad] = (c + 1) * 64 <= n ? ~0ull : (1ull << (n & 63)) - 1ull;
+    }
     return;
+  }
+  if (mrow) {  // the prefix [0, min(P, pos + 1)): whole words stored, the partial one OR-ed
+    const int npre = min(p.prefix, pos + 1);
+    for (int c = tid; c < (npre >> 6); c += kRowThreads) mrow[(size_t)c * p.nq_pad] = ~0ull;
+    if (tid == 0 && (npre & 63))
+      atomicOr(reinterpret_cast<unsigned long long*>(&mrow[(size_t)(npre >> 6) * p.nq_pad]), (1ull << (npre & 63)) - 1ull);
   }
   const int32_t* row = p.scores + (size_t)i * p.ld;
   const int t_lo = p.prefix, t_hi = pos + 1;
@@ -520,6 +534,8 @@ __global__ void __launch_bounds__(kRowThreads) prefill_topk_kernel(const RowTopk
   const int gt_before = block_exclusive_scan(n_gt, s_scratch, &tot_gt);
   int tr = eq_before;
   int o = gt_before + min(eq_before, quota);
+  int mword = -1;            // bitmap word being gathered (this thread's run spans few words)
+  unsigned long long mbits = 0;
   for (int c = a; c < e; ++c) {
     const int4 x = row_chunk(row, c, t_lo, t_hi);
     const int v4[4] = {x.x, x.y, x.z, x.w};
@@ -527,11 +543,21 @@ __global__ void __launch_bounds__(kRowThreads) prefill_topk_kernel(const RowTopk
     for (int u = 0; u < 4; ++u) {
       const int v = v4[u];
       if (v > tau || (v == tau && tr++ < quota)) {
-        if (o < p.k) out[o] = 4 * c + u;
+        const int t = 4 * c + u;
+        if (o < p.k) out[o] = t;
         ++o;
+        if (mrow) {
+          if ((t >> 6) != mword) {
+            if (mbits) atomicOr(reinterpret_cast<unsigned long long*>(&mrow[(size_t)mword * p.nq_pad]), mbits);
+            mword = t >> 6;
+            mbits = 0;
+          }
+          mbits |= 1ull << (t & 63);
+        }
       }
     }
   }
+  if (mbits) atomicOr(reinterpret_cast<unsigned long long*>(&mrow[(size_t)mword * p.nq_pad]), mbits);
   const int n_out = min(tot_gt + min(tot_eq, quota), p.k);
   for (int j = n_out + tid; j < p.k; j += kRowThreads) out[j] = -1;
   if (tid == 0) p.n_sel[i] = n_out;
@@ -690,8 +716,11 @@ cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, in
 }
 
 cudaError_t launch_prefill_topk(const QS& qs, const int32_t* scores, int ld, int prefix, int k, int32_t* idx,
-                                int32_t* n_sel, cudaStream_t st) {
+                                int32_t* n_sel, cudaStream_t st, uint64_t* mask, int n_dense, int nq_pad) {
   RowTopkParams p;
+  p.mask = mask;
+  p.n_dense = mask ? n_dense : 0;
+  p.nq_pad = nq_pad;
   p.scores = scores;
   p.ld = ld;
   p.prefix = prefix;

@@ -328,6 +328,22 @@ dsa_status dsa_window_attn_prefill(const dsa_paged_kv* kv, const dsa_query_set* 
                                    int32_t num_q_heads, int32_t window, float softmax_scale, void* out,
                                    int32_t out_dtype, float* lse, cudaStream_t stream);
 
+/* ---------------------------------------------------- prefill step --- */
+/* Steps 1-4 for one prefill chunk (a DSA_MODE_PREFILL query set) in one call:
+ * scores (written to `scores`, [n_q][ld]), top-k (idx, n_sel) and attention
+ * (out, lse) with the automatic split of dsa_sparse_attn_prefill (the first
+ * dsa_prefill_dense_queries() queries through the masked dense pass, the rest
+ * gathered).  The top-k writes the dense pass's attended-position bitmap as it
+ * writes the index lists, so the attention needs no pass over them.  Same
+ * argument rules as the single calls; the workspace is
+ * dsa_prefill_attn_workspace_size(kv, qs, k, num_q_heads, prefix_len, -1)
+ * bytes.  Results equal those of the three calls in sequence (indices bit for
+ * bit; outputs within rounding). */
+dsa_status dsa_prefill_step(const dsa_paged_kv* kv, const dsa_query_set* qs, const void* q, const int8_t* q_idx,
+                            int32_t num_q_heads, int32_t prefix_len, int32_t k, float softmax_scale,
+                            int32_t* scores, int32_t ld, int32_t* idx, int32_t* n_sel, void* out,
+                            int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------- fused decode step --- */
 /* Steps 1-4 for one decode token per sequence, in one call: scores (written to
  * `scores`, [batch][ld]), top-k (idx, n_sel) and attention (out, lse), with the

@@ -180,6 +180,26 @@ def run_prefill(w: dict, out_dtype=torch.bfloat16, n_dense=None) -> dict:
     return {"scores": scores, "idx": idx, "n_sel": n_sel, "out": out, "lse": lse}
 
 
+def run_prefill_step(w: dict, out_dtype=torch.bfloat16) -> dict:
+    """The same chunk through the one-call prefill step (scores, top-k with
+    the dense pass's bitmap, attention with the automatic split)."""
+    dev = w["q"].device
+    kv = paged_kv(w)
+    T, k, P, hq = int(w["num_queries"]), int(w["k"]), int(w["prefix_len"]), int(w["num_q_heads"])
+    qs = dsa.query_set(dsa.MODE_PREFILL, T, int(w["seq"]), int(w["pos0"]))
+    ld = round4(int(w["pos0"]) + T)
+    scores = torch.zeros((T, ld), dtype=torch.int32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    n_sel = torch.empty(T, dtype=torch.int32, device=dev)
+    out = torch.empty((T, hq, 128), dtype=out_dtype, device=dev)
+    lse = torch.empty((T, hq), dtype=torch.float32, device=dev)
+    ws = dsa.make_workspace(dsa.prefill_attn_workspace_size(kv, qs, k, hq, P, -1), dev)
+    dsa.prefill_step(kv, qs, w["q"], w["q_idx"], P, k, scores, idx, n_sel, out, lse, ws)
+    status = dsa.check_device_status(dev)
+    assert status == 0, f"device status {status}"
+    return {"scores": scores, "idx": idx, "n_sel": n_sel, "out": out, "lse": lse}
+
+
 def check_prefill_against_oracle(wn: dict, res: dict, rows=None):
     P = int(wn["prefix_len"])
     pos0 = int(wn["pos0"])

@@ -182,6 +182,15 @@ def test_argument_checks(lib):
                                        None) == INVALID
     assert lib.dsa_window_attn_prefill(C.byref(kv), C.byref(qs10), 0x60000, 8, 16, float("nan"), 0xB0000, 0,
                                        None, None) == INVALID
+    # the prefill step: a prefill query set, aligned q_idx, outputs present
+    assert lib.dsa_prefill_step(C.byref(kv), C.byref(qs), 0x60000, 0x70000, 8, 0, 8, 0.1, 0x80000, 512, 0x90000,
+                                0xA0000, 0xB0000, 0, None, None, 0, None) == INVALID   # decode query set
+    assert lib.dsa_prefill_step(C.byref(kv), C.byref(qs10), 0x60000, 0x70004, 8, 0, 8, 0.1, 0x80000, 512,
+                                0x90000, 0xA0000, 0xB0000, 0, None, None, 0, None) == INVALID   # misaligned q_idx
+    assert lib.dsa_prefill_step(C.byref(kv), C.byref(qs10), 0x60000, 0x70000, 8, 0, 8, 0.1, 0x80000, 512,
+                                None, 0xA0000, 0xB0000, 0, None, None, 0, None) == INVALID      # no idx
+    assert lib.dsa_prefill_step(C.byref(kv), C.byref(qs10), 0x60000, 0x70000, 8, 0, 8, 0.1, 0x80000, 512,
+                                0x90000, 0xA0000, 0xB0000, 0, None, 0xC0000, 16, None) == WORKSPACE
     # prefill attention refuses a decode query set
     assert lib.dsa_sparse_attn_prefill(C.byref(kv), C.byref(qs), 0x60000, 8, 0x80000, 0x90000, 8, 0, 0.1,
                                        0xB0000, 0, None, None, 0, None) == INVALID

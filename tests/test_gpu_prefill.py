@@ -262,3 +262,24 @@ def test_fused_select_full_16k_equals_separate_steps(lib):
     idx_h, n_h = idx.cpu().numpy(), n_sel.cpu().numpy()
     for i in rows:
         assert int(n_h[i]) == ref[i]["n_sel"] and np.array_equal(idx_h[i], ref[i]["idx"]), f"query {i}"
+
+
+@pytest.mark.parametrize("T,pos0,P,k,hq,hkv,out_dtype", [
+    (400, 0, 64, 100, 8, 2, torch.bfloat16),     # from position 0: every query dense (automatic split)
+    (400, 300, 16, 24, 8, 2, torch.bfloat16),    # past the dense range: dense tile pairs, then gathered
+    (260, 90, 64, 100, 32, 2, torch.float32),    # group 16, fp32 out
+])
+def test_prefill_step_one_call(lib, T, pos0, P, k, hq, hkv, out_dtype):
+    """The one-call prefill step (its top-k writes the dense pass's bitmap)
+    against the oracle, and against the three calls in sequence: the same
+    scores and selections bit for bit, outputs within tolerance."""
+    spec = _prefill_spec(T=T, pos0=pos0, P=P, k=k, hq=hq, hkv=hkv)
+    w_cpu = synth.make_workload(spec, 5, "cpu")
+    w_cpu["seq"] = 0
+    w = H.on(w_cpu, DEV)
+    one = H.run_prefill_step(w, out_dtype=out_dtype)
+    H.check_prefill_against_oracle(synth.to_numpy(w_cpu), one)
+    three = H.run_prefill(w, out_dtype=out_dtype)
+    assert torch.equal(one["scores"], three["scores"])
+    assert torch.equal(one["idx"], three["idx"]) and torch.equal(one["n_sel"], three["n_sel"])
+    H.assert_close(one["out"].float().cpu().numpy(), three["out"].float().cpu().numpy(), "step vs three calls")
