@@ -643,8 +643,10 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const AttnPa
   // starts the CTA's range, else in slot 1.
   const int c_first = range_begin(T, grid_ctas, c_lo) >= first ? 0 : 1;  // slot of CTA c_lo
   const float4* part_o = reinterpret_cast<const float4*>(p.part_o);
-  pdl_wait();
+  // The next kernel may start its own set-up while the merge waits: whatever it
+  // reads before its wait on this kernel, no kernel here writes.
   pdl_trigger();
+  pdl_wait();
   // The trip count depends on hg only, so the four warps of a head meet at
   // the same named barriers.
   for (int h = j + hg * nb; h < p.hq; h += kCombHeads * nb) {
@@ -733,8 +735,8 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine2_kernel(const AttnP
   const int f1 = range_begin(p.units, grid_ctas, c1) >= first1 ? 0 : 1;
   const int n = n0 + n1;
   const float4* part_o = reinterpret_cast<const float4*>(p.part_o);
+  pdl_trigger();  // as in attn_combine_kernel
   pdl_wait();
-  pdl_trigger();
   if (h < p.hq) {
     float M = -INFINITY, Lsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);

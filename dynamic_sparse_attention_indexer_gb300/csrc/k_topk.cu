@@ -138,8 +138,6 @@ __global__ void __launch_bounds__(NTH) decode_select_kernel(const SelectParams p
   int* e_pos = s_ent;
   int* e_sc = s_ent + kSelCap;
   int* e_slot = s_ent + 2 * kSelCap;
-  pdl_wait();
-  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, b = blockIdx.y;
   const int r = C > 1 ? (int)cluster_rank() : 0;
   const int L = min(__ldg(p.ctx + b), p.max_ctx);
@@ -148,6 +146,15 @@ __global__ void __launch_bounds__(NTH) decode_select_kernel(const SelectParams p
   const int te = p.prefix + (int)((long long)n_cand * (r + 1) / C);
   int32_t* out = p.idx + (size_t)b * p.k;
   int32_t* out_slot = p.slot ? p.slot + (size_t)b * p.k : nullptr;
+  const int a0 = tb & ~(kSelPer - 1);
+  int t = a0 + tid * kSelPer;  // kSelPer positions inside one 64-position block
+  const int bt0 = (out_slot && t < te) ? __ldg(p.bt + (size_t)b * p.max_blocks + (t >> 6)) : 0;
+  // The context length and the block table are inputs no kernel of the step
+  // writes: they are read before the wait on the scoring kernel.  This kernel
+  // lets the next one start only after its own wait (the attention's first
+  // pass relies on that).
+  pdl_wait();
+  pdl_trigger();
 
   if (n_cand <= p.k) {  // every candidate is selected: position t goes to entry t - prefix
     for (int t = tb + tid; t < te; t += kSelThreads) {
@@ -163,17 +170,14 @@ __global__ void __launch_bounds__(NTH) decode_select_kernel(const SelectParams p
 
   const int32_t* row = p.scores + (size_t)b * p.ld;
   int* gh = p.coarse + (size_t)b * kCoarseBins;
-  const int a0 = tb & ~(kSelPer - 1);
   // First round of scores and slots, then the histogram: all in flight together.
   constexpr int kHB = kCoarseBins / kSelThreads;  // histogram bins per thread
   int hreg[kHB];
 #pragma unroll
   for (int i = 0; i < kHB; ++i) hreg[i] = __ldcg(gh + tid + i * kSelThreads);
   int v[kSelPer];
-  int t = a0 + tid * kSelPer;  // kSelPer positions inside one 64-position block
   int4 xr[kSelPer / 4];
   load_raw<kSelPer>(row, p.ld, t, tb, te, xr);
-  const int bt0 = (out_slot && t < te) ? __ldg(p.bt + (size_t)b * p.max_blocks + (t >> 6)) : 0;
 #pragma unroll
   for (int i = 0; i < kHB; ++i) s_hist[tid + i * kSelThreads] = hreg[i];
   if (tid < kCounts) s_counts[tid] = 0;

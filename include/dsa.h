@@ -362,7 +362,11 @@ dsa_status dsa_prefill_step(const dsa_paged_kv* kv, const dsa_query_set* qs, con
  * sequences whose context reaches past the prefix), while the selection still
  * runs on part of the SMs, and the selected rows after it; by then the scoring
  * kernel, and so every kernel before the step, has completed.  The selection's
- * clusters are kept to at most half of the SMs to leave room for that pass. */
+ * clusters are kept to at most half of the SMs to leave room for that pass.
+ * The step's last kernel (the merge) lets the next kernel of the stream launch
+ * before it finishes: a kernel launched after the step with programmatic
+ * dependent launch must wait for it (griddepcontrol.wait) before it reads out,
+ * lse or anything else the step writes. */
 dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* q_idx,
                            int32_t num_q_heads, int32_t prefix_len, int32_t k,
                            float softmax_scale, int32_t* scores, int32_t ld, int32_t* idx,
