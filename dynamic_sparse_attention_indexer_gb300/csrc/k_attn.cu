@@ -112,15 +112,19 @@ struct QueryInfo {
 // reaches past the prefix, else none; pass 1 then holds its selected rows, or
 // (context inside the prefix) its whole causal range.  The first pass reads
 // no selection output: it runs before the wait on the previous kernel.
+// PS: prefill (queries of one sequence, the prefix part possibly from pre_ml);
+// else decode (one query per sequence, or per (sequence, KV head) with hsplit).
+// TP: two-pass decode.
+template <bool PS, bool TP>
 __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi, int pass) {
   QueryInfo qf;
   qf.qi = qi;
-  const int hh = p.mode == 0 && p.hsplit > 1 ? qi % p.hsplit : 0;
-  qf.seq = p.mode == 0 ? (qi - hh) / p.hsplit : p.seq;
-  qf.bt_row = p.bt_per_query ? qi : qf.seq;
+  const int hh = !PS && p.hsplit > 1 ? qi % p.hsplit : 0;
+  qf.seq = PS ? p.seq : p.hsplit > 1 ? (qi - hh) / p.hsplit : qi;
+  qf.bt_row = !PS && p.bt_per_query ? qi : qf.seq;
   qf.hoff = hh * kHeadDim;
-  const int pos = p.mode == 0 ? min(__ldg(p.ctx + qf.seq), p.max_ctx) - 1 : p.pos0 + qi;
-  if (p.two_pass) {
+  const int pos = PS ? p.pos0 + qi : min(__ldg(p.ctx + qf.seq), p.max_ctx) - 1;
+  if constexpr (TP) {
     const bool past = pos + 1 > p.prefix;
     if (pass == 0) {
       qf.n_pre = past ? p.prefix : 0;
@@ -131,7 +135,7 @@ __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi, int
     }
     return qf;
   }
-  qf.n_pre = p.pre_ml ? 0 : max(0, min(p.prefix, pos + 1));  // with pre_ml every row is a selected one
+  qf.n_pre = PS && p.pre_ml ? 0 : max(0, min(p.prefix, pos + 1));  // with pre_ml every row is a selected one
   qf.rows = qf.n_pre + min(max(__ldg(p.nsel + qi), 0), p.k);
   return qf;
 }
@@ -177,15 +181,17 @@ __device__ __forceinline__ void cursor_pass(Cursor& c, const AttnParams& p, int 
   c.seg_start = c.x_begin;
   c.fresh = false;
 }
+template <bool TP>
 __device__ __forceinline__ void cursor_init(Cursor& c, const AttnParams& p) {
   c.hold = false;
-  cursor_pass(c, p, p.two_pass ? 0 : 1);
+  cursor_pass(c, p, TP ? 0 : 1);
 }
 
+template <bool PS, bool TP>
 __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* t) {
   for (;;) {
     if (c.x >= c.x_end) {
-      if (c.pass == 1 || c.hold) return false;
+      if (!TP || c.pass == 1 || c.hold) return false;
       // The selected rows come from the previous kernel of the stream.
       pdl_wait();
       cursor_pass(c, p, 1);
@@ -199,7 +205,7 @@ __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* 
     c.x = x + min(min(c.x_end, q_end) - x, p.rows);
     if (qi != c.qi) {
       c.qi = qi;
-      c.qf = query_info(p, qi, c.pass);
+      c.qf = query_info<PS, TP>(p, qi, c.pass);
       c.seg_start = x;
       c.fresh = true;
     }
@@ -210,9 +216,9 @@ __device__ __forceinline__ bool next_tile(Cursor& c, const AttnParams& p, Tile* 
     t->r0 = r;
     t->nvalid = nvalid;
     t->flags = (c.fresh ? kFirst : 0) | (last ? kLast : 0) |
-               (!p.two_pass && last && c.seg_start == qi * RPQ && c.x == q_end ? kWhole : 0) |
+               (!TP && last && c.seg_start == qi * RPQ && c.x == q_end ? kWhole : 0) |
                (c.fresh && c.seg_start == qi * RPQ ? kHead : 0);
-    t->slot = (p.two_pass ? 2 * c.pass : 0) + (c.seg_start == c.x_begin ? 0 : 1);
+    t->slot = (TP ? 2 * c.pass : 0) + (c.seg_start == c.x_begin ? 0 : 1);
     c.fresh = false;
     return true;
   }
@@ -271,8 +277,11 @@ __device__ __forceinline__ void write_out(const AttnParams& p, size_t head, int 
 // tile.  true (prefill, where L2-resident rows make the producer's per-tile
 // chain the limit): one producer warp per ring stage, each with kStages tile
 // times per tile, and Q copied by its own warp through a one-slot ring.
-template <int NT, bool PS>
+// TP (decode only): two passes, the prefix rows before the wait on the
+// previous kernel, then the selected rows.
+template <int NT, bool PS, bool TP>
 __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kernel(const AttnParams p) {
+  static_assert(!(PS && TP), "two passes are a decode form");
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* s_q = smem + kStages * kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(s_q + kQBytes);
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.group;
-  const bool none1 = !p.two_pass || (int)blockIdx.x >= p.grid1 ||
+  const bool none1 = !TP || (int)blockIdx.x >= p.grid1 ||
                      range_begin(p.units1, p.grid1, blockIdx.x) >= range_begin(p.units1, p.grid1, blockIdx.x + 1);
   if (none1 && range_begin(p.units, gridDim.x, blockIdx.x) >= range_begin(p.units, gridDim.x, blockIdx.x + 1)) return;
 
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
   // has passed its own wait, i.e. after the scoring kernel and everything
   // before it completed.  The first pass therefore runs before the wait; each
   // thread waits when its walk reaches the second pass.
-  if (!p.two_pass) pdl_wait();
+  if (!TP) pdl_wait();
   pdl_trigger();
 
   if (warp < kProducerWarps) {
@@ -336,19 +345,19 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
       // tiles back until the selection ended); the second phase then starts
       // its own look-ahead behind the wait.
       Cursor cur;
-      cursor_init(cur, p);
-      cur.hold = p.two_pass;
+      cursor_init<TP>(cur, p);
+      cur.hold = TP;
       const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
       int n = 0, seg = 0;
       for (int phase = 0; phase < 2 && !*s_abort; ++phase) {
       if (phase == 1) {
-        if (!p.two_pass) break;
+        if (!TP) break;
         cur.hold = false;  // the next tile switches to the second pass, after the wait
       }
       Tile t0, t1, t2;  // issued now, next, the one after
-      bool h0 = next_tile(cur, p, &t0);
-      bool h1 = h0 && next_tile(cur, p, &t1);
-      bool h2 = h1 && next_tile(cur, p, &t2);
+      bool h0 = next_tile<PS, TP>(cur, p, &t0);
+      bool h1 = h0 && next_tile<PS, TP>(cur, p, &t1);
+      bool h2 = h1 && next_tile<PS, TP>(cur, p, &t2);
       RowRef v0[2];  // rows of t0, both loads issued
       int f1[2];     // first loads of t1
 #pragma unroll
@@ -405,7 +414,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         h0 = h1;
         t1 = t2;
         h1 = h2;
-        h2 = more && next_tile(cur, p, &t2);
+        h2 = more && next_tile<PS, TP>(cur, p, &t2);
       }
       }
     } else {
@@ -430,11 +439,11 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
         auto active = [&](const Tile& tl, int i) { return i < R && lane + 32 * i < filled(tl); };
         auto row_of = [&](const Tile& tl, int i) { return tl.r0 + min(lane + 32 * i, tl.nvalid - 1); };
         Cursor cur;
-        cursor_init(cur, p);
+        cursor_init<TP>(cur, p);
         int n_walk = 0;
         auto next_own = [&](Tile* t) {
           Tile x;
-          while (next_tile(cur, p, &x))
+          while (next_tile<PS, TP>(cur, p, &x))
             if (n_walk++ % kStages == w) {
               *t = x;
               return true;
@@ -491,9 +500,9 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
       } else if (lane == 0) {
         const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
         Cursor cur;
-        cursor_init(cur, p);
+        cursor_init<TP>(cur, p);
         Tile t;
-        for (int seg = 0; next_tile(cur, p, &t);) {
+        for (int seg = 0; next_tile<PS, TP>(cur, p, &t);) {
           if (!(t.flags & kFirst)) continue;
           if (seg > 0 && !mbar_wait(q_empty, (seg - 1) & 1)) {
             set_status(&g_status, kStTimeout);
@@ -516,10 +525,10 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
   const int hc = 2 * (lane & 3);  // first head column of this lane in an 8-head tile
   HeadState<NT> hs;
   Cursor cur;
-  cursor_init(cur, p);
+  cursor_init<TP>(cur, p);
   Tile t;
   int seg = 0;
-  for (int n = 0; next_tile(cur, p, &t); ++n) {
+  for (int n = 0; next_tile<PS, TP>(cur, p, &t); ++n) {
     const int s = n % kStages;
     if (!mbar_wait(&full[s], (n / kStages) & 1)) {
       set_status(&g_status, kStTimeout);
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
       __syncwarp();
       if (lane == 0) mbar_arrive(q_empty);
       reset_state(hs);
-      if (p.pre_ml && (t.flags & kHead)) {
+      if (PS && p.pre_ml && (t.flags & kHead)) {
         // The query's prefix part is the starting state of the segment that
         // begins the query (its sum sits in one row group of lanes).
 #pragma unroll
@@ -574,7 +583,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
     if (t.flags & kLast) {
       total_sums(hs);
       const size_t head0 = (size_t)t.qf.qi * p.hq + (size_t)g * G;
-      const size_t sl = (size_t)blockIdx.x * (p.two_pass ? 4 : 2) + t.slot;
+      const size_t sl = (size_t)blockIdx.x * (TP ? 4 : 2) + t.slot;
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -806,10 +815,12 @@ cudaError_t setup_attn_kernels() {
   auto smem = [&](auto kernel) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   };
-  smem(sparse_attn_kernel<1, false>);
-  smem(sparse_attn_kernel<2, false>);
-  smem(sparse_attn_kernel<1, true>);
-  smem(sparse_attn_kernel<2, true>);
+  smem(sparse_attn_kernel<1, false, false>);
+  smem(sparse_attn_kernel<2, false, false>);
+  smem(sparse_attn_kernel<1, false, true>);
+  smem(sparse_attn_kernel<2, false, true>);
+  smem(sparse_attn_kernel<1, true, false>);
+  smem(sparse_attn_kernel<2, true, false>);
   int dev = 0, sms = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -886,12 +897,15 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   }
   const dim3 block(kProducerThreads + 32 * a.kv.hkv);
   const bool ps = a.qs.mode == DSA_MODE_PREFILL;
+  const bool tp = p.two_pass;
   if (p.group <= 8)
-    e = ps ? launch_pdl(sparse_attn_kernel<1, true>, dim3(grid), block, kSmemBytes, st, 1, p)
-           : launch_pdl(sparse_attn_kernel<1, false>, dim3(grid), block, kSmemBytes, st, 1, p);
+    e = ps   ? launch_pdl(sparse_attn_kernel<1, true, false>, dim3(grid), block, kSmemBytes, st, 1, p)
+        : tp ? launch_pdl(sparse_attn_kernel<1, false, true>, dim3(grid), block, kSmemBytes, st, 1, p)
+             : launch_pdl(sparse_attn_kernel<1, false, false>, dim3(grid), block, kSmemBytes, st, 1, p);
   else
-    e = ps ? launch_pdl(sparse_attn_kernel<2, true>, dim3(grid), block, kSmemBytes, st, 1, p)
-           : launch_pdl(sparse_attn_kernel<2, false>, dim3(grid), block, kSmemBytes, st, 1, p);
+    e = ps   ? launch_pdl(sparse_attn_kernel<2, true, false>, dim3(grid), block, kSmemBytes, st, 1, p)
+        : tp ? launch_pdl(sparse_attn_kernel<2, false, true>, dim3(grid), block, kSmemBytes, st, 1, p)
+             : launch_pdl(sparse_attn_kernel<2, false, false>, dim3(grid), block, kSmemBytes, st, 1, p);
   if (e != cudaSuccess) return e;
   if (p.two_pass)
     return launch_pdl(attn_combine2_kernel, dim3(a.qs.n_q, (a.hq + kCombHeads - 1) / kCombHeads),
