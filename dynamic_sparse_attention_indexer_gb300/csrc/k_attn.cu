@@ -93,14 +93,17 @@ struct AttnParams {
   int bt_per_query;      // the block table has one row per query (per-head tables), not per sequence
 };
 
-// 32-bit division when the products fit (the common case), 64-bit otherwise.
+// 32-bit division when the products fit (the common case), 64-bit otherwise;
+// the 64-bit forms stay out of line so that the kernels' code keeps one copy.
+__device__ __noinline__ int range_begin64(int T, int G, int c) { return (int)((long long)T * c / G); }
+__device__ __noinline__ int cta_of64(int T, int G, int x) { return (int)(((long long)(x + 1) * G - 1) / T); }
 __device__ __forceinline__ int range_begin(int T, int G, int c) {
   if ((unsigned long long)T * G < (1ull << 31)) return (int)((unsigned)(T * c) / (unsigned)G);
-  return (int)((long long)T * c / G);
+  return range_begin64(T, G, c);
 }
 __device__ __forceinline__ int cta_of(int T, int G, int x) {
   if ((unsigned long long)T * G < (1ull << 31)) return (int)((unsigned)((x + 1) * G - 1) / (unsigned)T);
-  return (int)(((long long)(x + 1) * G - 1) / T);
+  return cta_of64(T, G, x);
 }
 
 struct QueryInfo {
