@@ -125,6 +125,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// The same with an L2 cache policy made by createpolicy (l2_evict_first below).
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+// L2 policy for data streamed once per call (the decode step's indexer keys and
+// K/V rows): those lines go first, so that the small data a call writes and
+// reads back (scores, histograms, partial states, block tables) stays in L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
 // ------------------------------------------- programmatic dependent launch
 // A kernel launched with launch_pdl may start while the previous kernel of the
 // stream is still running; pdl_wait() blocks until that kernel has completed

@@ -351,6 +351,9 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
       cursor_init<TP>(cur, p);
       cur.hold = TP;
       const uint32_t q_bytes = (uint32_t)p.hq * kHeadDim * 2;
+      // Decode reads each attended row once per call: evict-first keeps the
+      // partial states, block table and selection in L2 around the stream.
+      const uint64_t stream_policy = l2_evict_first();
       int n = 0, seg = 0;
       for (int phase = 0; phase < 2 && !*s_abort; ++phase) {
       if (phase == 1) {
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(kProducerThreads + 8 * 32, 1) sparse_attn_kern
             const int r = c >> shift, part = c & shift;  // part 1: the V of a separate layout
             const size_t sl = (size_t)resolve(p, v0[u]);
             const __nv_bfloat16* src = (part ? p.vc : p.kc) + sl * p.row_stride + t0.qf.hoff;
-            bulk_g2s(st + r * p.pitch + part * p.v_off, src, p.cbytes, &full[s]);
+            bulk_g2s_hint(st + r * p.pitch + part * p.v_off, src, p.cbytes, &full[s], stream_policy);
           }
         }
         if (first && pt == 0)

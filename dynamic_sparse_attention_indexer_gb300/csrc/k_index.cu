@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
     // size or the first group holding a sequence's newest position (which the
     // cache write of this step may be the previous kernel to write).
     if (lane >= kGroupBlocks) return;
+    const uint64_t stream_policy = l2_evict_first();  // each key block is read once per call
     bool waited = false;
     for (int n = 0; next_group(cur, seg_start, jb_base, &g); ++n) {
       const int s = n % kStg;
@@ -156,8 +157,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
       mbar_arrive_expect_tx(&full[s], mine ? kIdxBlockBytes : 0);
       if (mine) {
         const int f = cur.f - g.count + lane;  // flattened block of this lane
-        bulk_g2s(stages + s * kIdxStageBytes + lane * kIdxBlockBytes,
-                 p.idx_cache + (size_t)ids[f - f_begin] * kIdxBlockBytes, kIdxBlockBytes, &full[s]);
+        bulk_g2s_hint(stages + s * kIdxStageBytes + lane * kIdxBlockBytes,
+                      p.idx_cache + (size_t)ids[f - f_begin] * kIdxBlockBytes, kIdxBlockBytes, &full[s],
+                      stream_policy);
       }
     }
     return;
