@@ -690,13 +690,34 @@ def run_gpu(args, rank, world, local_rank):
     step(0)
     torch.cuda.synchronize()
 
-    # --- end to end through the public API with host buffers
+    # --- end to end through the public API with host buffers.  A step's inputs
+    # (q, q_idx) sit back to back in one pinned staging buffer and one device
+    # buffer, its outputs (out, lse) likewise, so that each step is one copy in
+    # and one copy out (the API takes the device views).
     w0, kv0, b0, ws0 = layers[0]
-    q_host = [layers[l][0]["q"].cpu().pin_memory() for l in range(LAYERS)]
-    qi_host = [layers[l][0]["q_idx"].cpu().pin_memory() for l in range(LAYERS)]
-    out_host = torch.empty(b0["out"].shape, dtype=torch.bfloat16).pin_memory()
-    lse_host = torch.empty(b0["lse"].shape, dtype=torch.float32).pin_memory()
+    q_nb, qi_nb = w0["q"].numel() * 2, w0["q_idx"].numel()
+    out_nb, lse_nb = b0["out"].numel() * 2, b0["lse"].numel() * 4
+    in_dev, out_dev, views = [], [], []
+    for l in range(LAYERS):
+        w, kv, b, ws = layers[l]
+        bi = torch.empty(q_nb + qi_nb, dtype=torch.uint8, device=dev)
+        bo = torch.empty(out_nb + lse_nb, dtype=torch.uint8, device=dev)
+        qv = bi[:q_nb].view(torch.bfloat16).view(w["q"].shape)
+        qiv = bi[q_nb:].view(torch.int8).view(w["q_idx"].shape)
+        qv.copy_(w["q"])
+        qiv.copy_(w["q_idx"])
+        views.append((qv, qiv, bo[:out_nb].view(torch.bfloat16).view(b["out"].shape),
+                      bo[out_nb:].view(torch.float32).view(b["lse"].shape)))
+        in_dev.append(bi)
+        out_dev.append(bo)
+    in_host = [in_dev[l].cpu().pin_memory() for l in range(LAYERS)]
+    out_host = torch.empty(out_nb + lse_nb, dtype=torch.uint8).pin_memory()
     n_e2e = max(8, min(args.steps, 500))
+
+    def step_io(l):
+        w, kv, b, ws = layers[l]
+        qv, qiv, ov, lv = views[l]
+        dsa.decode_step(kv, qv, qiv, P, k, b["scores"], b["idx"], b["n_sel"], ov, lv, ws)
 
     # One graph per layer holds the whole call sequence a serving loop makes for
     # a step: the host-to-device copies of the step's queries (pinned host
@@ -708,11 +729,9 @@ def run_gpu(args, rank, world, local_rank):
             w, kv, b, ws = layers[l]
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                w["q"].copy_(q_host[l], non_blocking=True)
-                w["q_idx"].copy_(qi_host[l], non_blocking=True)
-                step(l)
-                out_host.copy_(b["out"], non_blocking=True)
-                lse_host.copy_(b["lse"], non_blocking=True)
+                in_dev[l].copy_(in_host[l], non_blocking=True)
+                step_io(l)
+                out_host.copy_(out_dev[l], non_blocking=True)
             e2e_graphs.append(g)
     torch.cuda.synchronize()
 
@@ -728,20 +747,18 @@ def run_gpu(args, rank, world, local_rank):
         for i in range(n_e2e):
             e2e_step(i)
         e2e_s = time.perf_counter() - t0
-    h2d = q_host[0].numel() * 2 + qi_host[0].numel()
-    d2h = out_host.numel() * 2 + lse_host.numel() * 4
+    h2d = in_host[0].numel()
+    d2h = out_host.numel()
 
     # The same sequence without a graph: every step the Python API call
     # (argument checks and launches through the C ABI), the host-to-device
     # copies of the step's queries from pinned memory before it and the
     # device-to-host copies of its output after it, then the host waits.
     def e2e_api_step(i):
-        w, kv, b, ws = layers[i % LAYERS]
-        w["q"].copy_(q_host[i % LAYERS], non_blocking=True)
-        w["q_idx"].copy_(qi_host[i % LAYERS], non_blocking=True)
-        step(i % LAYERS)
-        out_host.copy_(b["out"], non_blocking=True)
-        lse_host.copy_(b["lse"], non_blocking=True)
+        l = i % LAYERS
+        in_dev[l].copy_(in_host[l], non_blocking=True)
+        step_io(l)
+        out_host.copy_(out_dev[l], non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
@@ -810,12 +827,14 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clock_info,
         "e2e": {"value": tokens["e2e_tok"] / agg["e2e_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "graph replay: per step one captured graph of the host-to-device query copies, the "
-                       "decode step and the device-to-host output copies; the host waits for each step"},
+                "how": "graph replay: per step one captured graph of the host-to-device copy of the step's "
+                       "queries (q and q_idx packed in one pinned buffer), the decode step and the "
+                       "device-to-host copy of its output (out and lse packed); the host waits for each step"},
         "e2e_api": {"value": tokens["e2e_tok"] / agg["e2e_api_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "how": "no graph: per step the copies and the Python API call through the C ABI (host "
-                           "argument checks and kernel launches included); the host waits for each step"},
+                    "how": "no graph: per step the same two copies and the Python API call through the C "
+                           "ABI (host argument checks and kernel launches included); the host waits for each "
+                           "step"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
         "prefill": prefill,
