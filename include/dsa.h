@@ -28,6 +28,12 @@
  *     kernel goes on with block 0 in its place (outputs then undefined);
  *     dsa_check_device_status() reads and clears it.
  *   - Launch failures return DSA_ERR_CUDA with the CUDA error text.
+ *   - Kernels are launched with programmatic dependent launch: each one waits
+ *     (griddepcontrol.wait) for the previous kernel of the stream before it touches
+ *     anything that kernel may write, and may let the next kernel launch before it
+ *     finishes.  Kernels of the caller that follow a call on the same stream either
+ *     are launched without that attribute (the default: they start after the call
+ *     has completed) or must wait the same way before they read its outputs.
  *
  * Data layout (row-major, innermost last)
  *   k_cache, v_cache : bf16 rows of num_kv_heads * 128 values (every KV head of one position,
