@@ -49,7 +49,15 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device=None):
+    # The raw handle of the current stream without building a Stream object
+    # (a few microseconds less per call); the public accessor where it is missing.
+    if _raw_stream is not None:
+        idx = None if device is None else torch.device(device).index
+        return C.c_void_p(_raw_stream(torch.cuda.current_device() if idx is None else idx))
     return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
