@@ -693,7 +693,9 @@ def run_gpu(args, rank, world, local_rank):
     # --- end to end through the public API with host buffers.  A step's inputs
     # (q, q_idx) sit back to back in one pinned staging buffer and one device
     # buffer, its outputs (out, lse) likewise, so that each step is one copy in
-    # and one copy out (the API takes the device views).
+    # and one copy out (the API takes the device views); the copies are the
+    # library's staging copy (dsa_copy_async: a kernel, chained to the step by
+    # programmatic dependent launch, instead of the copy engines).
     w0, kv0, b0, ws0 = layers[0]
     q_nb, qi_nb = w0["q"].numel() * 2, w0["q_idx"].numel()
     out_nb, lse_nb = b0["out"].numel() * 2, b0["lse"].numel() * 4
@@ -729,9 +731,9 @@ def run_gpu(args, rank, world, local_rank):
             w, kv, b, ws = layers[l]
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                in_dev[l].copy_(in_host[l], non_blocking=True)
+                dsa.copy_async(in_dev[l], in_host[l])
                 step_io(l)
-                out_host.copy_(out_dev[l], non_blocking=True)
+                dsa.copy_async(out_host, out_dev[l])
             e2e_graphs.append(g)
     torch.cuda.synchronize()
 
@@ -756,9 +758,9 @@ def run_gpu(args, rank, world, local_rank):
     # device-to-host copies of its output after it, then the host waits.
     def e2e_api_step(i):
         l = i % LAYERS
-        in_dev[l].copy_(in_host[l], non_blocking=True)
+        dsa.copy_async(in_dev[l], in_host[l])
         step_io(l)
-        out_host.copy_(out_dev[l], non_blocking=True)
+        dsa.copy_async(out_host, out_dev[l])
         stream.synchronize()
 
     with torch.cuda.stream(stream):
@@ -829,7 +831,8 @@ def run_gpu(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h,
                 "how": "graph replay: per step one captured graph of the host-to-device copy of the step's "
                        "queries (q and q_idx packed in one pinned buffer), the decode step and the "
-                       "device-to-host copy of its output (out and lse packed); the host waits for each step"},
+                       "device-to-host copy of its output (out and lse packed), both copies by dsa_copy_async; "
+                       "the host waits for each step"},
         "e2e_api": {"value": tokens["e2e_tok"] / agg["e2e_api_s"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "how": "no graph: per step the same two copies and the Python API call through the C "

@@ -124,6 +124,19 @@ def _ws(ws):
     return (_ptr(ws), 0 if ws is None else ws.numel())
 
 
+def copy_async(dst, src):
+    """Staging copy by a kernel on the current stream of the CUDA side: dst and
+    src contiguous tensors of the same byte size, each a CUDA tensor or a
+    pinned CPU tensor (see dsa_copy_async)."""
+    nb = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nb or not dst.is_contiguous() or not src.is_contiguous():
+        raise ValueError("copy_async: dst and src must be contiguous and of the same size in bytes")
+    device = dst.device if dst.is_cuda else src.device
+    if not device.type == "cuda":
+        raise ValueError("copy_async: one side must be a CUDA tensor")
+    _check(lib().dsa_copy_async(_ptr(dst), _ptr(src), nb, _stream(device)))
+
+
 def kv_write(kv: PagedKV, slot_mapping, k, v, idx_k):
     _check(lib().dsa_kv_write(kv.ref, _ptr(slot_mapping), int(slot_mapping.numel()), _ptr(k), _ptr(v),
                               _ptr(idx_k), _stream(kv.k_cache.device)))

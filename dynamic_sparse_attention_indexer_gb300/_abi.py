@@ -49,6 +49,7 @@ SIGNATURES = {
     "dsa_index_scores": (c_i32, [PKV, PQS, c_p, c_i32, c_p, c_i32, c_p, C.c_size_t, c_p]),
     "dsa_topk_select": (c_i32, [PKV, PQS, c_p, c_i32, c_i32, c_i32, c_p, c_p, c_p, C.c_size_t, c_p]),
     "dsa_kv_gather": (c_i32, [PKV, PQS, c_p, c_p, c_i32, c_i32, c_p, c_p, c_p]),
+    "dsa_copy_async": (c_i32, [c_p, c_p, C.c_size_t, c_p]),
     "dsa_sparse_attn_decode": (c_i32, [PKV, c_p, c_i32, c_p, c_p, c_i32, c_i32, C.c_float, c_p, c_i32,
                                        c_p, c_p, C.c_size_t, c_p]),
     "dsa_sparse_attn_prefill": (c_i32, [PKV, PQS, c_p, c_i32, c_p, c_p, c_i32, c_i32, C.c_float, c_p,

@@ -662,6 +662,44 @@ dsa_status dsa_kv_gather(const dsa_paged_kv* kv_, const dsa_query_set* qs_, cons
   return DSA_OK;
 }
 
+// Device-side address of one end of a staging copy: device or managed memory
+// as it is, page-locked host memory through its device mapping; anything else
+// (pageable host memory, unknown pointers) is refused before any launch.
+static dsa_status staging_address(const void* ptr, const char* name, const void** out) {
+  cudaPointerAttributes at{};
+  const cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(DSA_ERR_INVALID_ARG, "%s: not a pointer the CUDA runtime knows (%s)", name, cudaGetErrorString(e));
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
+    *out = ptr;
+    return DSA_OK;
+  }
+  if (at.type == cudaMemoryTypeHost && at.devicePointer) {
+    *out = at.devicePointer;
+    return DSA_OK;
+  }
+  return fail(DSA_ERR_INVALID_ARG, "%s must be device memory or page-locked host memory", name);
+}
+
+dsa_status dsa_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+  if (!dst || !src) return fail(DSA_ERR_INVALID_ARG, "dst and src must be non-NULL");
+  if (!aligned16(dst) || !aligned16(src) || bytes % 16 != 0)
+    return fail(DSA_ERR_INVALID_ARG, "dst and src must be 16-byte aligned and bytes a multiple of 16 (got %zu)", bytes);
+  if (bytes == 0) return DSA_OK;
+  const void* d_src = nullptr;
+  const void* d_dst = nullptr;
+  DSA_TRY(staging_address(src, "src", &d_src));
+  DSA_TRY(staging_address(dst, "dst", &d_dst));
+  const char* s0 = static_cast<const char*>(d_src);
+  const char* d0 = static_cast<const char*>(d_dst);
+  if (s0 < d0 + bytes && d0 < s0 + bytes) return fail(DSA_ERR_INVALID_ARG, "dst and src overlap");
+  DSA_TRY(ensure_setup());
+  DSA_CUDA("staging copy launch", dsa::launch_stage_copy(const_cast<void*>(d_dst), d_src, bytes, stream));
+  return DSA_OK;
+}
+
 dsa_status dsa_sparse_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t hq, const int32_t* idx,
                                   const int32_t* n_sel, int32_t k, int32_t prefix, float scale, void* out,
                                   int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {

@@ -121,6 +121,9 @@ cudaError_t launch_kv_write_heads(const KV& kv, const int32_t* slots, int ntok, 
                                   const int8_t* idx_k, cudaStream_t st);
 cudaError_t launch_kv_write(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
                             const int8_t* idx_k, cudaStream_t st);
+// Staging copy by a kernel (device or page-locked host memory on either side;
+// device-side addresses, 16-byte aligned, bytes a multiple of 16).
+cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);
 cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, const int32_t* n_sel, int k,
                              int prefix, void* k_out, void* v_out, cudaStream_t st);
 

@@ -231,6 +231,30 @@ cudaError_t launch_kv_gather(const KV& kv, const QS& qs, const int32_t* idx, con
   return cudaGetLastError();
 }
 
+// Staging copy between device memory and page-locked host memory (or device to
+// device) by the SMs: 16-byte loads and stores over a grid-stride loop, after
+// the wait on the previous kernel of the stream (which may have written src).
+// Host memory is reached through its device-side address (unified addressing).
+namespace {
+__global__ void __launch_bounds__(256) stage_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                         size_t n16) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) dst[i] = src[i];
+}
+}  // namespace
+
+cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  const size_t n16 = bytes / 16;
+  size_t blocks = (n16 + 255) / 256;
+  const size_t cap = 4 * (size_t)attn_grid_ctas();
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(stage_copy_kernel, dim3((unsigned)blocks), dim3(256), 0, st, 1,
+                    static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+}
+
 cudaError_t read_clear_status_misc(int* code, cudaStream_t st) {
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st);

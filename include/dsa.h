@@ -64,7 +64,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 3
+#define DSA_ABI_VERSION 4
 
 typedef enum dsa_status {
   DSA_OK = 0,
@@ -349,6 +349,20 @@ dsa_status dsa_prefill_step(const dsa_paged_kv* kv, const dsa_query_set* qs, con
                             int32_t num_q_heads, int32_t prefix_len, int32_t k, float softmax_scale,
                             int32_t* scores, int32_t ld, int32_t* idx, int32_t* n_sel, void* out,
                             int32_t out_dtype, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------- staging copy --- */
+/* Copies `bytes` from src to dst with a kernel on `stream`: the staging of a
+ * step's inputs and outputs in a serving loop, without the copy engines.
+ * Either side may be device memory or page-locked host memory (cudaHostAlloc,
+ * cudaMallocHost or cudaHostRegister; the exception to "device memory only"
+ * above), which the kernel reaches through its device mapping; pageable host
+ * memory and overlapping ranges return DSA_ERR_INVALID_ARG before anything is
+ * launched.  dst and src 16-byte aligned, bytes a multiple of 16 (0: nothing
+ * happens).  Launched with programmatic dependent launch like every kernel
+ * here: it reads src only after the previous kernel of the stream has
+ * completed, so a step's outputs can be copied right behind it.  The host sees
+ * a copy into its memory once it has synchronised with the stream. */
+dsa_status dsa_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------- fused decode step --- */
 /* Steps 1-4 for one decode token per sequence, in one call: scores (written to

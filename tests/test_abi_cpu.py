@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(raw, n), f"{n} declared in dsa.h but not exported"
         assert n in _abi.SIGNATURES, f"{n} has no ctypes signature"
-    assert lib.dsa_abi_version() == 3
+    assert lib.dsa_abi_version() == 4
     assert lib.dsa_status_string(OOM) == b"DSA_ERR_OOM"
 
 
@@ -305,3 +305,19 @@ def test_per_head_decode_checks(lib):
     if not torch.cuda.is_available():
         assert call() == CUDA                     # every argument valid: the call reaches the runtime
         assert call(bth=0x50000) == CUDA          # with per-head block tables as well
+
+
+def test_copy_async_checks(lib):
+    """The staging copy refuses NULL, misaligned and odd-sized arguments on the
+    host, does nothing for zero bytes, and never launches for pointers the
+    runtime cannot vouch for (here: no device at all)."""
+    fn = lib.dsa_copy_async
+    assert fn(None, 0x1000, 16, None) == INVALID
+    assert fn(0x1000, None, 16, None) == INVALID
+    assert fn(0x1008, 0x2000, 16, None) == INVALID
+    assert fn(0x1000, 0x2008, 16, None) == INVALID
+    assert fn(0x1000, 0x2000, 24, None) == INVALID
+    assert fn(0x1000, 0x2000, 0, None) == DSA_OK
+    import torch
+    if not torch.cuda.is_available():
+        assert fn(0x1000, 0x2000, 16, None) != DSA_OK
