@@ -672,6 +672,12 @@ static dsa_status staging_address(const void* ptr, const char* name, const void*
     cudaGetLastError();
     return fail(DSA_ERR_INVALID_ARG, "%s: not a pointer the CUDA runtime knows (%s)", name, cudaGetErrorString(e));
   }
+  if (at.type == cudaMemoryTypeDevice) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != at.device)
+      return fail(DSA_ERR_INVALID_ARG, "%s is device memory of device %d, not of the current device %d", name,
+                  at.device, dev);
+  }
   if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) {
     *out = ptr;
     return DSA_OK;

@@ -356,8 +356,8 @@ dsa_status dsa_prefill_step(const dsa_paged_kv* kv, const dsa_query_set* qs, con
  * Either side may be device memory or page-locked host memory (cudaHostAlloc,
  * cudaMallocHost or cudaHostRegister; the exception to "device memory only"
  * above), which the kernel reaches through its device mapping; pageable host
- * memory and overlapping ranges return DSA_ERR_INVALID_ARG before anything is
- * launched.  dst and src 16-byte aligned, bytes a multiple of 16 (0: nothing
+ * memory, device memory of another device and overlapping ranges return
+ * DSA_ERR_INVALID_ARG before anything is launched.  dst and src 16-byte aligned, bytes a multiple of 16 (0: nothing
  * happens).  Launched with programmatic dependent launch like every kernel
  * here: it reads src only after the previous kernel of the stream has
  * completed, so a step's outputs can be copied right behind it.  The host sees
