@@ -127,8 +127,8 @@ def window_decode_line(spec, lens, ms, peak, peak_kind):
     rows = sum(min(WINDOW, int(L)) for L in lens)
     nbytes = rows * spec.num_kv_heads * 512 + 2 * len(lens) * spec.num_q_heads * 128 * 2
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"kernel": "dsa_window_attn_decode per call in a graph: window_idx_kernel + sparse_attn_kernel + "
-                      "attn_combine_kernel", "window": WINDOW, "ms": ms, "bound": "hbm", "achieved": gbs,
+    return {"kernel": "dsa_window_attn_decode per call in a graph: sparse_attn_kernel (the window's rows "
+                      "walked from each context's end) + attn_combine_kernel", "window": WINDOW, "ms": ms, "bound": "hbm", "achieved": gbs,
             "peak": peak, "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes, "peak_kind": peak_kind}
 
 

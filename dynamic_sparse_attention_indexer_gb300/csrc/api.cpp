@@ -380,19 +380,18 @@ dsa_status attn_impl(const dsa_paged_kv* kv_, const dsa_query_set* qs_, const vo
 
 // Local sliding-window attention (the hybrid attention's local sibling): decode
 // workspace = index lists [B][window] + counts [B] + the attention partials.
+// Decode window attention: the attention's own workspace only (the window's
+// rows are walked from each context's end, with no index lists).
 struct WindowLayout {
-  size_t idx = 0, n_sel = 0, attn = 0, total = 0;
+  size_t attn = 0, total = 0;
   Layout L;
 };
 
 WindowLayout window_layout(const dsa::KV& kv, int32_t hq, int32_t window) {
   WindowLayout W;
   const dsa::QS qs{DSA_MODE_DECODE, kv.batch, 0, 0};
-  W.idx = 0;
-  W.n_sel = up256((size_t)kv.batch * (size_t)window * 4);
-  W.attn = W.n_sel + up256((size_t)kv.batch * 4);
-  W.L = layout(kv, qs, window, hq, 0);
-  W.total = W.attn + W.L.total;
+  W.L = layout(kv, qs, 0, hq, window);
+  W.total = W.L.total;
   return W;
 }
 
@@ -874,19 +873,19 @@ dsa_status dsa_window_attn_decode(const dsa_paged_kv* kv_, const void* q, int32_
   DSA_TRY(check_ws(ws, ws_bytes, W.total));
   DSA_TRY(ensure_setup());
   char* w = static_cast<char*>(ws);
-  int32_t* idx = reinterpret_cast<int32_t*>(w + W.idx);
-  int32_t* n_sel = reinterpret_cast<int32_t*>(w + W.n_sel);
-  DSA_CUDA("window index launch", dsa::launch_window_idx(kv, window, idx, n_sel, stream));
+  // The window's rows are contiguous: the attention walks them as the
+  // query's prefix part from the window's start, with no index lists.
   dsa::AttnArgs a;
   a.kv = kv;
   a.qs = qs;
   a.q = q;
   a.hq = hq;
-  a.idx = idx;
-  a.n_sel = n_sel;
+  a.idx = nullptr;
+  a.n_sel = nullptr;
   a.slot = nullptr;
-  a.k = window;
-  a.prefix = 0;
+  a.window = window;
+  a.k = 0;
+  a.prefix = window;
   a.scale = scale;
   a.out = out;
   a.out_dtype = out_dtype;

@@ -64,6 +64,8 @@ struct AttnArgs {
   int bt_per_query = 0;  // kv.block_table has one row per query (qi), not per sequence
   int prefix_ctas = 0;  // decode: > 0 walks the prefix rows first, over that many CTAs, before the wait on
                         // the previous kernel (only where that kernel is the step's own selection)
+  int window = 0;  // decode: > 0 attends each query's last `window` positions (prefix = window, k = 0,
+                   // no index lists): the local sliding-window sibling
 };
 
 // Kernel launches (return the launch error, if any).
@@ -109,7 +111,6 @@ cudaError_t launch_dense_attn(const AttnArgs& a, int n_dense, void* mask_ws, cud
                               bool mask_ready = false);  // mask_ready: the bitmap is already in mask_ws
 // Decode window attention's index lists: idx[b][j] = L_b - min(window, L_b) + j,
 // n_sel[b] = min(window, L_b), -1 past it (k_misc.cu).
-cudaError_t launch_window_idx(const KV& kv, int window, int32_t* idx, int32_t* n_sel, cudaStream_t st);
 size_t dense_mask_bytes(const QS& qs, int n_dense);
 int dense_tile_queries(int group);
 // Prefill index scores and top-k in one kernel, the scores never written (k_pselect.cu).

@@ -91,6 +91,7 @@ struct AttnParams {
   const float* pre_o;    // queries beforehand ([n_q][hq] and [n_q][hq][128]), or null
   int hsplit;            // decode, per-KV-head indexer: query qi is (sequence qi / hsplit, head qi % hsplit)
   int bt_per_query;      // the block table has one row per query (per-head tables), not per sequence
+  int window;            // decode: > 0 attends the last `window` positions of each context, no selection
 };
 
 // 32-bit division when the products fit (the common case), 64-bit otherwise;
@@ -108,6 +109,7 @@ __device__ __forceinline__ int cta_of(int T, int G, int x) {
 
 struct QueryInfo {
   int qi, seq, n_pre, rows;
+  int pre_off;  // position of the query's first prefix-part row (the window's start; else 0)
   int bt_row;  // row of the block table: the query's (per-head tables) or its sequence's
   int hoff;  // bf16 offset of the query's KV head inside a cache row (per-head indexer), else 0
 };
@@ -127,6 +129,13 @@ __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi, int
   qf.bt_row = !PS && p.bt_per_query ? qi : qf.seq;
   qf.hoff = hh * kHeadDim;
   const int pos = PS ? p.pos0 + qi : min(__ldg(p.ctx + qf.seq), p.max_ctx) - 1;
+  qf.pre_off = 0;
+  if (!PS && p.window > 0) {  // the window [pos + 1 - n, pos]: contiguous rows, no index list
+    qf.n_pre = max(0, min(p.window, pos + 1));
+    qf.pre_off = pos + 1 - qf.n_pre;
+    qf.rows = qf.n_pre;
+    return qf;
+  }
   if constexpr (TP) {
     const bool past = pos + 1 > p.prefix;
     if (pass == 0) {
@@ -238,12 +247,12 @@ struct RowRef {
   int lo;  // row inside the block, or -1
 };
 __device__ __forceinline__ int fetch_first(const AttnParams& p, const QueryInfo& qf, int r) {
-  if (r < qf.n_pre) return __ldg(p.bt + (size_t)qf.bt_row * p.max_blocks + (r >> 6));
+  if (r < qf.n_pre) return __ldg(p.bt + (size_t)qf.bt_row * p.max_blocks + ((qf.pre_off + r) >> 6));
   const size_t e = (size_t)qf.qi * p.k + (r - qf.n_pre);
   return p.slot ? __ldg(p.slot + e) : __ldg(p.idx + e);
 }
 __device__ __forceinline__ RowRef fetch_second(const AttnParams& p, const QueryInfo& qf, int r, int first) {
-  if (r < qf.n_pre) return RowRef{first, r & 63};  // prefix row r is position r
+  if (r < qf.n_pre) return RowRef{first, (qf.pre_off + r) & 63};  // prefix-part row r is position pre_off + r
   if (p.slot) return RowRef{first, -1};
   int pos = first;
   if ((unsigned)pos >= (unsigned)p.max_blocks * kBlock) {
@@ -873,6 +882,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.pre_o = a.ws.pre_o;
   p.hsplit = a.hsplit > 1 ? a.hsplit : 1;
   p.bt_per_query = a.bt_per_query;
+  p.window = a.qs.mode == DSA_MODE_DECODE ? a.window : 0;
   p.rows_per_q = p.pre_ml ? a.k : a.prefix + a.k;
   p.two_pass = 0;
   p.units1 = 0;

@@ -5,10 +5,6 @@
 // §2.2: the attended rows of every query copied into a contiguous buffer,
 // 16 bytes per thread, prefix rows first, then the selected rows in order.
 // The attention kernels do not need it (they gather into shared memory).
-// window_idx_kernel writes the index lists of decode window attention (the
-// hybrid attention's local sliding window): the last `window` positions of
-// each sequence, which the sparse attention kernel then attends like a
-// selection.
 #include "common.cuh"
 #include "internal.h"
 
@@ -121,19 +117,6 @@ __global__ void __launch_bounds__(128) kv_gather_kernel(const GatherParams p) {
   *reinterpret_cast<int4*>(p.vo + o) = vval;
 }
 
-// idx[b][j] = L_b - n + j for j < n = min(window, L_b), -1 after; n_sel[b] = n.
-__global__ void __launch_bounds__(256) window_idx_kernel(const int32_t* __restrict__ lens, int window, int32_t* idx,
-                                                          int32_t* n_sel) {
-  pdl_wait();
-  pdl_trigger();
-  const int b = blockIdx.y;
-  const int L = max(__ldg(lens + b), 0);
-  const int n = min(window, L);
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < window; j += gridDim.x * blockDim.x)
-    idx[(size_t)b * window + j] = j < n ? L - n + j : -1;
-  if (blockIdx.x == 0 && threadIdx.x == 0) n_sel[b] = n;
-}
-
 // The (sequence, KV head) pairs of a per-head indexer as sequences of their own:
 // a head's indexer keys of block blk are virtual block blk * hkv + h (bt2); its
 // K and V rows are the head-h slices of block blk (bt3, the block id itself).
@@ -161,11 +144,6 @@ cudaError_t launch_head_table(const KV& kv, const int32_t* bt_heads, int32_t* bt
   const int bx = min((kv.max_blocks + 255) / 256, 32);
   return launch_ordered(head_table_kernel, dim3(bx, kv.batch * kv.hkv), dim3(256), 0, st, kv.block_table, bt_heads,
                         kv.context_lens, kv.batch, kv.max_blocks, kv.num_blocks, kv.hkv, bt2, bt3, lens2);
-}
-
-cudaError_t launch_window_idx(const KV& kv, int window, int32_t* idx, int32_t* n_sel, cudaStream_t st) {
-  const int bx = min((window + 255) / 256, 64);
-  return launch_pdl(window_idx_kernel, dim3(bx, kv.batch), dim3(256), 0, st, 1, kv.context_lens, window, idx, n_sel);
 }
 
 cudaError_t launch_kv_write_heads(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,

@@ -318,9 +318,9 @@ size_t dsa_prefill_attn_workspace_size(const dsa_paged_kv* kv, const dsa_query_s
  * selection.  Same q / out / lse layout, head rules (num_q_heads <= 64, group
  * <= 16) and softmax as the sparse attention above; window in [1, 2^24].
  * Decode form: the newest token of every sequence (pos = context_len - 1),
- * through the sparse attention kernels over the window's positions; the
- * workspace holds the window's index lists and the attention partials,
- * dsa_window_workspace_size bytes. */
+ * through the sparse attention kernels, which walk the window's rows from the
+ * end of each context (contiguous positions: no index lists); the workspace
+ * holds the attention partials, dsa_window_workspace_size bytes. */
 size_t dsa_window_workspace_size(const dsa_paged_kv* kv, int32_t num_q_heads, int32_t window);
 dsa_status dsa_window_attn_decode(const dsa_paged_kv* kv, const void* q, int32_t num_q_heads,
                                   int32_t window, float softmax_scale, void* out, int32_t out_dtype,
