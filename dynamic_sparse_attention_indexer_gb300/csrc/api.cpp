@@ -194,9 +194,14 @@ void overlap_shape(const dsa::KV& kv, int prefix, int* c_cap, int* prefix_ctas) 
   *c_cap = c;
   const int held = dsa::decode_select_ctas(kv, prefix, c);
   if (held <= kv.batch) {
-    // one CTA per sequence: a short selection, nothing to overlap (8K, B = 32:
-    // one pass 48.5 us, two passes 48.9 us)
-    *c_cap = 16;
+    // one CTA per sequence already fills half of the SMs: one pass, nothing
+    // to overlap (8K, B = 32: one pass 48.5 us, two passes 48.9 us).  The
+    // clusters are then capped so that the selection is about one wave of
+    // CTAs at two per SM (per-KV-head step, 64 rows of 128K: clusters of 16
+    // 168 us, of 8 157 us, of 4 153 us, of 2 155 us).
+    int cap = 16;
+    while (cap > 1 && cap * kv.batch > 2 * sms) cap >>= 1;
+    *c_cap = cap;
     *prefix_ctas = 0;
     return;
   }
