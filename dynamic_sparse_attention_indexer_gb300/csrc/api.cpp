@@ -418,7 +418,7 @@ struct HeadsPlan {
   dsa::KV kv2;    // the virtual sequences (scoring and selection)
   dsa::QS qs2;
   dsa::KV kva;    // the attention's view of the cache: one KV head per query
-  size_t bt2 = 0, bt3 = 0, lens2 = 0, sel = 0, total = 0;
+  size_t sel = 0, total = 0;
   Layout L;
 };
 
@@ -435,10 +435,7 @@ dsa_status heads_plan(const dsa::KV& kv, int32_t hq, int32_t k, int32_t prefix, 
   h.kva = kv;
   h.kva.hkv = 1;
   h.kva.adjacent = false;
-  h.bt2 = 0;
-  h.bt3 = up256((size_t)h.kv2.batch * (size_t)kv.max_blocks * 4);
-  h.lens2 = h.bt3 + up256((size_t)h.kv2.batch * (size_t)kv.max_blocks * 4);
-  h.sel = h.lens2 + up256((size_t)h.kv2.batch * 4);
+  h.sel = 0;
   h.L = layout(h.kv2, h.qs2, k, hq / kv.hkv, prefix);
   h.total = h.sel + h.L.total;
   *out = h;
@@ -815,26 +812,27 @@ dsa_status dsa_decode_step_heads(const dsa_paged_kv* kv_, const void* q, const i
   DSA_TRY(check_ws(ws, ws_bytes, h.total));
   DSA_TRY(ensure_setup());
   char* w = static_cast<char*>(ws);
-  int32_t* bt2 = reinterpret_cast<int32_t*>(w + h.bt2);
-  int32_t* bt3 = reinterpret_cast<int32_t*>(w + h.bt3);
-  int32_t* lens2 = reinterpret_cast<int32_t*>(w + h.lens2);
-  DSA_CUDA("head table launch", dsa::launch_head_table(kv, block_table_heads, bt2, bt3, lens2, stream));
-  dsa::KV kv2 = h.kv2;
-  kv2.block_table = bt2;
-  kv2.context_lens = lens2;
-  const dsa::SelState s2 = sel_state(h.L, w + h.sel, false);  // no cache slots: they would be virtual
-  // the scoring kernel reads block ids and lengths before its dependency wait:
-  // the virtual ones come from the kernel just launched, so no early start
-  DSA_CUDA("decode index launch", dsa::launch_decode_index(kv2, q_idx, prefix, scores, ld, &s2, k, stream, false));
+  // The (sequence, KV head) pairs are the rows of the scoring and the
+  // selection: row b * Hkv + h scores head h's indexer keys (block blk * Hkv + h
+  // of the indexer cache, blk from the shared table or from head h's own) with
+  // its sequence's context length; the attention reads head h's K and V rows
+  // of the same blocks.  The kernels map the rows themselves, so the scoring
+  // kernel starts early as in dsa_decode_step.
+  const dsa::KV kv2 = h.kv2;
+  const dsa::SelState s2 = sel_state(h.L, w + h.sel, false);  // no cache slots: the attention resolves positions
+  DSA_CUDA("decode index launch", dsa::launch_decode_index(kv2, q_idx, prefix, scores, ld, &s2, k, stream, true,
+                                                           kv.hkv, block_table_heads));
   int c_cap, prefix_ctas;
   overlap_shape(h.kv2, prefix, &c_cap, &prefix_ctas);
   DSA_CUDA("decode selection launch",
-           dsa::launch_decode_select(kv2, scores, ld, prefix, k, s2, idx, n_sel, stream, c_cap));
+           dsa::launch_decode_select(kv2, scores, ld, prefix, k, s2, idx, n_sel, stream, c_cap, kv.hkv));
   dsa::AttnArgs a;
   a.prefix_ctas = prefix_ctas;
   a.kv = h.kva;
-  a.kv.block_table = bt3;  // row b * hkv + h: head h's blocks of sequence b
-  a.bt_per_query = 1;
+  if (block_table_heads) {  // head h of sequence b reads row h * batch + b of the per-head tables
+    a.kv.block_table = block_table_heads;
+    a.bt_head_rows = kv.batch;
+  }
   a.qs = h.qs2;
   a.q = q;
   a.hq = hq / kv.hkv;

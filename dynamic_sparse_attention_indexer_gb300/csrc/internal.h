@@ -62,6 +62,7 @@ struct AttnArgs {
   AttnWs ws;
   int hsplit = 1;  // decode with a per-KV-head indexer: query qi is (sequence qi / hsplit, KV head qi % hsplit)
   int bt_per_query = 0;  // kv.block_table has one row per query (qi), not per sequence
+  int bt_head_rows = 0;  // decode, per-head block tables: query qi = (b, h) reads row h * bt_head_rows + b
   int prefix_ctas = 0;  // decode: > 0 walks the prefix rows first, over that many CTAs, before the wait on
                         // the previous kernel (only where that kernel is the step's own selection)
   int window = 0;  // decode: > 0 attends each query's last `window` positions (prefix = window, k = 0,
@@ -69,25 +70,22 @@ struct AttnArgs {
 };
 
 // Kernel launches (return the launch error, if any).
+// hsplit > 1: the per-KV-head indexer over kv.batch = sequences x hsplit rows
+// (kv.num_blocks = the KV cache's blocks x hsplit, kv.block_table and
+// kv.context_lens those of the sequences; bt_heads: per-head tables or null).
 cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, int* scores, int ld,
-                                const SelState* sel, int k, cudaStream_t st, bool early = true);
-// Per-KV-head indexer: the virtual block table and context lengths of the
-// (sequence, KV head) pairs, bt2[b * hkv + h][j] = bt[b][j] * hkv + h (-1 for an
-// id outside the pool), lens2[b * hkv + h] = lens[b] (k_misc.cu).
-// bt_heads: per-head block tables [hkv][batch][max_blocks] (the per-head block
-// bitmaps of the allocator), or null for the shared table.  bt3[b * hkv + h][j]:
-// the block id itself (head h's table row), for the attention.
-cudaError_t launch_head_table(const KV& kv, const int32_t* bt_heads, int32_t* bt2, int32_t* bt3, int32_t* lens2,
-                              cudaStream_t st);
+                                const SelState* sel, int k, cudaStream_t st, bool early = true, int hsplit = 1,
+                                const int32_t* bt_heads = nullptr);
 cudaError_t launch_decode_hist(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                const SelState& sel, cudaStream_t st);
 // Whether the decode selection of this batch runs with one CTA per SM.
 bool decode_select_spread(const KV& kv, int prefix);
 // c_cap: at most that many CTAs per sequence (the fused step leaves SMs to the
 // attention's first pass).
+// csplit > 1: kv.batch = sequences x csplit rows, kv.context_lens per sequence.
 cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
                                  const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st,
-                                 int c_cap = 16);
+                                 int c_cap = 16, int csplit = 1);
 // CTAs the decode selection of this batch launches with that cap.
 int decode_select_ctas(const KV& kv, int prefix, int c_cap);
 // CTAs of the persistent attention grid on the current device.

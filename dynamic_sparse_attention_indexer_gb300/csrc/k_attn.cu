@@ -90,7 +90,8 @@ struct AttnParams {
   const float2* pre_ml;  // prefill: the prefix part of every query, computed per tile of
   const float* pre_o;    // queries beforehand ([n_q][hq] and [n_q][hq][128]), or null
   int hsplit;            // decode, per-KV-head indexer: query qi is (sequence qi / hsplit, head qi % hsplit)
-  int bt_per_query;      // the block table has one row per query (per-head tables), not per sequence
+  int bt_per_query;      // the block table has one row per query, not per sequence
+  int bt_head_rows;      // per-head block tables [Hkv][batch]: query (b, h) reads row h * bt_head_rows + b
   int window;            // decode: > 0 attends the last `window` positions of each context, no selection
 };
 
@@ -126,7 +127,7 @@ __device__ __forceinline__ QueryInfo query_info(const AttnParams& p, int qi, int
   qf.qi = qi;
   const int hh = !PS && p.hsplit > 1 ? qi % p.hsplit : 0;
   qf.seq = PS ? p.seq : p.hsplit > 1 ? (qi - hh) / p.hsplit : qi;
-  qf.bt_row = !PS && p.bt_per_query ? qi : qf.seq;
+  qf.bt_row = PS ? qf.seq : p.bt_head_rows ? hh * p.bt_head_rows + qf.seq : p.bt_per_query ? qi : qf.seq;
   qf.hoff = hh * kHeadDim;
   const int pos = PS ? p.pos0 + qi : min(__ldg(p.ctx + qf.seq), p.max_ctx) - 1;
   qf.pre_off = 0;
@@ -882,6 +883,7 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t st) {
   p.pre_o = a.ws.pre_o;
   p.hsplit = a.hsplit > 1 ? a.hsplit : 1;
   p.bt_per_query = a.bt_per_query;
+  p.bt_head_rows = a.bt_head_rows;
   p.window = a.qs.mode == DSA_MODE_DECODE ? a.window : 0;
   p.rows_per_q = p.pre_ml ? a.k : a.prefix + a.k;
   p.two_pass = 0;

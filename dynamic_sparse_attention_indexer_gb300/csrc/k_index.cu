@@ -59,7 +59,22 @@ struct DecodeIndexParams {
   int* scores;
   int* coarse;  // [B][kCoarseBins] global histograms, or nullptr
   int ld, max_blocks, num_blocks, prefix, max_ctx, batch, k;
+  // Per-KV-head indexer (hsplit = Hkv > 1): row v = b * hsplit + h scores head
+  // h's keys, block id blk * hsplit + h of the indexer cache, blk from the
+  // shared table (row b) or from head h's own table (bt_heads[h][b]); ctx per
+  // sequence; num_blocks counts the KV cache's blocks.
+  int hsplit, real_batch;
+  const int32_t* bt_heads;
 };
+
+// Block id of block-table slot j of row v, checked against the pool.
+__device__ __forceinline__ int row_block(const DecodeIndexParams& p, int v, int j) {
+  if (p.hsplit <= 1) return load_block(p.bt, v, p.max_blocks, j, p.num_blocks, &g_status);
+  const int b = v / p.hsplit, h = v - b * p.hsplit;
+  const int blk = p.bt_heads ? load_block(p.bt_heads, h * p.real_batch + b, p.max_blocks, j, p.num_blocks, &g_status)
+                             : load_block(p.bt, b, p.max_blocks, j, p.num_blocks, &g_status);
+  return blk * p.hsplit + h;
+}
 
 // Sums the consumer warps' histograms of one sequence into its global one
 // (called by all consumer threads, ct = 0 .. 255); with `clear` the warp
@@ -107,7 +122,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
     }
     mbar_fence_init();
   }
-  candidate_blocks(p.ctx, p.batch, p.max_ctx, P, seg_start, len, scratch);
+  candidate_blocks(p.ctx, p.batch, p.max_ctx, P, seg_start, len, scratch, p.hsplit);
   const long long T = seg_start[p.batch];
   const int f_begin = (int)(T * blockIdx.x / gridDim.x), f_end = (int)(T * (blockIdx.x + 1) / gridDim.x);
   if (f_begin >= f_end) return;
@@ -127,7 +142,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) decode_index_kernel(const Deco
       const int mid = (lo + hi + 1) >> 1;
       if (seg_start[mid] <= f) lo = mid; else hi = mid - 1;
     }
-    ids[f - f_begin] = load_block(p.bt, lo, p.max_blocks, f - seg_start[lo] + jb_base, p.num_blocks, &g_status);
+    ids[f - f_begin] = row_block(p, lo, f - seg_start[lo] + jb_base);
   }
   __syncthreads();
   GroupCursor cur{f_begin, f_end, b_first};
@@ -478,8 +493,12 @@ static int index_grid(const KV& kv, int prefix) {
 }
 
 cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, int* scores, int ld,
-                                const SelState* sel, int k, cudaStream_t st, bool early) {
+                                const SelState* sel, int k, cudaStream_t st, bool early, int hsplit,
+                                const int32_t* bt_heads) {
   DecodeIndexParams p;
+  p.hsplit = hsplit > 1 ? hsplit : 1;
+  p.real_batch = kv.batch / p.hsplit;
+  p.bt_heads = bt_heads;
   p.idx_cache = kv.idx_cache;
   p.bt = kv.block_table;
   p.ctx = kv.context_lens;
@@ -488,7 +507,7 @@ cudaError_t launch_decode_index(const KV& kv, const int8_t* q_idx, int prefix, i
   p.coarse = sel ? sel->coarse : nullptr;
   p.ld = ld;
   p.max_blocks = kv.max_blocks;
-  p.num_blocks = kv.num_blocks;
+  p.num_blocks = kv.num_blocks / p.hsplit;
   p.prefix = prefix;
   p.max_ctx = kv.max_ctx;
   p.batch = kv.batch;

@@ -117,34 +117,7 @@ __global__ void __launch_bounds__(128) kv_gather_kernel(const GatherParams p) {
   *reinterpret_cast<int4*>(p.vo + o) = vval;
 }
 
-// The (sequence, KV head) pairs of a per-head indexer as sequences of their own:
-// a head's indexer keys of block blk are virtual block blk * hkv + h (bt2); its
-// K and V rows are the head-h slices of block blk (bt3, the block id itself).
-// The block id comes from the shared table, or from head h's own table (the
-// per-head block bitmaps of the allocator).
-__global__ void __launch_bounds__(256) head_table_kernel(const int32_t* __restrict__ bt,
-                                                          const int32_t* __restrict__ bt_heads,
-                                                          const int32_t* __restrict__ lens, int batch, int max_blocks,
-                                                          int num_blocks, int hkv, int32_t* bt2, int32_t* bt3,
-                                                          int32_t* lens2) {
-  const int v = blockIdx.y, b = v / hkv, h = v - b * hkv;
-  const int32_t* row = bt_heads ? bt_heads + ((size_t)h * batch + b) * max_blocks : bt + (size_t)b * max_blocks;
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < max_blocks; j += gridDim.x * blockDim.x) {
-    const int blk = __ldg(row + j);
-    bt2[(size_t)v * max_blocks + j] = (unsigned)blk < (unsigned)num_blocks ? blk * hkv + h : -1;
-    bt3[(size_t)v * max_blocks + j] = blk;  // checked against the pool where the attention uses it
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) lens2[v] = __ldg(lens + b);
-}
-
 }  // namespace
-
-cudaError_t launch_head_table(const KV& kv, const int32_t* bt_heads, int32_t* bt2, int32_t* bt3, int32_t* lens2,
-                              cudaStream_t st) {
-  const int bx = min((kv.max_blocks + 255) / 256, 32);
-  return launch_ordered(head_table_kernel, dim3(bx, kv.batch * kv.hkv), dim3(256), 0, st, kv.block_table, bt_heads,
-                        kv.context_lens, kv.batch, kv.max_blocks, kv.num_blocks, kv.hkv, bt2, bt3, lens2);
-}
 
 cudaError_t launch_kv_write_heads(const KV& kv, const int32_t* slots, int ntok, const void* k, const void* v,
                                   const int8_t* idx_k, cudaStream_t st) {

@@ -63,6 +63,7 @@ struct SelectParams {
   int32_t* idx;
   int32_t* n_sel;
   int32_t* slot;  // cache slots of the selected positions, or nullptr
+  int csplit;     // row b's context length is ctx[b / csplit] (per-KV-head rows: csplit = Hkv)
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(NTH) decode_select_kernel(const SelectParams p
   int* e_slot = s_ent + 2 * kSelCap;
   const int tid = threadIdx.x, lane = tid & 31, b = blockIdx.y;
   const int r = C > 1 ? (int)cluster_rank() : 0;
-  const int L = min(__ldg(p.ctx + b), p.max_ctx);
+  const int L = min(__ldg(p.ctx + (p.csplit > 1 ? b / p.csplit : b)), p.max_ctx);
   const int n_cand = max(0, L - p.prefix);
   const int tb = p.prefix + (int)((long long)n_cand * r / C);
   const int te = p.prefix + (int)((long long)n_cand * (r + 1) / C);
@@ -675,8 +676,10 @@ int decode_select_ctas(const KV& kv, int prefix, int c_cap) {
 }
 
 cudaError_t launch_decode_select(const KV& kv, const int32_t* scores, int ld, int prefix, int k,
-                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st, int c_cap) {
+                                 const SelState& sel, int32_t* idx, int32_t* n_sel, cudaStream_t st, int c_cap,
+                                 int csplit) {
   SelectParams p;
+  p.csplit = csplit > 1 ? csplit : 1;
   p.scores = scores;
   p.ctx = kv.context_lens;
   p.bt = kv.block_table;

@@ -11,15 +11,17 @@ namespace dsa {
 constexpr int kGroupBlocks = 4;  // cache blocks per scoring stage (4 x 4 KB)
 
 // Candidate blocks of every sequence and their prefix sums: seg_start[b] is the
-// first flattened block of sequence b, seg_start[batch] the total.
+// first flattened block of sequence b, seg_start[batch] the total.  Row b's
+// context length is ctx[b / csplit] (csplit > 1: rows are (sequence, KV head)
+// pairs of the per-head indexer).
 __device__ __forceinline__ void candidate_blocks(const int32_t* __restrict__ ctx, int batch, int max_ctx, int prefix,
-                                 int* seg_start, int* len, int* scratch) {
+                                 int* seg_start, int* len, int* scratch, int csplit = 1) {
   int carry = 0;
   for (int base = 0; base < batch; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int nb = 0;
     if (b < batch) {
-      const int L = min(__ldg(ctx + b), max_ctx);
+      const int L = min(__ldg(ctx + (csplit > 1 ? b / csplit : b)), max_ctx);
       len[b] = L;
       nb = L > prefix ? (L + kBlock - 1) / kBlock - prefix / kBlock : 0;
     }

@@ -407,12 +407,13 @@ dsa_status dsa_decode_step(const dsa_paged_kv* kv, const void* q, const int8_t* 
  *   scores        : int32 [batch * num_kv_heads][ld], ld >= max_context_len
  *   idx, n_sel    : int32 [batch][num_kv_heads][k] and [batch][num_kv_heads]
  * q / out / lse as in dsa_decode_step.  batch * num_kv_heads <= 2048.  The
- * workspace (dsa_heads_workspace_size bytes) holds a virtual block table of the
- * (sequence, head) pairs, their histograms and the attention partials.  The
- * scoring kernel of this call starts only after the previous work of the
- * stream has finished (its block ids come from the call's first kernel).  The
- * attention copies each selected row per KV head (256-byte K and V pieces)
- * instead of one piece per position.
+ * workspace (dsa_heads_workspace_size bytes) holds the histograms of the
+ * (sequence, head) pairs and the attention partials; the kernels map each pair
+ * onto its sequence's context length and block-table row themselves.  The same
+ * overlap with the previous kernel as dsa_decode_step (block tables, context
+ * lengths and the cache outside the newest positions must be complete before
+ * the call's first kernel starts).  The attention copies each selected row per
+ * KV head (256-byte K and V pieces) instead of one piece per position.
  * block_table_heads (device, or NULL): one block table per KV head, int32
  * [num_kv_heads][batch][max_blocks_per_seq], the tables of the per-(layer,
  * head) block bitmaps (dsa_kv_bitmap_*): head g then reads its positions'
