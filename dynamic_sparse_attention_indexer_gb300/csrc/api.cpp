@@ -699,6 +699,8 @@ dsa_status dsa_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t
   const void* d_dst = nullptr;
   DSA_TRY(staging_address(src, "src", &d_src));
   DSA_TRY(staging_address(dst, "dst", &d_dst));
+  if (!aligned16(d_src) || !aligned16(d_dst))
+    return fail(DSA_ERR_INVALID_ARG, "the device-side addresses of dst and src must be 16-byte aligned");
   const char* s0 = static_cast<const char*>(d_src);
   const char* d0 = static_cast<const char*>(d_dst);
   if (s0 < d0 + bytes && d0 < s0 + bytes) return fail(DSA_ERR_INVALID_ARG, "dst and src overlap");
