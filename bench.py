@@ -142,8 +142,8 @@ def heads_decode_line(spec, lens, n_sel_heads, ms, peak, peak_kind):
     rows = sum(min(P, L) + int(n) for L, ns in zip(lens, n_sel_heads) for n in ns)
     nbytes = idx_bytes + rows * 512 + 2 * len(lens) * hq * 128 * 2 + len(lens) * hkv * spec.k * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"kernel": "dsa_decode_step_heads per call in a graph: head_table_kernel + the scoring, selection and "
-                      "attention kernels over (sequence, KV head) rows", "ms": ms,
+    return {"kernel": "dsa_decode_step_heads per call in a graph: the scoring, selection, attention and merge "
+                      "kernels over (sequence, KV head) rows", "ms": ms,
             "tokens_per_s": len(lens) / (ms * 1e-3), "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
             "frac": gbs / peak, "algorithmic_bytes": nbytes, "peak_kind": peak_kind}
 
